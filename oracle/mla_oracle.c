@@ -1,0 +1,151 @@
+/*
+ * MLA decode oracle: the plain definition, in fp64, on the CPU.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this file; only the tests, the package smoke check and the CPU
+ * baseline leg of the benchmark do.  It shares no code, header, table or
+ * helper with the CUDA kernels.
+ *
+ * Sources (cited by page title and section):
+ *   [TL]  "用 TileLang 编写高性能 DeepSeek MLA 内核：从 FlashAttention 到
+ *          FlashMLA 级性能的完整实战指南" (lmnt.cn/news/253096)
+ *   [FM]  "DeepSeek开源周第一天：FlashMLA 深度分析" (pxiaoer.blog)
+ *
+ * What is computed (one query token per sequence, one shared latent KV head):
+ *   [TL §先看核心难点]  q and k rows are 576 wide: 512 latent + 64 RoPE;
+ *                       v is 512 wide.
+ *   [TL §Split Kernel]  the same cached tile feeds both the score GEMM and the
+ *                       value GEMM, so v = the first 512 columns of the cached
+ *                       row; the score is q_nope.k_nope + q_pe.k_pe, i.e. one
+ *                       dot product over all 576 columns.
+ *   [TL §参考实现与正确性验证]  the reference concatenates the two parts,
+ *                       takes einsum scores, a softmax, and the weighted sum
+ *                       of v.  That is what this file does, in fp64, without
+ *                       any tiling, splitting or exp2 rewriting.
+ *   [TL §变体内核], [FM §内存访问优化]  the cache is paged: token t of
+ *                       sequence b lives in physical page
+ *                       block_table[b][t / page_size], row t % page_size;
+ *                       tokens at or beyond cache_seqlens[b] do not exist.
+ *
+ * Readings where the pages are silent:
+ *   - lse is the natural-log log-sum-exp of the scaled scores,
+ *     lse = m + ln(sum_t exp(s_t - m)), m = max_t s_t  (the FlashAttention
+ *     convention; the kernels' base-2 internals convert to it).
+ *   - a sequence of length 0 gives out = 0 and lse = -inf.
+ *   - inputs are the bf16 / fp16 bit patterns exactly as stored; the oracle
+ *     widens them to double and rounds nothing afterwards (the kernels round
+ *     P to the input dtype; the parity tolerance absorbs that).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define MLA_D 576  /* q/k head dim: 512 latent + 64 RoPE */
+#define MLA_DV 512 /* v head dim: the latent part of the cached row */
+
+/* IEEE binary16 -> double, straight from the format's definition
+ * (1 sign bit, 5 exponent bits with bias 15, 10 fraction bits). */
+static double half_bits_to_double(uint16_t x) {
+  int sign = (x >> 15) & 1;
+  int e = (x >> 10) & 0x1f;
+  int f = x & 0x3ff;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)f, -24); /* subnormal: f * 2^-14 * 2^-10 */
+  } else if (e == 31) {
+    v = f ? NAN : INFINITY;
+  } else {
+    v = ldexp((double)(f | 0x400), e - 25); /* (1024+f) * 2^(e-15-10) */
+  }
+  return sign ? -v : v;
+}
+
+/* bfloat16 -> double: bf16 is the top half of an IEEE binary32. */
+static double bf16_bits_to_double(uint16_t x) {
+  uint32_t u = (uint32_t)x << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* dtype: 0 = fp16, 1 = bf16 */
+static double widen(uint16_t x, int dtype) {
+  return dtype == 1 ? bf16_bits_to_double(x) : half_bits_to_double(x);
+}
+
+/* Exported for the exhaustive conversion pin. */
+double oracle_widen(uint16_t x, int dtype) { return widen(x, dtype); }
+
+/*
+ * One (sequence, head) row of the definition.
+ *   q_row       : 576 stored values of this head's query
+ *   kv          : [num_pages][page_size][576] stored values
+ *   table_row   : this sequence's block_table row
+ *   out_row     : 512 doubles
+ *   scores      : scratch, at least seqlen doubles
+ * Returns 0, or -1 if the block table points outside the cache.
+ */
+static int one_row(const uint16_t *q_row, const uint16_t *kv, int64_t num_pages,
+                   int page_size, const int32_t *table_row, int seqlen,
+                   double softmax_scale, int dtype, double *out_row,
+                   double *lse_out, double *scores) {
+  for (int d = 0; d < MLA_DV; ++d) out_row[d] = 0.0;
+  if (seqlen <= 0) {
+    *lse_out = -INFINITY;
+    return 0;
+  }
+  /* s_t = scale * sum_c q[c] * k_t[c]  over all 576 columns */
+  double m = -INFINITY;
+  for (int t = 0; t < seqlen; ++t) {
+    int32_t page = table_row[t / page_size];
+    if (page < 0 || page >= num_pages) return -1;
+    const uint16_t *k = kv + ((int64_t)page * page_size + t % page_size) * MLA_D;
+    double dot = 0.0;
+    for (int c = 0; c < MLA_D; ++c) dot += widen(q_row[c], dtype) * widen(k[c], dtype);
+    scores[t] = softmax_scale * dot;
+    if (scores[t] > m) m = scores[t];
+  }
+  /* Z = sum_t exp(s_t - m);  out = sum_t exp(s_t - m) / Z * v_t */
+  double z = 0.0;
+  for (int t = 0; t < seqlen; ++t) z += exp(scores[t] - m);
+  for (int t = 0; t < seqlen; ++t) {
+    int32_t page = table_row[t / page_size];
+    const uint16_t *v = kv + ((int64_t)page * page_size + t % page_size) * MLA_D;
+    double p = exp(scores[t] - m) / z;
+    for (int d = 0; d < MLA_DV; ++d) out_row[d] += p * widen(v[d], dtype);
+  }
+  *lse_out = m + log(z);
+  return 0;
+}
+
+/*
+ * Selected rows of the MLA decode definition.
+ *   q            : [b][h][576] stored values (seqlen_q = 1 folded away)
+ *   kv           : [num_pages][page_size][576] stored values (one KV head)
+ *   block_table  : [b][max_blocks]
+ *   cache_seqlens: [b]
+ *   row_b, row_h : n_rows (sequence, head) pairs to evaluate
+ *   out          : [n_rows][512] doubles
+ *   lse          : [n_rows] doubles
+ *   scratch      : at least max(cache_seqlens) doubles
+ * Returns 0 on success, -1 on an out-of-range page or row index.
+ */
+int oracle_mla_decode_rows(int b, int h, const uint16_t *q, const uint16_t *kv,
+                           int64_t num_pages, int page_size,
+                           const int32_t *block_table, int max_blocks,
+                           const int32_t *cache_seqlens, double softmax_scale,
+                           int dtype, int n_rows, const int32_t *row_b,
+                           const int32_t *row_h, double *out, double *lse,
+                           double *scratch) {
+  for (int r = 0; r < n_rows; ++r) {
+    int bi = row_b[r], hi = row_h[r];
+    if (bi < 0 || bi >= b || hi < 0 || hi >= h) return -1;
+    int L = cache_seqlens[bi];
+    if (L > max_blocks * page_size) return -1;
+    int rc = one_row(q + ((int64_t)bi * h + hi) * MLA_D, kv, num_pages, page_size,
+                     block_table + (int64_t)bi * max_blocks, L, softmax_scale, dtype,
+                     out + (int64_t)r * MLA_DV, lse + r, scratch);
+    if (rc) return rc;
+  }
+  return 0;
+}

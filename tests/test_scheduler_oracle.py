@@ -1,0 +1,92 @@
+"""Pins for the scheduler oracle (the split-KV work partition is this project's design;
+what the pages fix is that it must cover every KV block exactly once, keep each
+sequence's splits contiguous and ordered, and balance work across the parts)."""
+import numpy as np
+import pytest
+
+from oracle import scheduler as sch
+
+FIXED = 5
+
+
+def check_partition(seqlens, parts, fixed):
+    meta, num_splits = sch.schedule(seqlens, parts, fixed)
+    b = len(seqlens)
+    assert len(meta) == parts and len(num_splits) == b + 1
+    assert num_splits[0] == 0 and all(x < y for x, y in zip(num_splits, num_splits[1:]))
+    covered = [np.zeros(sch.num_blocks(L), dtype=int) for L in seqlens]
+    touched = [0] * b
+    split_ids = []
+    prev_end = (0, 0)
+    costs = []
+    for row in meta:
+        assert (row[0], row[1]) == prev_end  # parts are contiguous and ordered
+        prev_end = (row[2], row[3])
+        cost = 0
+        for (i, lo, hi, sid) in sch.segments_of_part(row, seqlens):
+            assert 0 <= lo <= hi <= sch.num_blocks(seqlens[i])
+            assert lo < hi or sch.num_blocks(seqlens[i]) == 0
+            covered[i][lo:hi] += 1
+            touched[i] += 1
+            split_ids.append((sid, i, lo))
+            cost += hi - lo + fixed
+        costs.append(cost)
+    assert prev_end == (b, 0)
+    for i in range(b):
+        assert (covered[i] == 1).all()            # every block exactly once
+        assert touched[i] == num_splits[i + 1] - num_splits[i]
+    # split ids are 0..S-1 in (sequence, block) order, each sequence's ids contiguous
+    split_ids.sort()
+    assert [s for s, _, _ in split_ids] == list(range(num_splits[b]))
+    assert [(i, lo) for _, i, lo in split_ids] == sorted((i, lo) for _, i, lo in split_ids)
+    for s, i, _ in split_ids:
+        assert num_splits[i] <= s < num_splits[i + 1]
+    # balance: no part exceeds its share by more than a block plus two fixed costs
+    total = sum(sch.num_blocks(L) + fixed for L in seqlens)
+    assert max(costs) <= total / parts + 2 * fixed + 1
+    return meta, num_splits
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_partitions(seed):
+    rng = np.random.default_rng(seed)
+    b = int(rng.integers(1, 300))
+    kind = seed % 4
+    if kind == 0:
+        lens = rng.integers(0, 20000, size=b)
+    elif kind == 1:
+        lens = np.full(b, int(rng.integers(1, 9000)))
+    elif kind == 2:
+        lens = rng.integers(0, 130, size=b)
+    else:
+        lens = np.where(rng.random(b) < 0.3, 0, rng.integers(1, 70000, size=b))
+    parts = int(rng.integers(1, 160))
+    check_partition([int(x) for x in lens], parts, FIXED if seed % 5 else 0)
+
+
+def test_config_shapes():
+    # the paged / split / mqa decode workloads on 76 SM pairs
+    for b, L in ((64, 4096), (128, 8192), (256, 32768), (2, 256)):
+        meta, ns = check_partition([L] * b, 76, FIXED)
+    # one part: every sequence in one split (num_split = 1)
+    meta, ns = check_partition([4096] * 64, 1, FIXED)
+    assert ns == list(range(65))
+
+
+def test_more_parts_than_work():
+    meta, ns = check_partition([1, 0, 64], 150, FIXED)
+    assert ns[-1] >= 3
+
+
+def test_hand_example():
+    """Three sequences of 2, 0 and 3 blocks, F = 1, two parts: TOTAL = 8, cut at 4,
+    which lands in sequence 1's fixed cost... sequence 0 spans [0,3), 1 spans [3,4),
+    2 spans [4,8): position 4 is sequence 2's fixed unit -> cut (2, 0)."""
+    meta, ns = sch.schedule([128, 0, 150], 2, 1)
+    assert meta[0][:5] == [0, 0, 2, 0, 0]
+    assert meta[1][:5] == [2, 0, 3, 0, 2]
+    assert ns == [0, 1, 2, 3]
+    # with three parts: cuts at floor(8/3)=2 -> seq 0 block 1, floor(16/3)=5 -> seq 2 block 0
+    meta, ns = sch.schedule([128, 0, 150], 3, 1)
+    assert [m[:5] for m in meta] == [[0, 0, 0, 1, 0], [0, 1, 2, 0, 1], [2, 0, 3, 0, 3]]
+    assert ns == [0, 2, 3, 4]
