@@ -1,0 +1,215 @@
+/*
+ * mla_decode.h — C ABI of the GB300 (sm_103a) MLA decode library.
+ *
+ * DeepSeek Multi-Head Latent Attention, decode phase: one query token per
+ * sequence, h query heads sharing ONE latent KV head.  Query and key rows are
+ * 576 wide (512 latent + 64 RoPE); the value is the first 512 columns of the
+ * same cached row.  The cache is paged: 64-token-aligned pages addressed
+ * through a per-sequence block table.
+ *
+ * Sources (cited by page title and section):
+ *   [TL] "用 TileLang 编写高性能 DeepSeek MLA 内核：从 FlashAttention 到 FlashMLA
+ *        级性能的完整实战指南" (lmnt.cn/news/253096)
+ *   [FM] "DeepSeek开源周第一天：FlashMLA 深度分析" (pxiaoer.blog)
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     allocates no device memory and keeps no state between calls (apart from
+ *     a per-device error word and cached device properties).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; no entry point synchronises
+ *     except mla_get_device_error.
+ *   - Strides are in ELEMENTS.  Element types: q / kv_cache / out are fp16 or
+ *     bf16 (the same for all three); lse, the workspace are fp32; tables int32.
+ *   - Argument errors are detected on the host, before any launch, and return
+ *     a negative mla_status without touching the GPU.  Launch failures return
+ *     MLA_ERR_CUDA.  Faults the kernels detect while running (a block-table
+ *     entry outside the cache, a wait that ran out) are recorded in the
+ *     device error word and read back with mla_get_device_error.
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_ABI_VERSION 1
+
+/* Shape contract [TL §先看核心难点]: 576 = 512 latent + 64 RoPE; v = 512. */
+#define MLA_HEAD_DIM 576
+#define MLA_HEAD_DIM_V 512
+/* KV tokens per scheduling block (pages must be a multiple of it). */
+#define MLA_BLOCK_N 64
+/* Integers per part in tile_scheduler_metadata. */
+#define MLA_META_STRIDE 8
+/* Fixed per-split cost, in 64-token blocks, used by the scheduler. */
+#define MLA_SCHED_FIXED_COST 5
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_NULL = -1,            /* a required pointer is NULL */
+  MLA_ERR_SHAPE = -2,           /* unsupported or inconsistent dimension */
+  MLA_ERR_DTYPE = -3,           /* dtype is not fp16 / bf16 */
+  MLA_ERR_ALIGN = -4,           /* pointer or stride violates 16-byte alignment */
+  MLA_ERR_PAGE = -5,            /* page_block_size not a positive multiple of 64 */
+  MLA_ERR_WORKSPACE = -6,       /* workspace missing or too small */
+  MLA_ERR_CUDA = -7,            /* a CUDA runtime call or launch failed */
+  MLA_ERR_DEVICE_TIMEOUT = -8,  /* (device word) a bounded wait gave up */
+  MLA_ERR_DEVICE_BOUNDS = -9,   /* (device word) block table / length out of range */
+  MLA_ERR_ARCH = -10            /* the current device is not sm_103 */
+} mla_status;
+
+enum { MLA_DTYPE_FP16 = 0, MLA_DTYPE_BF16 = 1 };
+
+/*
+ * Arguments of one decode call.  Follows the field set of FlashMLA's
+ * Flash_fwd_mla_params [FM §内存访问优化]; fields for seqlen_q > 1 (is_causal,
+ * ngroups, h_h_k_ratio) are not part of this ABI.
+ *
+ * Tensors (device, caller-owned):
+ *   q            [b][1][h][576]        strides q_batch_stride, q_head_stride;
+ *                                      the 576 columns contiguous.
+ *   kv_cache     [num_pages][page_block_size][1][576]
+ *                                      strides kv_page_stride, kv_row_stride;
+ *                                      columns contiguous.  Token t of sequence
+ *                                      i is row t % page_block_size of page
+ *                                      block_table[i][t / page_block_size]
+ *                                      [TL §变体内核].
+ *   block_table  int32 [b][max_blocks_per_seq], row stride
+ *                block_table_batch_stride.  Only the first
+ *                ceil(L_i / page_block_size) entries of row i are read; each
+ *                must lie in [0, num_pages).
+ *   cache_seqlens int32 [b], 0 <= L_i <= max_blocks_per_seq*page_block_size.
+ *   out          [b][1][h][512]        strides o_batch_stride, o_head_stride.
+ *   lse          fp32 [b][h]           stride lse_batch_stride (heads
+ *                contiguous); natural-log log-sum-exp of the scaled scores,
+ *                -inf for an empty sequence (whose out row is all zeros).
+ *   tile_scheduler_metadata, num_splits: as written by mla_get_metadata for
+ *                the same cache_seqlens, b, h and num_sm.
+ *   workspace    at least mla_workspace_size(b, h, num_sm_parts) bytes, 16-byte
+ *                aligned; holds per-split partial outputs and their LSEs.
+ *
+ * Result: out[i][0][j][:] = sum_t softmax_t(s) * kv[t][0:512] with
+ * s_t = softmax_scale * q[i][0][j][:] . kv[t][:] over t < L_i, computed with
+ * exp2-based online softmax, split-KV partials and a combine pass
+ * [TL §Split Kernel, §Combine Kernel].  Accumulation is fp32; the softmax
+ * weights are rounded to the input dtype before the value product.
+ */
+typedef struct mla_fwd_params {
+  int32_t b;              /* sequences (>= 1) */
+  int32_t seqlen_q;       /* query tokens per sequence: must be 1 */
+  int32_t h;              /* query heads (1..1024) */
+  int32_t h_k;            /* KV heads: must be 1 */
+  int32_t d;              /* must be MLA_HEAD_DIM */
+  int32_t d_v;            /* must be MLA_HEAD_DIM_V */
+  int32_t dtype;          /* MLA_DTYPE_FP16 or MLA_DTYPE_BF16 */
+  float softmax_scale;    /* multiplies q.k before the softmax */
+
+  const void *q;
+  int64_t q_batch_stride, q_head_stride;
+
+  const void *kv_cache;
+  int64_t kv_page_stride, kv_row_stride;
+  int32_t num_pages;
+  int32_t page_block_size;
+
+  const int32_t *block_table;
+  int64_t block_table_batch_stride;
+  int32_t max_blocks_per_seq;
+
+  const int32_t *cache_seqlens;
+
+  void *out;
+  int64_t o_batch_stride, o_head_stride;
+  float *lse;
+  int64_t lse_batch_stride;
+
+  const int32_t *tile_scheduler_metadata;
+  const int32_t *num_splits;
+  int32_t num_sm_parts;
+
+  void *workspace;
+  size_t workspace_bytes;
+} mla_fwd_params;
+
+/* ABI version (MLA_ABI_VERSION) and sizeof(mla_fwd_params), for bindings. */
+int mla_abi_version(void);
+size_t mla_fwd_params_size(void);
+
+/* Static string for an mla_status value (never NULL). */
+const char *mla_status_string(int status);
+
+/*
+ * How many SMs the split kernel can occupy at once on `device`: twice the
+ * number of co-resident 2-CTA clusters of its launch configuration.  Pass it
+ * as num_sm below.  Returns MLA_ERR_CUDA / MLA_ERR_ARCH on failure.
+ */
+int mla_device_num_sm(int device, int *num_sm);
+
+/*
+ * Scheduler shape for b sequences and h heads on num_sm SMs (host only, no
+ * GPU needed): *num_sm_parts = max(1, (num_sm / 2) / ceil(h / 128)) parts (one
+ * 2-CTA cluster per part and 128-head tile), *meta_stride = MLA_META_STRIDE.
+ */
+int mla_metadata_shape(int b, int h, int num_sm, int *num_sm_parts, int *meta_stride);
+
+/*
+ * Tile-scheduler metadata [FM §内存访问优化: tile_scheduler_metadata_ptr,
+ * num_sm_parts, num_splits_ptr; TL §6. Split-KV: per-sequence split sizing
+ * from cache_seqlens].  One small device kernel, no host synchronisation.
+ *   cache_seqlens           device int32 [b]
+ *   tile_scheduler_metadata device int32 [num_sm_parts][MLA_META_STRIDE]:
+ *       {begin_seq, begin_blk, end_seq, end_blk, first_split, 0, 0, 0}; part k
+ *       covers the 64-token blocks from (begin_seq, begin_blk) up to, not
+ *       including, (end_seq, end_blk) in (sequence, block) order.
+ *   num_splits              device int32 [b + 1]: prefix sums; sequence i owns
+ *       split slots num_splits[i] .. num_splits[i+1]-1 of the workspace.
+ * Partition: sequences are laid end to end on a cost axis, each costing
+ * MLA_SCHED_FIXED_COST + ceil(L_i/64) blocks; part k starts at cost position
+ * floor(k*TOTAL/num_sm_parts).  Deterministic; the decode result does not
+ * depend on it beyond rounding.
+ */
+int mla_get_metadata(const int32_t *cache_seqlens, int b, int h, int num_sm,
+                     int32_t *tile_scheduler_metadata, int32_t *num_splits,
+                     void *stream);
+
+/* Workspace bytes for mla_decode_fwd: fp32 partial outputs and LSEs for up to
+ * b + num_sm_parts splits of h heads. */
+int mla_workspace_size(int b, int h, int num_sm_parts, size_t *bytes);
+
+/*
+ * Paged split-KV MLA decode [TL §Split Kernel, §Combine Kernel, §变体内核;
+ * FM §内存访问优化, §Softmax 计算优化].  Enqueues the split kernel (a
+ * persistent grid of 2-CTA clusters walking the metadata) and the combine
+ * kernel on `stream`.  Alignment: q, kv_cache, out, workspace 16-byte
+ * aligned; q/kv/out strides multiples of 8 elements.
+ */
+int mla_decode_fwd(const mla_fwd_params *params, void *stream);
+
+/*
+ * mla_decode_fwd plus a measurement hook: records the caller-owned CUDA events
+ * `split_begin` and `split_end` (cudaEvent_t as void*, either may be NULL) on
+ * `stream` immediately before and after the split kernel, so that its device
+ * time can be read with cudaEventElapsedTime.  Same results and errors as
+ * mla_decode_fwd.
+ */
+int mla_decode_fwd_timed(const mla_fwd_params *params, void *stream, void *split_begin,
+                         void *split_end);
+
+/*
+ * Synchronises `stream`, then returns (and clears) the device error word of
+ * the current device: MLA_OK, MLA_ERR_DEVICE_BOUNDS or MLA_ERR_DEVICE_TIMEOUT.
+ * If `detail` is non-NULL it receives a kernel-specific code (which wait, or
+ * the offending sequence index).
+ */
+int mla_get_device_error(void *stream, int *detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

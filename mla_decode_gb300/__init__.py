@@ -1,0 +1,288 @@
+"""GB300 (sm_103a) MLA decode: thin Python binding over the library's C ABI.
+
+Every function here has the name of the C entry point it wraps
+(include/mla_decode.h) and only marshals arguments: it checks tensor
+shapes/dtypes/devices, allocates caller-owned outputs with torch when they are
+not given, and passes raw device pointers plus the current CUDA stream.  All
+computation happens in the library's CUDA kernels.  If the compiled library is
+missing this module raises instead of falling back to anything else; build it
+with `python -m mla_decode_gb300._build` (or __graft_entry__.build()).
+"""
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "MlaError", "mla_abi_version", "mla_status_string", "mla_device_num_sm",
+    "mla_metadata_shape", "mla_get_metadata", "mla_workspace_size", "mla_decode_fwd",
+    "mla_decode_fwd_timed", "prepare_decode", "DecodeCall",
+    "mla_get_device_error", "library_path", "HEAD_DIM", "HEAD_DIM_V", "BLOCK_N",
+    "META_STRIDE", "SCHED_FIXED_COST",
+]
+
+HEAD_DIM = 576
+HEAD_DIM_V = 512
+BLOCK_N = 64
+META_STRIDE = 8
+SCHED_FIXED_COST = 5
+_DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1}
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        super().__init__(f"{what}: {mla_status_string(status)} ({status})")
+
+
+class FwdParams(ctypes.Structure):
+    """Mirror of `mla_fwd_params` (checked against the library's sizeof at load)."""
+    _fields_ = [
+        ("b", _i32), ("seqlen_q", _i32), ("h", _i32), ("h_k", _i32), ("d", _i32),
+        ("d_v", _i32), ("dtype", _i32), ("softmax_scale", ctypes.c_float),
+        ("q", _vp), ("q_batch_stride", _i64), ("q_head_stride", _i64),
+        ("kv_cache", _vp), ("kv_page_stride", _i64), ("kv_row_stride", _i64),
+        ("num_pages", _i32), ("page_block_size", _i32),
+        ("block_table", _vp), ("block_table_batch_stride", _i64), ("max_blocks_per_seq", _i32),
+        ("cache_seqlens", _vp),
+        ("out", _vp), ("o_batch_stride", _i64), ("o_head_stride", _i64),
+        ("lse", _vp), ("lse_batch_stride", _i64),
+        ("tile_scheduler_metadata", _vp), ("num_splits", _vp), ("num_sm_parts", _i32),
+        ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_lib = None
+
+
+def library_path():
+    return _build.LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise ImportError(
+            f"MLA decode library not built ({_build.LIB} missing); "
+            "run `python -m mla_decode_gb300._build`")
+    lib = ctypes.CDLL(_build.LIB)
+    lib.mla_abi_version.restype = ctypes.c_int
+    lib.mla_fwd_params_size.restype = ctypes.c_size_t
+    lib.mla_status_string.restype = ctypes.c_char_p
+    lib.mla_status_string.argtypes = [ctypes.c_int]
+    lib.mla_device_num_sm.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+    lib.mla_metadata_shape.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+    lib.mla_get_metadata.argtypes = [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp]
+    lib.mla_workspace_size.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.POINTER(ctypes.c_size_t)]
+    lib.mla_decode_fwd.argtypes = [ctypes.POINTER(FwdParams), _vp]
+    lib.mla_decode_fwd_timed.argtypes = [ctypes.POINTER(FwdParams), _vp, _vp, _vp]
+    lib.mla_get_device_error.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
+    for name in ("mla_device_num_sm", "mla_metadata_shape", "mla_get_metadata",
+                 "mla_workspace_size", "mla_decode_fwd", "mla_decode_fwd_timed",
+                 "mla_get_device_error"):
+        getattr(lib, name).restype = ctypes.c_int
+    if lib.mla_abi_version() != 1 or lib.mla_fwd_params_size() != ctypes.sizeof(FwdParams):
+        raise ImportError("MLA decode library ABI mismatch; rebuild it")
+    _lib = lib
+    return lib
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise MlaError(rc, what)
+
+
+def _stream(device):
+    return _vp(torch.cuda.current_stream(device).cuda_stream)
+
+
+def mla_abi_version():
+    return _load().mla_abi_version()
+
+
+def mla_status_string(status):
+    return _load().mla_status_string(int(status)).decode()
+
+
+def mla_device_num_sm(device=None):
+    """SMs the split kernel can occupy at once (2 x co-resident 2-CTA clusters)."""
+    dev = torch.cuda.current_device() if device is None else torch.device(device).index or 0
+    n = ctypes.c_int(0)
+    _check(_load().mla_device_num_sm(int(dev), ctypes.byref(n)), "mla_device_num_sm")
+    return n.value
+
+
+def mla_metadata_shape(b, h, num_sm):
+    parts, stride = ctypes.c_int(0), ctypes.c_int(0)
+    _check(_load().mla_metadata_shape(int(b), int(h), int(num_sm), ctypes.byref(parts),
+                                      ctypes.byref(stride)), "mla_metadata_shape")
+    return parts.value, stride.value
+
+
+def mla_get_metadata(cache_seqlens, h, num_sm=None, tile_scheduler_metadata=None,
+                     num_splits=None):
+    """Scheduler metadata for `cache_seqlens` (int32 [b], on the GPU).
+
+    Returns (tile_scheduler_metadata int32 [num_sm_parts, 8], num_splits int32 [b + 1]),
+    writing into the given tensors when they are passed.
+    """
+    if cache_seqlens.dtype != torch.int32 or not cache_seqlens.is_cuda or cache_seqlens.dim() != 1:
+        raise ValueError("cache_seqlens must be a CUDA int32 vector")
+    cache_seqlens = cache_seqlens.contiguous()
+    dev = cache_seqlens.device
+    if num_sm is None:
+        num_sm = mla_device_num_sm(dev)
+    b = cache_seqlens.numel()
+    parts, stride = mla_metadata_shape(b, h, num_sm)
+    meta = tile_scheduler_metadata
+    if meta is None:
+        meta = torch.empty((parts, stride), dtype=torch.int32, device=dev)
+    if num_splits is None:
+        num_splits = torch.empty((b + 1,), dtype=torch.int32, device=dev)
+    if (meta.shape != (parts, stride) or meta.dtype != torch.int32 or not meta.is_contiguous()
+            or num_splits.shape != (b + 1,) or num_splits.dtype != torch.int32
+            or not num_splits.is_contiguous()):
+        raise ValueError("metadata outputs have the wrong shape/dtype")
+    with torch.cuda.device(dev):
+        _check(_load().mla_get_metadata(_vp(cache_seqlens.data_ptr()), b, int(h), int(num_sm),
+                                        _vp(meta.data_ptr()), _vp(num_splits.data_ptr()),
+                                        _stream(dev)), "mla_get_metadata")
+    return meta, num_splits
+
+
+def mla_workspace_size(b, h, num_sm_parts):
+    n = ctypes.c_size_t(0)
+    _check(_load().mla_workspace_size(int(b), int(h), int(num_sm_parts), ctypes.byref(n)),
+           "mla_workspace_size")
+    return n.value
+
+
+def mla_decode_fwd(q, kv_cache, block_table, cache_seqlens, softmax_scale,
+                   tile_scheduler_metadata, num_splits, out=None, lse=None, workspace=None,
+                   split_events=None):
+    """Paged split-KV MLA decode (see prepare_decode for the argument contract).
+
+    split_events: optional (begin, end) torch.cuda.Event pair recorded around the
+    split kernel (mla_decode_fwd_timed).  Returns (out, lse).
+    """
+    call = prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
+                          tile_scheduler_metadata, num_splits, out, lse, workspace)
+    call(split_events=split_events)
+    return call.out, call.lse
+
+
+class DecodeCall:
+    """A validated, pre-marshalled mla_decode_fwd call (reusable: the tensors it
+    points at are kept alive by this object; re-run it after updating them in place)."""
+
+    def __init__(self, params, tensors, out, lse):
+        self.params = params
+        self._keep = tensors
+        self.out = out
+        self.lse = lse
+        self.device = out.device
+
+    def __call__(self, split_events=None):
+        lib = _load()
+        stream = _stream(self.device)
+        with torch.cuda.device(self.device):
+            if split_events is None:
+                rc = lib.mla_decode_fwd(ctypes.byref(self.params), stream)
+            else:
+                b, e = split_events
+                rc = lib.mla_decode_fwd_timed(ctypes.byref(self.params), stream,
+                                              _vp(b.cuda_event), _vp(e.cuda_event))
+        _check(rc, "mla_decode_fwd")
+        return self.out, self.lse
+
+
+def prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
+                   tile_scheduler_metadata, num_splits, out=None, lse=None, workspace=None):
+    """Paged split-KV MLA decode.
+
+    q [b, 1, h, 576], kv_cache [num_pages, page_size, 1, 576] (fp16 or bf16, same
+    dtype), block_table int32 [b, max_blocks], cache_seqlens int32 [b], metadata
+    from mla_get_metadata.  Returns (out [b, 1, h, 512] in q's dtype, lse fp32 [b, h]
+    natural-log).  Launches on the current stream of q's device.
+    """
+    if q.dim() != 4 or q.shape[1] != 1 or q.shape[3] != HEAD_DIM:
+        raise ValueError("q must be [b, 1, h, 576]")
+    if kv_cache.dim() != 4 or kv_cache.shape[2] != 1 or kv_cache.shape[3] != HEAD_DIM:
+        raise ValueError("kv_cache must be [num_pages, page_size, 1, 576]")
+    if q.dtype not in _DTYPE_CODE or kv_cache.dtype != q.dtype:
+        raise ValueError("q and kv_cache must share dtype fp16 or bf16")
+    for name, t in (("q", q), ("kv_cache", kv_cache), ("block_table", block_table),
+                    ("cache_seqlens", cache_seqlens), ("tile_scheduler_metadata",
+                                                       tile_scheduler_metadata),
+                    ("num_splits", num_splits)):
+        if not t.is_cuda or t.device != q.device:
+            raise ValueError(f"{name} must be on {q.device}")
+    if q.stride(3) != 1 or kv_cache.stride(3) != 1:
+        raise ValueError("the 576 columns of q and kv_cache must be contiguous")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be int32 [b, max_blocks] with unit column stride")
+    if cache_seqlens.dtype != torch.int32 or not cache_seqlens.is_contiguous():
+        raise ValueError("cache_seqlens must be a contiguous int32 vector")
+    b, _, h, _ = q.shape
+    if block_table.shape[0] != b or cache_seqlens.numel() != b or num_splits.numel() != b + 1:
+        raise ValueError("batch size mismatch among q, block_table, cache_seqlens, num_splits")
+    parts = tile_scheduler_metadata.shape[0]
+    dev = q.device
+    if out is None:
+        out = torch.empty((b, 1, h, HEAD_DIM_V), dtype=q.dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((b, h), dtype=torch.float32, device=dev)
+    if out.shape != (b, 1, h, HEAD_DIM_V) or out.dtype != q.dtype or out.stride(3) != 1:
+        raise ValueError("out must be [b, 1, h, 512] in q's dtype with contiguous columns")
+    if lse.shape != (b, h) or lse.dtype != torch.float32 or lse.stride(1) != 1:
+        raise ValueError("lse must be fp32 [b, h] with contiguous heads")
+    need = mla_workspace_size(b, h, parts)
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+
+    p = FwdParams()
+    p.b, p.seqlen_q, p.h, p.h_k, p.d, p.d_v = b, 1, h, 1, HEAD_DIM, HEAD_DIM_V
+    p.dtype = _DTYPE_CODE[q.dtype]
+    p.softmax_scale = float(softmax_scale)
+    p.q, p.q_batch_stride, p.q_head_stride = q.data_ptr(), q.stride(0), q.stride(2)
+    p.kv_cache = kv_cache.data_ptr()
+    p.kv_page_stride, p.kv_row_stride = kv_cache.stride(0), kv_cache.stride(1)
+    p.num_pages, p.page_block_size = kv_cache.shape[0], kv_cache.shape[1]
+    p.block_table = block_table.data_ptr()
+    p.block_table_batch_stride = block_table.stride(0)
+    p.max_blocks_per_seq = block_table.shape[1]
+    p.cache_seqlens = cache_seqlens.data_ptr()
+    p.out, p.o_batch_stride, p.o_head_stride = out.data_ptr(), out.stride(0), out.stride(2)
+    p.lse, p.lse_batch_stride = lse.data_ptr(), lse.stride(0)
+    p.tile_scheduler_metadata = tile_scheduler_metadata.data_ptr()
+    p.num_splits = num_splits.data_ptr()
+    p.num_sm_parts = parts
+    p.workspace = workspace.data_ptr()
+    p.workspace_bytes = workspace.numel() * workspace.element_size()
+    keep = (q, kv_cache, block_table, cache_seqlens, tile_scheduler_metadata, num_splits,
+            workspace)
+    return DecodeCall(p, keep, out, lse)
+
+
+def mla_decode_fwd_timed(*args, split_events, **kw):
+    """mla_decode_fwd with (begin, end) CUDA events recorded around the split kernel."""
+    return mla_decode_fwd(*args, split_events=split_events, **kw)
+
+
+def mla_get_device_error(device=None):
+    """Synchronise the current stream and return (status, detail) of the device error word."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    detail = ctypes.c_int(0)
+    with torch.cuda.device(dev):
+        rc = _load().mla_get_device_error(_stream(dev), ctypes.byref(detail))
+    return rc, detail.value

@@ -1,0 +1,83 @@
+// Split-KV combine kernel ("用 TileLang 编写高性能 DeepSeek MLA 内核…", section
+// Combine Kernel): for a sequence with S > 1 splits and each head,
+//   lse_max = max_k lse_k
+//   lse     = log2(sum_k 2^(lse_k - lse_max)) + lse_max
+//   out     = sum_k 2^(lse_k - lse) * O_k
+// with lse_k the base-2 LSE of split k (scale folded in) and O_k its
+// normalised partial output.  Sequences with one split were finished by the
+// split kernel and are skipped.
+//
+// Grid (b, ceil(h / 8)); one warp per head; lane j owns columns
+// 4j + 128c + {0..3}, c = 0..3, so every partial row is read as four fully
+// coalesced 512-byte warp loads.
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kWarps = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+combine_kernel(FwdArgs a) {
+  const int seq = blockIdx.x;
+  const int s0 = a.num_splits[seq];
+  const int n = a.num_splits[seq + 1] - s0;
+  if (n <= 1) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int head = blockIdx.y * kWarps + warp;
+  if (head >= a.h) return;
+
+  float mx = -INFINITY;
+  for (int k = lane; k < n; k += 32) mx = fmaxf(mx, a.lseaccum[(int64_t)(s0 + k) * a.h + head]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float mref = (mx == -INFINITY) ? 0.f : mx;
+  float sum = 0.f;
+  for (int k = lane; k < n; k += 32) sum += fast_exp2(a.lseaccum[(int64_t)(s0 + k) * a.h + head] - mref);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float lse = sum > 0.f ? fast_log2(sum) + mref : -INFINITY;
+
+  float4 acc[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < n; ++k) {
+    const int64_t sp = (int64_t)(s0 + k) * a.h + head;
+    const float w = (lse == -INFINITY) ? 0.f : fast_exp2(a.lseaccum[sp] - lse);
+    const float4 *src = reinterpret_cast<const float4 *>(a.oaccum + sp * MLA_HEAD_DIM_V);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float4 v = src[lane + 32 * c];
+      acc[c].x = fmaf(w, v.x, acc[c].x);
+      acc[c].y = fmaf(w, v.y, acc[c].y);
+      acc[c].z = fmaf(w, v.z, acc[c].z);
+      acc[c].w = fmaf(w, v.w, acc[c].w);
+    }
+  }
+  T *o = reinterpret_cast<T *>(a.out) + seq * a.o_batch_stride + (int64_t)head * a.o_head_stride;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int d = 4 * lane + 128 * c;
+    o[d + 0] = Elem<T>::from_f(acc[c].x);
+    o[d + 1] = Elem<T>::from_f(acc[c].y);
+    o[d + 2] = Elem<T>::from_f(acc[c].z);
+    o[d + 3] = Elem<T>::from_f(acc[c].w);
+  }
+  if (lane == 0) a.lse[seq * a.lse_stride + head] = lse * kLn2;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const FwdArgs &a, cudaStream_t s) {
+  dim3 grid(a.b, (a.h + kWarps - 1) / kWarps);
+  if (a.dtype == MLA_DTYPE_BF16)
+    combine_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, s>>>(a);
+  else
+    combine_kernel<__half><<<grid, kWarps * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,50 @@
+// Internal declarations shared by the library's translation units (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mla_decode.h"
+
+namespace mla {
+
+// Everything a split / combine kernel needs, resolved and validated on the host.
+struct FwdArgs {
+  int b, h, dtype;
+  float scale_log2;  // softmax_scale * log2(e): scores are kept in base-2 units
+  const void *q;
+  int64_t q_batch_stride, q_head_stride;
+  const void *kv;
+  int64_t kv_page_stride, kv_row_stride;
+  int num_pages, page_size;
+  const int32_t *block_table;
+  int64_t bt_stride;
+  int max_blocks;
+  const int32_t *seqlens;
+  void *out;
+  int64_t o_batch_stride, o_head_stride;
+  float *lse;
+  int64_t lse_stride;
+  const int32_t *meta;
+  const int32_t *num_splits;
+  int num_parts;
+  float *oaccum;    // [max_splits][h][512]
+  float *lseaccum;  // [max_splits][h], base-2 units
+  int max_splits;
+  int *err;         // device error word (two ints: code, detail)
+};
+
+int max_splits_for(int b, int num_parts);
+size_t workspace_bytes_for(int b, int h, int num_parts);
+
+// device error word of the current device
+int *device_error_word();
+
+cudaError_t launch_metadata(const int32_t *seqlens, int b, int parts, int fixed,
+                            int32_t *meta, int32_t *num_splits, cudaStream_t s);
+cudaError_t launch_split(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_split_simt(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_combine(const FwdArgs &a, cudaStream_t s);
+cudaError_t split_num_sm(int device, int *num_sm);
+
+}  // namespace mla

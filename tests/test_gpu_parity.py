@@ -1,0 +1,137 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same
+seeded inputs, element by element, plus scheduler bit-exactness and device-side
+error reporting."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import scheduler as sch
+from tests import _parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from mla_decode_gb300 import _build
+    _build.build()
+    import mla_decode_gb300 as mla
+    mla._load()
+
+
+def test_tiny_config_full():
+    w = workloads.get("tiny")
+    stats, *_ = P.check_workload(w)
+    assert stats["out_max_abs"] < P.OUT_MAX_ABS
+
+
+SMALL = [
+    dict(batch=3, heads=128, seqlens=(1, 64, 1000), dtype="bf16"),
+    dict(batch=2, heads=16, seqlens=(65, 4097), dtype="fp16"),
+    dict(batch=4, heads=100, seqlens=(0, 63, 129, 700), dtype="bf16", page_size=128),
+    dict(batch=1, heads=1, seqlens=(300,), dtype="bf16"),
+    dict(batch=5, heads=130, seqlens=(2, 5000, 191, 64, 1), dtype="fp16", page_size=256),
+    dict(batch=2, heads=128, seqlens=(8192, 0), dtype="bf16", shuffle=False),
+    dict(batch=3, heads=64, seqlens=(3000, 2999, 1), dtype="bf16", softmax_scale=1.0),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_small_cases(case):
+    kw = dict(SMALL[case])
+    w = workloads.custom(name=f"small{case}", seed=100 + case, **kw)
+    P.check_workload(w)
+
+
+@pytest.mark.parametrize("num_sm", [2, 6, 20, 64, None])
+def test_split_invariance(num_sm):
+    w = workloads.custom(4, 128, (3000, 50, 5000, 777), "bf16", seed=7, name="splits")
+    inputs = workloads.make_inputs(w, "cuda")
+    stats, out, lse, meta, ns, _ = P.check_workload(w, num_sm=num_sm, inputs=inputs)
+    base_o, base_l, *_ = P.run_gpu(inputs, w.heads, w.softmax_scale, num_sm=2)  # one split each
+    d = (out.float() - base_o.float()).abs().max().item()
+    assert d <= P.OUT_MAX_ABS
+    assert (lse - base_l).abs().max().item() <= P.LSE_MAX_ABS
+
+
+def test_poisoned_tail_rows_are_never_read():
+    w = workloads.custom(3, 128, (70, 130, 5), "bf16", seed=9, name="poison")
+    P.check_workload(w, poison_tail=True)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_metadata_bit_exact(seed):
+    import mla_decode_gb300 as mla
+    rng = np.random.default_rng(seed)
+    b = int(rng.integers(1, 400))
+    lens = np.where(rng.random(b) < 0.1, 0, rng.integers(1, 40000, size=b)).astype(np.int32)
+    num_sm = int(rng.integers(1, 400))
+    h = int(rng.choice([1, 16, 128, 200]))
+    meta, ns = mla.mla_get_metadata(torch.from_numpy(lens).cuda(), h, num_sm)
+    parts, _ = mla.mla_metadata_shape(b, h, num_sm)
+    ref_meta, ref_ns = sch.schedule([int(x) for x in lens], parts, mla.SCHED_FIXED_COST)
+    assert meta.cpu().tolist() == ref_meta
+    assert ns.cpu().tolist() == ref_ns
+
+
+def test_out_of_range_page_is_reported_and_gpu_stays_usable():
+    import mla_decode_gb300 as mla
+    w = workloads.custom(2, 16, (100, 100), "bf16", seed=3, name="bounds")
+    inputs = workloads.make_inputs(w, "cuda")
+    bad = dict(inputs)
+    bt = inputs["block_table"].clone()
+    bt[1, 1] = w.num_pages + 1000
+    bad["block_table"] = bt
+    meta, ns = mla.mla_get_metadata(bad["cache_seqlens"], w.heads)
+    mla.mla_decode_fwd(bad["q"], bad["kv_cache"], bad["block_table"], bad["cache_seqlens"],
+                       w.softmax_scale, meta, ns)
+    code, detail = mla.mla_get_device_error()
+    assert code == mla_status("MLA_ERR_DEVICE_BOUNDS") and detail == 1
+    # the context is intact: a correct call afterwards passes parity
+    P.check_workload(w, inputs=inputs)
+
+
+def mla_status(name):
+    return {"MLA_ERR_DEVICE_BOUNDS": -9, "MLA_ERR_DEVICE_TIMEOUT": -8}[name]
+
+
+# --- the pages' workloads at full size (sampled sequences, all heads) -------------------
+
+def test_paged_config_full_size():
+    w = workloads.get("paged")
+    P.check_workload(w, seqs=workloads.sample_seqs(w, 12))
+
+
+def test_split_config_full_size_split_vs_unsplit():
+    import mla_decode_gb300 as mla
+    w = workloads.get("split")
+    seqs = workloads.sample_seqs(w, 8)
+    inputs = workloads.make_inputs(w, "cuda")
+    ref_o, ref_l = P.oracle_rows(w, inputs, seqs)
+    idx = torch.as_tensor(seqs, device="cuda")
+    results = {}
+    for label, num_sm in (("default", None), ("many", 1024), ("one", 2)):
+        out, lse, meta, ns = P.run_gpu(inputs, w.heads, w.softmax_scale, num_sm)
+        per_seq = (ns[1:] - ns[:-1]).cpu()
+        if label == "many":
+            assert int(per_seq.min()) >= 4   # at least four splits per sequence
+        if label == "one":
+            assert int(per_seq.max()) == 1   # num_split = 1
+        P.compare(out[idx, 0], lse[idx], ref_o, ref_l, what=f"split/{label}")
+        results[label] = (out, lse)
+    for label in ("default", "many"):
+        assert (results[label][0].float() - results["one"][0].float()).abs().max().item() <= P.OUT_MAX_ABS
+        assert (results[label][1] - results["one"][1]).abs().max().item() <= P.LSE_MAX_ABS
+    del mla
+
+
+def test_varlen_config_full_size():
+    w = workloads.get("varlen")
+    seqs = sorted(set(workloads.sample_seqs(w, 10)) | {0, 1, 3})  # len 1, 2, 63 included
+    P.check_workload(w, seqs=seqs)
+
+
+def test_mqa_config_full_size():
+    w = workloads.get("mqa")
+    P.check_workload(w, seqs=workloads.sample_seqs(w, 6))
