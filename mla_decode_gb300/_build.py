@@ -47,6 +47,7 @@ def build(verbose=False, force=False, ptxas_verbose=False):
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    extra += os.environ.get("MLA_NVCC_FLAGS", "").split()
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")

@@ -36,6 +36,10 @@ int *device_error_word() {
 
 int max_splits_for(int b, int num_parts) { return b + num_parts; }
 
+cudaError_t launch_split(const FwdArgs &a, cudaStream_t s) { return launch_split_tc(a, s); }
+
+cudaError_t split_num_sm(int device, int *num_sm) { return split_tc_num_sm(device, num_sm); }
+
 size_t workspace_bytes_for(int b, int h, int num_parts) {
   size_t splits = (size_t)max_splits_for(b, num_parts);
   size_t o = splits * (size_t)h * MLA_HEAD_DIM_V * sizeof(float);

@@ -44,6 +44,8 @@ cudaError_t launch_metadata(const int32_t *seqlens, int b, int parts, int fixed,
                             int32_t *meta, int32_t *num_splits, cudaStream_t s);
 cudaError_t launch_split(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_split_simt(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_split_tc(const FwdArgs &a, cudaStream_t s);
+cudaError_t split_tc_num_sm(int device, int *num_sm);
 cudaError_t launch_combine(const FwdArgs &a, cudaStream_t s);
 cudaError_t split_num_sm(int device, int *num_sm);
 

@@ -189,12 +189,3 @@ cudaError_t launch_split_simt(const FwdArgs &a, cudaStream_t s) {
 
 }  // namespace mla
 
-namespace mla {
-
-cudaError_t launch_split(const FwdArgs &a, cudaStream_t s) { return launch_split_simt(a, s); }
-
-cudaError_t split_num_sm(int device, int *num_sm) {
-  return cudaDeviceGetAttribute(num_sm, cudaDevAttrMultiProcessorCount, device);
-}
-
-}  // namespace mla
