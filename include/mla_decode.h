@@ -201,6 +201,42 @@ int mla_decode_fwd_timed(const mla_fwd_params *params, void *stream, void *split
                          void *split_end);
 
 /*
+ * Size of the library's built-in per-device scratch used by
+ * mla_decode_fwd_static: 64 MiB, enough for b + num_sm_parts <= 255 at h = 128
+ * (b = 128 with 76 parts needs 53.6 MB; see mla_workspace_size).
+ */
+#define MLA_STATIC_WORKSPACE_BYTES (64u << 20)
+
+/*
+ * mla_decode_fwd with no caller workspace and no allocation of any kind.  The
+ * source pages have no counterpart: their decode always receives a workspace
+ * tensor from the caller.  This entry is for callers that cannot allocate
+ * device memory on the decode path: plain C hosts with no device allocator of
+ * their own, and runtimes that reserve all device memory up front, for whom a
+ * cudaMalloc/cudaFree per step (each of which synchronises the device) would
+ * stall the stream.
+ *
+ * The split kernel's partial outputs and log-sum-exps go to a fixed array of
+ * MLA_STATIC_WORKSPACE_BYTES inside the library, one per device, held from
+ * the library's first use on that device until the process exits.
+ * params->workspace and params->workspace_bytes are ignored; every other field
+ * means what it means for mla_decode_fwd, and so do the results and errors.
+ * If mla_workspace_size(b, h, num_sm_parts) exceeds
+ * MLA_STATIC_WORKSPACE_BYTES, the call returns MLA_ERR_WORKSPACE before
+ * touching the device (MLA_ERR_SHAPE if b, h or num_sm_parts is out of range).
+ *
+ * The first call on a device, made with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and caches it; make that first
+ * call before any stream capture.  Nothing in the array has to start at zero:
+ * every partial the combine kernel reads was written by the split kernel
+ * earlier in the same call, so what an earlier call left there is never read.
+ * All calls on a device share the one array, so calls that overlap on the GPU
+ * (on different streams, or unordered calls from several host threads) race
+ * on it and give wrong results: order them on one stream or with events.
+ */
+int mla_decode_fwd_static(const mla_fwd_params *params, void *stream);
+
+/*
  * Synchronises `stream`, then returns (and clears) the device error word of
  * the current device: MLA_OK, MLA_ERR_DEVICE_BOUNDS or MLA_ERR_DEVICE_TIMEOUT.
  * If `detail` is non-NULL it receives a kernel-specific code (which wait, or

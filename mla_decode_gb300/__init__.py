@@ -28,6 +28,7 @@ HEAD_DIM_V = 512
 BLOCK_N = 64
 META_STRIDE = 8
 SCHED_FIXED_COST = 5
+STATIC_WORKSPACE_BYTES = 64 << 20
 _DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1}
 
 _vp = ctypes.c_void_p
@@ -86,6 +87,7 @@ def _load():
                                        ctypes.POINTER(ctypes.c_size_t)]
     lib.mla_decode_fwd.argtypes = [ctypes.POINTER(FwdParams), _vp]
     lib.mla_decode_fwd_timed.argtypes = [ctypes.POINTER(FwdParams), _vp, _vp, _vp]
+    lib.mla_decode_fwd_static.argtypes = [ctypes.POINTER(FwdParams), _vp]
     lib.mla_get_device_error.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
     for name in ("mla_device_num_sm", "mla_metadata_shape", "mla_get_metadata",
                  "mla_workspace_size", "mla_decode_fwd", "mla_decode_fwd_timed",
@@ -277,6 +279,21 @@ def prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
 def mla_decode_fwd_timed(*args, split_events, **kw):
     """mla_decode_fwd with (begin, end) CUDA events recorded around the split kernel."""
     return mla_decode_fwd(*args, split_events=split_events, **kw)
+
+
+def mla_decode_fwd_static(q, kv_cache, block_table, cache_seqlens, softmax_scale,
+                          tile_scheduler_metadata, num_splits, out=None, lse=None):
+    """mla_decode_fwd with the library's built-in per-device scratch
+    (STATIC_WORKSPACE_BYTES) in place of a workspace tensor: the C call allocates
+    nothing.  Calls on one device must not overlap on the GPU.  Returns (out, lse)."""
+    no_ws = torch.empty((0,), dtype=torch.uint8, device=q.device)
+    call = prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
+                          tile_scheduler_metadata, num_splits, out, lse, no_ws)
+    lib = _load()
+    with torch.cuda.device(call.device):
+        rc = lib.mla_decode_fwd_static(ctypes.byref(call.params), _stream(call.device))
+    _check(rc, "mla_decode_fwd_static")
+    return call.out, call.lse
 
 
 def mla_get_device_error(device=None):

@@ -12,11 +12,19 @@ namespace mla {
 // Device error word: {code, detail}.  One instance per device context.
 __device__ int g_error_word[2];
 
+// Scratch for mla_decode_fwd_static: oaccum and lseaccum of one call.  One
+// instance per device context; never cleared (nothing in it is read before the
+// same call writes it).  Host code must not pass this name to a kernel: it
+// stands for the array only on the device; static_workspace() gives the
+// device address.
+static __device__ __align__(256) unsigned char g_static_workspace[MLA_STATIC_WORKSPACE_BYTES];
+
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int *g_err_ptr[kMaxDevices] = {nullptr};
 int g_num_sm[kMaxDevices] = {0};
+void *g_static_ws_ptr[kMaxDevices] = {nullptr};
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int head_tiles(int h) { return (h + 127) / 128; }
@@ -32,6 +40,19 @@ int *device_error_word() {
     g_err_ptr[dev] = static_cast<int *>(p);
   }
   return g_err_ptr[dev];
+}
+
+// Device address of g_static_workspace on the current device, looked up once.
+void *static_workspace() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_static_ws_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess) return nullptr;
+    g_static_ws_ptr[dev] = p;
+  }
+  return g_static_ws_ptr[dev];
 }
 
 int max_splits_for(int b, int num_parts) { return b + num_parts; }
@@ -125,6 +146,19 @@ int mla_workspace_size(int b, int h, int num_sm_parts, size_t *bytes) {
 
 int mla_decode_fwd(const mla_fwd_params *p, void *stream) {
   return mla_decode_fwd_timed(p, stream, nullptr, nullptr);
+}
+
+int mla_decode_fwd_static(const mla_fwd_params *p, void *stream) {
+  if (!p) return MLA_ERR_NULL;
+  if (p->b < 1 || p->h < 1 || p->h > 1024 || p->num_sm_parts < 1) return MLA_ERR_SHAPE;
+  if (workspace_bytes_for(p->b, p->h, p->num_sm_parts) > (size_t)MLA_STATIC_WORKSPACE_BYTES)
+    return MLA_ERR_WORKSPACE;
+  void *ws = static_workspace();
+  if (!ws) return MLA_ERR_CUDA;
+  mla_fwd_params with_ws = *p;
+  with_ws.workspace = ws;
+  with_ws.workspace_bytes = MLA_STATIC_WORKSPACE_BYTES;
+  return mla_decode_fwd(&with_ws, stream);
 }
 
 int mla_decode_fwd_timed(const mla_fwd_params *p, void *stream, void *split_begin,
