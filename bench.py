@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (smaller cases for profiler captures)")
     return ap.parse_args()
 
 
@@ -227,6 +229,8 @@ def run_reference(args):
         return 0
     import workloads
     w = workloads.get(args.config)
+    if args.batch is not None:
+        w = workloads.get(args.config, batch=args.batch, seqlens=tuple(w.seqlens[:1]) * args.batch)
     cores = os.cpu_count() or 1
     # one step = the oracle on one whole sequence (all heads) of the workload; the
     # sequence is trimmed if needed so that warmup+steps stay within ~2 minutes.
@@ -287,6 +291,8 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = workloads.get(args.config)
+    if args.batch is not None:
+        w = workloads.get(args.config, batch=args.batch, seqlens=tuple(w.seqlens[:1]) * args.batch)
 
     # ---- inputs: `copies` sets that differ in where their KV cache lives
     base = workloads.make_inputs(w, dev)

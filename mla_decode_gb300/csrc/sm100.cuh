@@ -273,11 +273,26 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
       : "memory");
 }
 
+// Same, for a barrier given by its shared-memory address.
+__device__ __forceinline__ void mma_commit_addr(uint32_t bar_addr) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar_addr)
+      : "memory");
+}
+
 // Same, arriving on the mbarrier at this offset in every CTA of `cta_mask`.
 __device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_multicast_addr(uint32_t bar_addr, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar_addr),
       "h"(cta_mask)
       : "memory");
 }

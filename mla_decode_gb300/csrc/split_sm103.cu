@@ -15,19 +15,23 @@
 // part is served by a cluster of two CTAs with different roles:
 //   * score CTA (cluster rank 0): Q columns 0..511 live in TMEM as the A operand
 //     (packed 16-bit pairs), the RoPE columns 512..575 in shared memory.  For a
-//     superblock of up to four 64-token pages it issues S = Q K^T as 36 MMAs of
-//     M=128 x N=256 x K=16 into a TMEM accumulator, streaming K through a ring of
-//     [256 tokens x 64 columns] TMA tiles.  Eight softmax warps read S, keep the
-//     running max with a lazy rescale (the reference max only moves when a block
-//     exceeds it by more than kTau in log2 units, which is exact in real
-//     arithmetic), write P as 16-bit swizzled tiles and bulk-copy them, with the
-//     per-head rescale factors, into the value CTA's shared memory.
-//   * value CTA (rank 1): O lives in TMEM (two 256-column halves).  Its own TMA
-//     stream brings each page's 512 value columns; per page and O half it issues
-//     M=128 x N=256 x K=16 MMAs with P (shared memory, K-major) as A and V
-//     (shared memory, N-major) as B.  Eight correction warps apply the rescale
-//     factors to O when the score CTA moved its reference max, and run the
-//     epilogue (O / l to out, or to the split workspace).
+//     superblock of up to two 64-token pages it issues S = Q K^T as 36 MMAs of
+//     M=128 x N=128 x K=16 into one of two TMEM accumulators (so the MMAs of one
+//     superblock overlap the softmax of the previous one), streaming K through a
+//     ring of [128 tokens x 64 columns] TMA tiles.  Eight softmax warps (one
+//     64-token page each per head row) keep the running max with a lazy rescale
+//     (the reference max only moves when a block exceeds it by more than kTau in
+//     log2 units, which is exact in real arithmetic), write P as 16-bit swizzled
+//     tiles into a double-buffered staging area, and a copier warp bulk-copies
+//     them, with the per-head rescale factors, into the value CTA.
+//   * value CTA (rank 1): O lives in TMEM as two 256-column halves.  Its own TMA
+//     stream brings each page's value columns; for each superblock it issues all
+//     M=128 x N=256 x K=16 MMAs of half 0 (P from shared memory, K-major, as A;
+//     V from shared memory, N-major, as B), then those of half 1.  Two groups of
+//     four correction warps, one per half, rescale their half of O when the
+//     score CTA moved its reference max, so one half is rescaled while the
+//     other half's MMAs still run, and write the epilogue (O / l to out, or to
+//     the split workspace).
 // Every wait is bounded; a wait that runs out records MLA_ERR_DEVICE_TIMEOUT
 // with the wait site as detail, and the CTA unwinds.
 #include <cuda.h>
@@ -45,19 +49,27 @@ namespace {
 using namespace sm100;
 
 constexpr int kThreads = 352;            // 11 warps (see the role map in the kernel)
-constexpr int kSB = 4;                   // pages (64 tokens each) per score superblock
-constexpr int kNK = 4;                   // K tiles in flight (score CTA)
+constexpr int kSB = 2;                   // pages (64 tokens each) per superblock
+constexpr int kSBTok = 64 * kSB;         // tokens per superblock: N of the score MMAs
+#ifndef MLA_NK
+#define MLA_NK 8
+#endif
+constexpr int kNK = MLA_NK;              // K tiles in flight (score CTA)
 #ifndef MLA_NV
-#define MLA_NV 5
+#define MLA_NV 4
 #endif
 constexpr int kNV = MLA_NV;              // V half-page tiles in flight (value CTA)
-constexpr int kNPR = 3;                  // P tiles in the value CTA's ring
+#ifndef MLA_NPR
+#define MLA_NPR 4
+#endif
+constexpr int kNPR = MLA_NPR;            // P tiles in the value CTA's ring
+constexpr int kStages = 2;               // P staging buffers in the score CTA
 #ifndef MLA_TAU
 #define MLA_TAU 0.0f
 #endif
 constexpr float kTau = MLA_TAU;          // lazy-rescale threshold, log2 units
 constexpr int kChunk = 8192;             // [64 rows][128 B] swizzled TMA box
-constexpr int kKSlot = kSB * kChunk;     // 64 columns of 256 tokens
+constexpr int kKSlot = kSB * kChunk;     // 64 columns of one superblock's tokens
 constexpr int kVSlot = 4 * kChunk;       // 256 value columns of one page
 constexpr int kPTile = 16384;            // [128 heads][64 tokens] 16-bit, swizzled
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -66,36 +78,37 @@ struct Header {  // score -> value CTA, one per superblock
   float alpha[128];
   float l[128];
   float m[128];
-  uint32_t flags;  // bit 0: rescale O first; bit 1: last superblock of the segment
+  uint32_t flags;  // bit 1: last superblock of the segment
   uint32_t pad[3];
 };
 static_assert(sizeof(Header) % 16 == 0, "bulk copies move multiples of 16 bytes");
 
 // shared-memory map (offsets from the 1024-aligned base)
-constexpr int kOffQ8 = 0;                                   // score: Q columns 512..575
-constexpr int kOffK = kOffQ8 + 16384;                       // score: K ring
-constexpr int kOffPStage = kOffK + kNK * kKSlot;            // score: P staging tiles
-constexpr int kOffHdrStage = kOffPStage + kSB * kPTile;     // score: 2 staging headers
-constexpr int kOffRed = kOffHdrStage + 2 * (int)sizeof(Header);  // score: [2][2][128] floats
-constexpr int kOffV = 0;                                    // value: V ring
-constexpr int kOffPRing = kOffV + kNV * kVSlot;             // value: P tiles
-constexpr int kOffHdr = kOffPRing + kNPR * kPTile;          // value: 2 headers
-constexpr int kOffBars = (((kOffRed + 4 * 128 * 4) > (kOffHdr + 2 * (int)sizeof(Header))
-                               ? (kOffRed + 4 * 128 * 4)
-                               : (kOffHdr + 2 * (int)sizeof(Header))) + 127) & ~127;
-static_assert(kOffHdr + 2 * (int)sizeof(Header) <= kOffBars, "value layout overlaps barriers");
+constexpr int kOffQ8 = 0;                                     // score: Q columns 512..575
+constexpr int kOffK = kOffQ8 + 16384;                         // score: K ring
+constexpr int kOffPStage = kOffK + kNK * kKSlot;              // score: P staging tiles
+constexpr int kOffHdrStage = kOffPStage + kStages * kSB * kPTile;  // score: 2 headers
+constexpr int kOffRed = kOffHdrStage + 2 * (int)sizeof(Header);    // score: [2][2][128] floats
+constexpr int kScoreEnd = kOffRed + 4 * 128 * 4;
+constexpr int kOffV = 0;                                      // value: V ring
+constexpr int kOffPRing = kOffV + kNV * kVSlot;               // value: P tiles
+constexpr int kOffHdr = kOffPRing + kNPR * kPTile;            // value: 2 headers
+constexpr int kValueEnd = kOffHdr + 2 * (int)sizeof(Header);
+constexpr int kOffBars = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 127) & ~127;
 
 struct Bars {
-  uint64_t k_full[kNK], k_empty[kNK];  // score
-  uint64_t s_full, s_free, q_ready;    // score
-  uint64_t stage_ready;                // score: P tiles + header staged (softmax -> copier)
-  uint64_t stage_free[kSB];            // score, arrived by the value CTA
-  uint64_t slot_free[kNPR];            // score, value-CTA MMA commits (multicast)
-  uint64_t hdr_free[2];                // score, arrived by the value CTA
-  uint64_t v_full[kNV], v_empty[kNV];  // value
-  uint64_t p_full[kNPR];               // value, bulk copies from the score CTA
-  uint64_t hdr_full[2];                // value, bulk copies from the score CTA
-  uint64_t o_ready[2], o_done[2], o_free;  // value
+  uint64_t k_full[kNK], k_empty[kNK];   // score
+  uint64_t s_full[2], s_free[2];        // score, per S buffer
+  uint64_t q_ready;                     // score
+  uint64_t stage_ready[kStages];        // score: P tiles + header staged (softmax -> copier)
+  uint64_t stage_free[kStages * kSB];   // score, arrived by the value CTA
+  uint64_t slot_free[kNPR];             // score, value-CTA MMA commits (multicast)
+  uint64_t hdr_free[2];                 // score, arrived by the value CTA (both groups)
+  uint64_t v_full[kNV], v_empty[kNV];   // value
+  uint64_t p_full[kNPR];                // value, bulk copies from the score CTA
+  uint64_t hdr_full[2];                 // value, bulk copies from the score CTA
+  uint64_t o_ready[2][2], o_done[2][2]; // value, [O half][superblock parity]
+  uint64_t o_free;                      // value
   uint32_t tmem_base;
   int abort;
 };
@@ -108,43 +121,31 @@ enum : int {
   W_V_EMPTY, W_O_FREE, W_O_READY, W_P_FULL, W_V_FULL, W_HDR_FULL, W_O_DONE, W_STAGE_READY
 };
 
-// Optional event trace of part 0 (build with -DMLA_TRACE=1): globaltimer stamps
-// per (role, superblock, event), read back with mla_debug_trace().
-#if MLA_TRACE
-__device__ unsigned long long g_trace[2][256][16];
-__device__ unsigned long long g_trace_k[2][256][16];  // per K chunk: [0..8] arrival, [9..] reuse
-__device__ unsigned long long g_trace_v[256][16];     // value CTA per page p: p_full, v_full h0/h1, V issue
-__device__ unsigned long long g_parts[1024][4];        // per part: start, score end, value end, segments
-#define TRACE_V(part, sb, ev)                                                     \
-  do {                                                                            \
-    if ((part) == 0 && (sb) < 256) g_trace_v[(sb)][(ev)] = globaltimer_ns();      \
-  } while (0)
-#define TRACE_K(role, part, sb, ev)                                                   \
-  do {                                                                                \
-    if ((part) == 0 && (sb) < 256) g_trace_k[(role)][(sb)][(ev)] = globaltimer_ns(); \
-  } while (0)
-#define TRACE(role, part, sb, ev)                                             \
-  do {                                                                        \
-    if ((part) == 0 && (sb) < 256) g_trace[(role)][(sb)][(ev)] = globaltimer_ns(); \
-  } while (0)
+// Optional wait profile (build with -DMLA_WAIT_PROFILE=1): per part, CTA, warp
+// and wait site (or timed phase), the time lane 0 spent there, plus each warp's
+// role start and end; read back with mla_debug_wait_profile().
+#if MLA_WAIT_PROFILE
+constexpr int kProfParts = 128, kProfSites = 32;
+__device__ unsigned long long g_wait_ns[kProfParts][2][kThreads / 32][kProfSites];
+__device__ unsigned long long g_role_ns[kProfParts][2][kThreads / 32][2];
+// (SM clock cycles: cheap to read, and every interval is taken on one SM)
+__device__ __forceinline__ uint64_t prof_now() { return clock64(); }
+__device__ __forceinline__ void prof_wait(int where, uint64_t t0) {
+  const int part = blockIdx.x >> 1;
+  if ((threadIdx.x & 31) == 0 && blockIdx.y == 0 && part < kProfParts && where < kProfSites)
+    atomicAdd(&g_wait_ns[part][blockIdx.x & 1][threadIdx.x >> 5][where],
+              (unsigned long long)(clock64() - t0));
+}
+__device__ __forceinline__ void prof_role(int which) {
+  const int part = blockIdx.x >> 1;
+  if ((threadIdx.x & 31) == 0 && blockIdx.y == 0 && part < kProfParts)
+    g_role_ns[part][blockIdx.x & 1][threadIdx.x >> 5][which] = clock64();
+}
 #else
-#define TRACE(role, part, sb, ev) \
-  do {                            \
-  } while (0)
-#define TRACE_K(role, part, sb, ev) \
-  do {                              \
-  } while (0)
-#define TRACE_V(part, sb, ev) \
-  do {                        \
-  } while (0)
+__device__ __forceinline__ uint64_t prof_now() { return 0; }
+__device__ __forceinline__ void prof_wait(int, uint64_t) {}
+__device__ __forceinline__ void prof_role(int) {}
 #endif
-
-#ifndef MLA_LINE_PREFETCH_SB
-#define MLA_LINE_PREFETCH_SB 0
-#endif
-// The value CTA's correction warps prefetch, line by line into L2, the cache rows
-// of the superblock this many superblocks ahead of the one they are handling.
-constexpr int kLinePrefetchSb = MLA_LINE_PREFETCH_SB;
 
 struct Ctx {
   Bars *bars;
@@ -152,10 +153,13 @@ struct Ctx {
   __device__ bool aborted() const { return *reinterpret_cast<volatile int *>(&bars->abort) != 0; }
 };
 
+// Bounded wait on an mbarrier phase.  The fast path (the phase already
+// completed) is one try_wait inline; the spin, its time limit and the abort
+// protocol live out of line so that issue loops stay short.  On timeout the
+// CTA and its peer are flagged to unwind and MLA_ERR_DEVICE_TIMEOUT is
+// recorded with the wait site.
 template <bool kCl>
-__device__ __forceinline__ bool wait_bar(const Ctx &c, uint64_t *bar, uint32_t parity, int where) {
-  const uint32_t addr = smem_u32(bar);
-  if (kCl ? mbar_try_wait_cluster(addr, parity) : mbar_try_wait(addr, parity)) return true;
+__device__ __noinline__ bool wait_bar_slow(const Ctx &c, uint32_t addr, uint32_t parity, int where) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
@@ -169,6 +173,25 @@ __device__ __forceinline__ bool wait_bar(const Ctx &c, uint64_t *bar, uint32_t p
       return false;
     }
   }
+}
+
+template <bool kCl>
+__device__ __forceinline__ bool wait_addr(const Ctx &c, uint32_t addr, uint32_t parity, int where) {
+#if MLA_WAIT_PROFILE
+  const uint64_t tp = prof_now();
+  const bool ok = (kCl ? mbar_try_wait_cluster(addr, parity) : mbar_try_wait(addr, parity)) ||
+                  wait_bar_slow<kCl>(c, addr, parity, where);
+  prof_wait(where, tp);
+  return ok;
+#else
+  if (kCl ? mbar_try_wait_cluster(addr, parity) : mbar_try_wait(addr, parity)) return true;
+  return wait_bar_slow<kCl>(c, addr, parity, where);
+#endif
+}
+
+template <bool kCl>
+__device__ __forceinline__ bool wait_bar(const Ctx &c, uint64_t *bar, uint32_t parity, int where) {
+  return wait_addr<kCl>(c, smem_u32(bar), parity, where);
 }
 
 // One sequence's share of a part: blocks [lo, hi) of sequence `seq`.
@@ -186,7 +209,7 @@ struct SegWalk {
     end_blk = row[3];
     split = row[4];
   }
-  __device__ __forceinline__ bool next(const FwdArgs &a, Seg &s) {
+  __device__ __noinline__ bool next(const FwdArgs &a, Seg &s) {
     if (!(seq < end_seq || (seq == end_seq && blk < end_blk))) return false;
     int L = a.seqlens[seq];
     const int cap = a.max_blocks * a.page_size;
@@ -216,14 +239,14 @@ struct TileUse {
   uint32_t par = 0, used = 0;
   __device__ __forceinline__ uint32_t parity(int t) const { return (par >> t) & 1u; }
   __device__ __forceinline__ bool was_used(int t) const { return (used >> t) & 1u; }
-  __device__ __forceinline__ void advance(int np) {
-    const uint32_t m = (1u << np) - 1u;
+  __device__ __forceinline__ void advance(int first, int n) {
+    const uint32_t m = ((1u << n) - 1u) << first;
     par ^= m;
     used |= m;
   }
 };
 
-// Physical pages and first rows of the (up to four) pages of a superblock.  The
+// Physical pages and first rows of the (up to kSB) pages of a superblock.  The
 // block-table loads are issued early (issue) and only consumed later (finish):
 // issued right before use they would queue behind this SM's in-flight TMA traffic
 // for microseconds.  Out-of-range entries are reported and clamped to page 0.
@@ -232,13 +255,19 @@ struct SbPages {
 };
 __device__ __forceinline__ void issue_sb_pages(const FwdArgs &a, int seq, int blk0, int np,
                                                SbPages &r) {
+  const int tok0 = blk0 << 6;
+  int lb = tok0 / a.page_size;
+  int row = tok0 - lb * a.page_size;
 #pragma unroll
   for (int p = 0; p < kSB; ++p) {
-    const int tok0 = (blk0 + p) << 6;
-    const int lb = tok0 / a.page_size;
-    r.row0[p] = tok0 - lb * a.page_size;
+    r.row0[p] = row;
     r.page[p] = (p < np && lb < a.max_blocks) ? a.block_table[(int64_t)seq * a.bt_stride + lb]
                                               : (p < np ? -1 : 0);
+    row += 64;
+    if (row == a.page_size) {
+      row = 0;
+      ++lb;
+    }
   }
 }
 __device__ __forceinline__ void finish_sb_pages(const FwdArgs &a, int seq, int np, SbPages &r) {
@@ -316,23 +345,15 @@ template <typename T>
 __device__ void score_producer(const FwdArgs &a, const CUtensorMap *map, uint8_t *smem,
                                const Ctx &c, int part) {
   Bars *b = c.bars;
-  uint32_t kc = 0, tsb = 0;
-  // two superblock jobs in flight: the block-table loads of job j + 2 are issued
-  // while job j's chunks are being loaded
+  uint32_t kc = 0;
   SbWalk w(a, part);
-  SbJob ja, jb;
-  bool ha = w.more, hb = false;
-  if (ha) issue_job(a, w, ja);
-  hb = w.more;
-  if (hb) issue_job(a, w, jb);
+  SbJob cur{}, nxt{};
+  bool hc = false, hn = false;
   auto run = [&](SbJob &j) -> bool {
-    TRACE(0, part, tsb, 8);
     finish_sb_pages(a, j.seq, j.np, j.pg);
-    TRACE(0, part, tsb, 10);
     for (int ch = 0; ch < 9; ++ch, ++kc) {
       const uint32_t slot = kc % kNK, use = kc / kNK;
       if (use > 0 && !wait_bar<false>(c, &b->k_empty[slot], (use - 1) & 1, W_K_EMPTY)) return false;
-      TRACE_K(1, part, tsb, ch);  // issue time of K chunk ch
       mbar_arrive_expect_tx(&b->k_full[slot], j.np * kChunk);
       uint8_t *dst = smem + kOffK + slot * kKSlot;
 #pragma unroll
@@ -340,28 +361,36 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *map, uint8_t
         if (p < j.np)
           tma_load_3d(dst + p * kChunk, map, &b->k_full[slot], 64 * ch, j.pg.row0[p], j.pg.page[p]);
     }
-    TRACE(0, part, tsb, 9);
-    ++tsb;
     return true;
   };
-  while (ha) {
-    if (!run(ja)) return;
-    ha = w.more;
-    if (ha) issue_job(a, w, ja);
-    if (!hb) break;
-    if (!run(jb)) return;
-    hb = w.more;
-    if (hb) issue_job(a, w, jb);
+  // one superblock of block-table lookahead: job j + 1's loads are issued
+  // before job j's tiles are requested
+  while (true) {
+    cur = nxt;
+    hc = hn;
+    hn = w.more;
+    if (hn) issue_job(a, w, nxt);
+    if (!hc) {
+      if (!hn) break;
+      continue;
+    }
+    if (!run(cur)) return;
   }
 }
 
+// The issue loop is kept short (slot and phase counters, descriptors advanced by
+// adding offsets): with N = 128 one MMA takes 64 tensor-core cycles, and a
+// single thread must issue the next one within that time.
 template <typename T>
 __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int part, uint32_t tmem) {
   Bars *b = c.bars;
-  const uint32_t tQ = tmem, tS = tmem + 256;
-  const uint32_t idesc = idesc_f16(128, 256, Pack<T>::kBf16, false, false);
-  const uint32_t q8 = smem_u32(smem + kOffQ8);
-  uint32_t kc = 0, sb = 0, segn = 0;
+  const uint32_t tQ = tmem;
+  const uint32_t idesc = idesc_f16(128, kSBTok, Pack<T>::kBf16, false, false);
+  const uint64_t qdesc = desc_kmajor_sw128(smem_u32(smem + kOffQ8));
+  const uint64_t kdesc = desc_kmajor_sw128(smem_u32(smem + kOffK));
+  const uint32_t kfull = smem_u32(&b->k_full[0]), kempty = smem_u32(&b->k_empty[0]);
+  uint32_t slot = 0, phase = 0;  // K ring position of the next chunk and its k_full parity
+  uint32_t sb = 0, segn = 0;
   SegWalk walk(a, part);
   Seg s;
   while (walk.next(a, s)) {
@@ -369,31 +398,31 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
     if (!wait_bar<false>(c, &b->q_ready, segn & 1, W_Q_READY)) return;
     tc_fence_after();
     for (int sb0 = s.lo; sb0 < s.hi; sb0 += kSB, ++sb) {
-      if (sb > 0) {
-        if (!wait_bar<false>(c, &b->s_free, (sb - 1) & 1, W_S_FREE)) return;
+      const uint32_t buf = sb & 1;
+      if (sb >= 2) {  // the softmax has read this buffer's previous superblock
+        if (!wait_bar<false>(c, &b->s_free[buf], ((sb >> 1) - 1) & 1, W_S_FREE)) return;
         tc_fence_after();
       }
-      TRACE(0, part, sb, 0);
-      for (int ch = 0; ch < 9; ++ch, ++kc) {
-        const uint32_t slot = kc % kNK, use = kc / kNK;
-        if (!wait_bar<false>(c, &b->k_full[slot], use & 1, W_K_FULL)) return;
+      const uint32_t tS = tmem + 256 + kSBTok * buf;
+#pragma unroll 1
+      for (int ch = 0; ch < 9; ++ch) {
+        if (!wait_addr<false>(c, kfull + 8 * slot, phase, W_K_FULL)) return;
         tc_fence_after();
-        if (ch == 0) TRACE(0, part, sb, 1);
-        TRACE_K(0, part, sb, ch);
-        const uint32_t kb = smem_u32(smem + kOffK + slot * kKSlot);
+        const uint64_t bd = kdesc + (uint64_t)(slot * (kKSlot >> 4));
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint64_t bd = desc_kmajor_sw128(kb + 32 * k);
           if (ch < 8)
-            mma_ts(tS, tQ + 32 * ch + 8 * k, bd, idesc, (ch | k) != 0);
+            mma_ts(tS, tQ + 32 * ch + 8 * k, bd + 2 * k, idesc, (ch | k) != 0);
           else
-            mma_ss(tS, desc_kmajor_sw128(q8 + 32 * k), bd, idesc, 1);
+            mma_ss(tS, qdesc + 2 * k, bd + 2 * k, idesc, 1);
         }
-        mma_commit(&b->k_empty[slot]);
-        if (ch == 5) TRACE(0, part, sb, 11);
+        mma_commit_addr(kempty + 8 * slot);
+        if (++slot == kNK) {
+          slot = 0;
+          phase ^= 1u;
+        }
       }
-      mma_commit(&b->s_full);
-      TRACE(0, part, sb, 2);
+      mma_commit(&b->s_full[buf]);
     }
     ++segn;
   }
@@ -409,26 +438,73 @@ __device__ void score_copier(const FwdArgs &a, uint8_t *smem, const Ctx &c, int 
   const uint32_t peer_hfull = map_to_rank(smem_u32(&b->hdr_full[0]), 1);
   uint32_t pc = 0;  // P tiles shipped so far (ring slot pc % kNPR)
   uint32_t sb = 0;
-  SegWalk walk(a, part);
-  Seg s;
-  while (walk.next(a, s)) {
-    for (int sb0 = s.lo; sb0 < s.hi; sb0 += kSB, ++sb) {
-      const int np = min(kSB, s.hi - sb0);
-      if (!wait_bar<false>(c, &b->stage_ready, sb & 1, W_STAGE_READY)) return;
-      // the header first: the value CTA can prepare O for this superblock while it
-      // is still consuming the previous one's tiles
-      const int hs = sb & 1;
-      bulk_copy_to_peer(peer_hdr + hs * sizeof(Header), smem + kOffHdrStage + hs * sizeof(Header),
-                        sizeof(Header), peer_hfull + hs * 8);
-      for (int p = 0; p < np; ++p, ++pc) {
-        const uint32_t r = pc % kNPR, use = pc / kNPR;
-        if (use > 0 && !wait_bar<true>(c, &b->slot_free[r], (use - 1) & 1, W_SLOT_FREE)) return;
-        bulk_copy_to_peer(peer_pring + r * kPTile, smem + kOffPStage + p * kPTile, kPTile,
-                          peer_pfull + r * 8);
+  SbWalk w(a, part);
+  while (w.more) {
+    const int np = min(kSB, w.s.hi - w.sb0);
+    const uint32_t buf = sb & 1;
+    if (!wait_bar<false>(c, &b->stage_ready[buf], (sb >> 1) & 1, W_STAGE_READY)) return;
+    // the header first: the value CTA can prepare O for this superblock while it
+    // is still consuming the previous one's tiles
+    bulk_copy_to_peer(peer_hdr + buf * sizeof(Header), smem + kOffHdrStage + buf * sizeof(Header),
+                      sizeof(Header), peer_hfull + buf * 8);
+    for (int t = 0; t < np; ++t, ++pc) {
+      const uint32_t r = pc % kNPR, use = pc / kNPR;
+      if (use > 0 && !wait_bar<true>(c, &b->slot_free[r], (use - 1) & 1, W_SLOT_FREE)) return;
+      bulk_copy_to_peer(peer_pring + r * kPTile, smem + kOffPStage + (buf * kSB + t) * kPTile,
+                        kPTile, peer_pfull + r * 8);
+    }
+    w.advance(a);
+    ++sb;
+  }
+}
+
+// Q row `head` of sequence `seq` for one softmax thread: its half of columns
+// 0..511 into TMEM (A operand layout: 16-bit pairs per 32-bit column), and for
+// the second half's threads columns 512..575 into the swizzled Q8 tile.  Once
+// per segment, so out of line.
+template <typename T>
+__device__ __noinline__ void load_q(const FwdArgs &a, uint8_t *smem, int seq, int head, bool head_ok,
+                                    int half, int r, uint32_t tQ) {
+  const T *q = reinterpret_cast<const T *>(a.q);
+  const uint4 *src = reinterpret_cast<const uint4 *>(q + (int64_t)seq * a.q_batch_stride +
+                                                     (int64_t)head * a.q_head_stride);
+#pragma unroll 1
+  for (int bt = 0; bt < 2; ++bt) {  // 16 loads in flight, then 64 TMEM columns
+    uint4 qv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) qv[i] = head_ok ? src[32 * half + 16 * bt + i] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      uint32_t w[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        w[4 * i + 0] = qv[8 * cc + i].x;
+        w[4 * i + 1] = qv[8 * cc + i].y;
+        w[4 * i + 2] = qv[8 * cc + i].z;
+        w[4 * i + 3] = qv[8 * cc + i].w;
       }
-      TRACE(0, part, sb, 7);
+      tmem_st32(tQ + 32 * (4 * half + 2 * bt + cc), w);
     }
   }
+  if (half == 1) {
+    const uint32_t row = smem_u32(smem + kOffQ8) + r * 128;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint4 v = head_ok ? src[64 + i] : make_uint4(0, 0, 0, 0);
+      st_shared_v4(row + ((i ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
+    }
+  }
+  tmem_wait_st();
+  fence_proxy_async_smem();
+  tc_fence_before();
+}
+
+template <typename T>
+__device__ __noinline__ void prefetch_q_row(const FwdArgs &a, int seq, int head, int half) {
+  const char *row = reinterpret_cast<const char *>(reinterpret_cast<const T *>(a.q) +
+                                                   (int64_t)seq * a.q_batch_stride +
+                                                   (int64_t)head * a.q_head_stride);
+  for (int ln = half; ln < 9; ln += 2) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 128 * ln));
 }
 
 template <typename T>
@@ -438,19 +514,18 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sw = warp - 2;             // 0..7
   const int quad = warp & 3;           // TMEM lane quadrant this warp may touch
-  const int half = sw >> 2;            // column half of S
+  const int half = sw >> 2;            // page of the superblock (64 S columns)
   const int r = 32 * quad + lane;      // head row within the tile
   const int head = head0 + r;
   const bool head_ok = head < a.h;
   const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
-  const uint32_t tQ = tmem + lane_off, tS = tmem + 256 + lane_off;
+  const uint32_t tQ = tmem + lane_off;
+  const uint32_t tS = tmem + 256 + lane_off + 64 * half;
   float *red_max = reinterpret_cast<float *>(smem + kOffRed);  // [2][128]
   float *red_sum = red_max + 256;                               // [2][128]
-  const T *q = reinterpret_cast<const T *>(a.q);
-
   const float scale = a.scale_log2;
   uint32_t sb = 0;
-  TileUse tu;
+  TileUse tu;  // staging tile buf * kSB + t
   SegWalk walk(a, part);
   Seg s;
   while (walk.next(a, s)) {
@@ -463,33 +538,14 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
     }
     // ---- Q of this sequence: columns 0..511 into TMEM, 512..575 into shared memory
     {
-      const uint4 *src = reinterpret_cast<const uint4 *>(
-          q + (int64_t)s.seq * a.q_batch_stride + (int64_t)(head_ok ? head : head0) * a.q_head_stride);
-      const int c0 = half * 4;
-      for (int ch = c0; ch < c0 + 4; ++ch) {
-        uint32_t w[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint4 v = head_ok ? src[ch * 8 + i] : make_uint4(0, 0, 0, 0);
-          w[4 * i + 0] = v.x;
-          w[4 * i + 1] = v.y;
-          w[4 * i + 2] = v.z;
-          w[4 * i + 3] = v.w;
-        }
-        tmem_st32(tQ + 32 * ch, w);
-      }
-      if (half == 1) {
-        const uint32_t row = smem_u32(smem + kOffQ8) + r * 128;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint4 v = head_ok ? src[64 + i] : make_uint4(0, 0, 0, 0);
-          st_shared_v4(row + ((i ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
-        }
-      }
-      tmem_wait_st();
-      fence_proxy_async_smem();
-      tc_fence_before();
+      const uint64_t tq = prof_now();
+      load_q<T>(a, smem, s.seq, head_ok ? head : head0, head_ok, half, r, tQ);
       mbar_arrive(&b->q_ready);
+      // bring the next segment's Q rows into L2 while this segment runs
+      SegWalk nx = walk;
+      Seg s2;
+      if (head_ok && nx.next(a, s2)) prefetch_q_row<T>(a, s2.seq, head, half);
+      prof_wait(23, tq);
     }
 
     float m_ref = -INFINITY, l = 0.f;
@@ -498,78 +554,83 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       const int sb0 = s.lo + j * kSB;
       const int np = min(kSB, s.hi - sb0);
       const bool last = j == nsb - 1;
-      bool ok = wait_bar<false>(c, &b->s_full, sb & 1, W_S_FULL);
-      if (sw == 0 && lane == 0) TRACE(0, part, sb, 3);
+      const uint32_t buf = sb & 1;
+      bool ok = wait_bar<false>(c, &b->s_full[buf], (sb >> 1) & 1, W_S_FULL);
       tc_fence_after();
-      uint32_t v[4][32];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) tmem_ld32(tS + 128 * half + 32 * i, v[i]);
+      uint64_t tp = prof_now();
+      uint32_t v[2][32];
+      tmem_ld32(tS + kSBTok * buf, v[0]);
+      tmem_ld32(tS + kSBTok * buf + 32, v[1]);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&b->s_free);
+      mbar_arrive(&b->s_free[buf]);
+      prof_wait(19, tp);
+      tp = prof_now();
 
-      // scale to base-2 units and mask tokens past the sequence / superblock
-      // (the valid columns of a superblock are a prefix of length min(64 np, L - 64 sb0))
-      const int lim = min(np << 6, s.L - (sb0 << 6)) - 128 * half;
+      // base-2 units; tokens past the sequence end (a suffix of my page) and a page
+      // past the segment end (all of it) become -inf after the scale
+      const int lim = half < np ? min(64, s.L - ((sb0 + half) << 6)) : 0;
+      float sc = scale;
+      if (lim < 64) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            v[i][e] = __float_as_uint(32 * i + e < lim ? __uint_as_float(v[i][e]) * scale : -INFINITY);
+        sc = 1.f;
+      }
       float mloc = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 2; ++i)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float x = (32 * i + e < lim) ? __uint_as_float(v[i][e]) * scale : -INFINITY;
-          v[i][e] = __float_as_uint(x);
-          mloc = fmaxf(mloc, x);
-        }
-      }
+        for (int e = 0; e < 32; ++e) mloc = fmaxf(mloc, __uint_as_float(v[i][e]) * sc);
       red_max[half * 128 + r] = mloc;
+      prof_wait(20, tp);
+      tp = prof_now();
       if (bar_red_or(1, 256, !ok || c.aborted())) return;  // all softmax threads leave together
-      if (sw == 0 && lane == 0) TRACE(0, part, sb, 4);
+      prof_wait(17, tp);
       const float m_blk = fmaxf(red_max[r], red_max[128 + r]);
       float alpha = 1.f;
-      bool resc = false;
       if (m_blk > m_ref + kTau) {  // also the first block (m_ref = -inf)
         alpha = fast_exp2(m_ref - m_blk);
         m_ref = m_blk;
-        resc = true;
       }
-      // my two staging tiles must have left for the value CTA
-#pragma unroll
-      for (int t2 = 0; t2 < 2; ++t2) {
-        const int t = 2 * half + t2;
-        if (ok && t < np && tu.was_used(t))
-          ok = wait_bar<true>(c, &b->stage_free[t], tu.parity(t) ^ 1u, W_STAGE_FREE);
-      }
+      // my staging tile must have left for the value CTA
+      const int tb = buf * kSB + half;
+      if (ok && half < np && tu.was_used(tb))
+        ok = wait_bar<true>(c, &b->stage_free[tb], tu.parity(tb) ^ 1u, W_STAGE_FREE);
+      tp = prof_now();
       float psum = 0.f;
+      const bool write = ok && half < np;
+      const uint32_t row = smem_u32(smem + kOffPStage + tb * kPTile) + r * 128;
+      const float nm = -m_ref;
 #pragma unroll
-      for (int t2 = 0; t2 < 2; ++t2) {
-        const int t = 2 * half + t2;
-        const bool write = t < np && ok;
-        const uint32_t row = smem_u32(smem + kOffPStage + t * kPTile) + r * 128;
+      for (int ch = 0; ch < 8; ++ch) {
+        float p[8];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          float p[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            p[e] = fast_exp2(__uint_as_float(v[2 * t2 + (ch >> 2)][(ch & 3) * 8 + e]) - m_ref);
-            psum += p[e];
-          }
-          if (write)
-            st_shared_v4(row + ((ch ^ (r & 7)) << 4), Pack<T>::two(p[0], p[1]),
-                         Pack<T>::two(p[2], p[3]), Pack<T>::two(p[4], p[5]),
-                         Pack<T>::two(p[6], p[7]));
+        for (int e = 0; e < 8; ++e) {
+          p[e] = fast_exp2(fmaf(__uint_as_float(v[ch >> 2][(ch & 3) * 8 + e]), sc, nm));
+          psum += p[e];
         }
+        if (write)
+          st_shared_v4(row + ((ch ^ (r & 7)) << 4), Pack<T>::two(p[0], p[1]),
+                       Pack<T>::two(p[2], p[3]), Pack<T>::two(p[4], p[5]),
+                       Pack<T>::two(p[6], p[7]));
       }
       red_sum[half * 128 + r] = psum;
-      if (sw == 0 && lane == 0) TRACE(0, part, sb, 5);
+      prof_wait(21, tp);
       const int hs = sb & 1;
       Header *hdr = reinterpret_cast<Header *>(smem + kOffHdrStage + hs * sizeof(Header));
       if (ok && half == 0 && sb >= 2)
         ok = wait_bar<true>(c, &b->hdr_free[hs], ((sb >> 1) - 1) & 1, W_HDR_FREE);
-      const bool any_resc = bar_red_or(1, 256, resc);
+      tp = prof_now();
       if (bar_red_or(1, 256, !ok || c.aborted())) return;
+      prof_wait(18, tp);
+      tp = prof_now();
       l = l * alpha + (red_sum[r] + red_sum[128 + r]);
       if (half == 0) {
-        hdr->alpha[r] = alpha;
+        // the first superblock of a segment overwrites O: nothing to rescale
+        hdr->alpha[r] = j == 0 ? 1.f : alpha;
         if (last) {
           hdr->l[r] = l;
           hdr->m[r] = m_ref;
@@ -580,11 +641,11 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
           }
         }
       }
-      if (sw == 0 && lane == 0) hdr->flags = ((any_resc && j > 0) ? 1u : 0u) | (last ? 2u : 0u);
+      if (sw == 0 && lane == 0) hdr->flags = last ? 2u : 0u;
       fence_proxy_async_smem();
-      mbar_arrive(&b->stage_ready);  // the copier thread ships the tiles and the header
-      if (sw == 0 && lane == 0) TRACE(0, part, sb, 6);
-      tu.advance(np);
+      mbar_arrive(&b->stage_ready[buf]);  // the copier ships the tiles and the header
+      prof_wait(22, tp);
+      tu.advance(buf * kSB, np);
     }
   }
 }
@@ -595,145 +656,119 @@ template <typename T>
 __device__ void value_producer(const FwdArgs &a, const CUtensorMap *map, uint8_t *smem,
                                const Ctx &c, int part) {
   Bars *b = c.bars;
-  uint32_t vc = 0, tsb = 0;
+  uint32_t vc = 0;
   SbWalk w(a, part);
-  SbJob ja, jb;
-  bool ha = w.more, hb = false;
-  if (ha) issue_job(a, w, ja);
-  hb = w.more;
-  if (hb) issue_job(a, w, jb);
+  SbJob cur{}, nxt{};
+  bool hc = false, hn = false;
+  // the MMA warp's order: all pages' O-half-0 columns, then all pages' half-1 columns
   auto run = [&](SbJob &j) -> bool {
-    TRACE(1, part, tsb, 8);
     finish_sb_pages(a, j.seq, j.np, j.pg);
+    for (int g = 0; g < 2; ++g) {
 #pragma unroll
-    for (int p = 0; p < kSB; ++p) {
-      if (p >= j.np) break;
-      for (int hv = 0; hv < 2; ++hv, ++vc) {
+      for (int p = 0; p < kSB; ++p) {
+        if (p >= j.np) break;
         const uint32_t slot = vc % kNV, use = vc / kNV;
+        ++vc;
         if (use > 0 && !wait_bar<false>(c, &b->v_empty[slot], (use - 1) & 1, W_V_EMPTY)) return false;
-        if (hv == 0) TRACE_V(part, tsb, 12 + p);
         mbar_arrive_expect_tx(&b->v_full[slot], kVSlot);
         uint8_t *dst = smem + kOffV + slot * kVSlot;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          tma_load_3d(dst + i * kChunk, map, &b->v_full[slot], 64 * (4 * hv + i), j.pg.row0[p],
+          tma_load_3d(dst + i * kChunk, map, &b->v_full[slot], 64 * (4 * g + i), j.pg.row0[p],
                       j.pg.page[p]);
       }
     }
-    TRACE(1, part, tsb, 9);
-    ++tsb;
     return true;
   };
-  while (ha) {
-    if (!run(ja)) return;
-    ha = w.more;
-    if (ha) issue_job(a, w, ja);
-    if (!hb) break;
-    if (!run(jb)) return;
-    hb = w.more;
-    if (hb) issue_job(a, w, jb);
+  // one superblock of block-table lookahead: job j + 1's loads are issued
+  // before job j's tiles are requested
+  while (true) {
+    cur = nxt;
+    hc = hn;
+    hn = w.more;
+    if (hn) issue_job(a, w, nxt);
+    if (!hc) {
+      if (!hn) break;
+      continue;
+    }
+    if (!run(cur)) return;
   }
 }
 
+// Rows [r0, r1) of a V tile (four 64-column boxes) set to zero, for the MMA
+// that reads them (once per segment end, so kept out of line).
+__device__ __noinline__ void zero_rows(uint8_t *vs, int r0, int r1) {
+#pragma unroll 1
+  for (int row = r0; row < r1; ++row)
+#pragma unroll 1
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) st_shared_v4(smem_u32(vs + i * kChunk + row * 128 + ch * 16), 0, 0, 0, 0);
+  fence_proxy_async_smem();
+}
+
+// One thread issues; as in the score CTA the loop only advances counters and
+// descriptors between MMAs.
 template <typename T>
 __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int part, uint32_t tmem) {
   Bars *b = c.bars;
-  const int lane = threadIdx.x & 31;
   const uint32_t idesc = idesc_f16(128, 256, Pack<T>::kBf16, false, true);
-  uint32_t vc = 0, sb = 0, segn = 0;
-  uint32_t pc = 0;  // P tiles consumed (ring slot pc % kNPR)
+  const uint64_t pdesc = desc_kmajor_sw128(smem_u32(smem + kOffPRing));
+  const uint64_t vdesc = desc_mnmajor_sw128(smem_u32(smem + kOffV), 8192, 1024);
+  const uint32_t vfull = smem_u32(&b->v_full[0]), vempty = smem_u32(&b->v_empty[0]);
+  const uint32_t pfull = smem_u32(&b->p_full[0]), sfree = smem_u32(&b->slot_free[0]);
+  uint32_t vslot = 0, vphase = 0;  // V ring position of the next tile and its v_full parity
+  uint32_t pslot = 0, pphase = 0;  // P ring position of this superblock's first tile
+  uint32_t sb = 0, segn = 0;
   SegWalk walk(a, part);
   Seg s;
   while (walk.next(a, s)) {
     if (s.hi <= s.lo) continue;
-    if (segn > 0) {
-      const bool ok = wait_bar<false>(c, &b->o_free, (segn - 1) & 1, W_O_FREE);
-      if (__any_sync(0xffffffffu, !ok || c.aborted())) return;
-    }
-    uint32_t first = 3u;  // bit hv: next MMA into O half hv starts the accumulation
+    if (segn > 0 && !wait_bar<false>(c, &b->o_free, (segn - 1) & 1, W_O_FREE)) return;  // epilogue read O
+    uint32_t first = 3u;  // bit g: the next MMA into O half g starts the accumulation
     const int nsb = (s.hi - s.lo + kSB - 1) / kSB;
     for (int j = 0; j < nsb; ++j, ++sb) {
       const int sb0 = s.lo + j * kSB;
       const int np = min(kSB, s.hi - sb0);
-      {
-        const bool ok = wait_bar<false>(c, &b->o_ready[sb & 1], (sb >> 1) & 1, W_O_READY);
-        if (__any_sync(0xffffffffu, !ok || c.aborted())) return;
-      }
-      if (lane == 0) TRACE(1, part, sb, 0);
-      tc_fence_after();
-      for (int p = 0; p < np; ++p, ++pc) {
-        const uint32_t r = pc % kNPR;
-        const int valid = min(64, s.L - ((sb0 + p) << 6));
-        const int ksteps = (valid + 15) >> 4;
-        {
-          const bool ok = wait_bar<true>(c, &b->p_full[r], (pc / kNPR) & 1, W_P_FULL);
-          if (__any_sync(0xffffffffu, !ok || c.aborted())) return;
-        }
-        if (lane == 0) TRACE_V(part, sb, p);
-        if (lane == 0 && p == 0) TRACE(1, part, sb, 1);
-        const uint32_t pt = smem_u32(smem + kOffPRing + r * kPTile);
-        for (int hv = 0; hv < 2; ++hv, ++vc) {
-          const uint32_t slot = vc % kNV, use = vc / kNV;
-          {
-            const bool ok = wait_bar<false>(c, &b->v_full[slot], use & 1, W_V_FULL);
-            if (__any_sync(0xffffffffu, !ok || c.aborted())) return;
-          }
-          if (lane == 0) TRACE_V(part, sb, 4 + 2 * p + hv);
-          if (lane == 0 && p == 0 && hv == 0) TRACE(1, part, sb, 3);
-          uint8_t *vs = smem + kOffV + slot * kVSlot;
-          if (valid & 15) {  // rows past the sequence inside the last K step: make them 0
-            const int r0 = valid, r1 = ksteps * 16;
-            for (int idx = lane; idx < (r1 - r0) * 4 * 8; idx += 32) {
-              const int row = r0 + idx / 32, i = (idx / 8) & 3, ch = idx & 7;
-              st_shared_v4(smem_u32(vs + i * kChunk + row * 128 + ch * 16), 0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
+#pragma unroll 1
+      for (int g = 0; g < 2; ++g) {
+        if (!wait_bar<false>(c, &b->o_ready[g][sb & 1], (sb >> 1) & 1, W_O_READY)) return;
+        tc_fence_after();
+        uint32_t r = pslot, rph = pphase;
+#pragma unroll 1
+        for (int p = 0; p < np; ++p) {
+          const int valid = min(64, s.L - ((sb0 + p) << 6));
+          const int ksteps = (valid + 15) >> 4;
+          if (g == 0 && !wait_addr<true>(c, pfull + 8 * r, rph, W_P_FULL)) return;
+          if (!wait_addr<false>(c, vfull + 8 * vslot, vphase, W_V_FULL)) return;
+          if (valid & 15) zero_rows(smem + kOffV + vslot * kVSlot, valid, ksteps * 16);
           tc_fence_after();
-          if (lane == 0) {
-            const uint32_t vb = smem_u32(vs);
-            for (int k = 0; k < ksteps; ++k) {
-              mma_ss(tmem + 256 * hv, desc_kmajor_sw128(pt + 32 * k),
-                     desc_mnmajor_sw128(vb + 2048 * k, 8192, 1024), idesc,
-                     (((first >> hv) & 1u) && k == 0) ? 0u : 1u);
-            }
-            first &= ~(1u << hv);
-            mma_commit(&b->v_empty[slot]);
+          const uint64_t pd = pdesc + (uint64_t)(r * (kPTile >> 4));
+          const uint64_t vd = vdesc + (uint64_t)(vslot * (kVSlot >> 4));
+          const uint32_t acc0 = (first >> g) & 1u ? 0u : 1u;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (k < ksteps) mma_ss(tmem + 256 * g, pd + 2 * k, vd + 128 * k, idesc, k == 0 ? acc0 : 1u);
+          first &= ~(1u << g);
+          mma_commit_addr(vempty + 8 * vslot);
+          if (g == 1) mma_commit_multicast_addr(sfree + 8 * r, 1);  // P tile fully used
+          if (++vslot == kNV) {
+            vslot = 0;
+            vphase ^= 1u;
           }
-          __syncwarp();
+          if (++r == kNPR) {
+            r = 0;
+            rph ^= 1u;
+          }
         }
-        if (lane == 0) mma_commit_multicast(&b->slot_free[r], 1);
-
+        mma_commit(&b->o_done[g][sb & 1]);
+        if (g == 1) {
+          pslot = r;
+          pphase = rph;
+        }
       }
-      if (lane == 0) mma_commit(&b->o_done[sb & 1]);
-      if (lane == 0) TRACE(1, part, sb, 2);
-      __syncwarp();
     }
     ++segn;
-  }
-}
-
-// 256 threads bring the four pages of superblock `w` (all 576 columns) into L2.
-__device__ __forceinline__ void prefetch_sb_lines(const FwdArgs &a, const SbWalk &w, int tid) {
-  if (!w.more) return;
-  const int np = min(kSB, w.s.hi - w.sb0);
-  SbPages pg;
-  issue_sb_pages(a, w.s.seq, w.sb0, np, pg);
-  finish_sb_pages(a, w.s.seq, np, pg);
-  const char *kv = reinterpret_cast<const char *>(a.kv);
-  constexpr int kLinesPerPage = 64 * 9;  // 64 rows x 1152 bytes
-#pragma unroll
-  for (int k = 0; k < (kSB * kLinesPerPage) / 256; ++k) {
-    const int line = tid + 256 * k;
-    const int p = line / kLinesPerPage;
-    if (p < np) {
-      const int rem = line - p * kLinesPerPage;
-      const int row = rem / 9, col = rem - row * 9;
-      const char *addr = kv + ((int64_t)pg.page[p] * a.kv_page_stride +
-                               (int64_t)(pg.row0[p] + row) * a.kv_row_stride) * 2 + col * 128;
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
-    }
   }
 }
 
@@ -741,7 +776,7 @@ __device__ __forceinline__ void prefetch_sb_lines(const FwdArgs &a, const SbWalk
 // has landed, so it can reuse the staging tile.
 __device__ void value_receiver(const FwdArgs &a, const Ctx &c, int part) {
   Bars *b = c.bars;
-  uint32_t pc = 0;
+  uint32_t pc = 0, sb = 0;
   SbWalk w(a, part);
   while (w.more) {
     const int np = min(kSB, w.s.hi - w.sb0);
@@ -749,9 +784,57 @@ __device__ void value_receiver(const FwdArgs &a, const Ctx &c, int part) {
       const uint32_t r = pc % kNPR;
       mbar_arrive_expect_tx(&b->p_full[r], kPTile);
       if (!wait_bar<true>(c, &b->p_full[r], (pc / kNPR) & 1, W_P_FULL)) return;
-      mbar_arrive_cluster(&b->stage_free[t], 0);
+      mbar_arrive_cluster(&b->stage_free[(sb & 1) * kSB + t], 0);
     }
     w.advance(a);
+    ++sb;
+  }
+}
+
+// Epilogue of one thread's head row and O half: O / l from TMEM to `out` (one
+// split) or to the fp32 split workspace.  Once per segment, so out of line.
+template <typename T>
+__device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int nsplit, int head,
+                                       bool head_ok, int g, uint32_t tO, float lrow) {
+  const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i) {
+    uint32_t w[2][32];
+    tmem_ld32(tO + 64 * i, w[0]);
+    tmem_ld32(tO + 64 * i + 32, w[1]);
+    tmem_wait_ld();
+    if (!head_ok) continue;
+    if (nsplit == 1) {
+      uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(a.out) + (int64_t)seq * a.o_batch_stride +
+                                           (int64_t)head * a.o_head_stride + 256 * g + 64 * i);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float *f = reinterpret_cast<const float *>(&w[k >> 2][8 * (k & 3)]);
+        o[k] = make_uint4(Pack<T>::two(f[0] * inv, f[1] * inv), Pack<T>::two(f[2] * inv, f[3] * inv),
+                          Pack<T>::two(f[4] * inv, f[5] * inv), Pack<T>::two(f[6] * inv, f[7] * inv));
+      }
+    } else {
+      float4 *o = reinterpret_cast<float4 *>(a.oaccum + ((int64_t)split * a.h + head) * 512 + 256 * g + 64 * i);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const uint32_t *x = &w[k >> 3][4 * (k & 7)];
+        o[k] = make_float4(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv,
+                           __uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv);
+      }
+    }
+  }
+}
+
+// The zero output row half of an empty sequence (its lse is -inf).
+template <typename T>
+__device__ __noinline__ void zero_out(const FwdArgs &a, int seq, int split, int nsplit, int head, int g) {
+  if (nsplit == 1) {
+    uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(a.out) + (int64_t)seq * a.o_batch_stride +
+                                         (int64_t)head * a.o_head_stride + 256 * g);
+    for (int i = 0; i < 32; ++i) o[i] = make_uint4(0, 0, 0, 0);
+  } else {
+    float4 *o = reinterpret_cast<float4 *>(a.oaccum + ((int64_t)split * a.h + head) * 512 + 256 * g);
+    for (int i = 0; i < 64; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
@@ -762,22 +845,18 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sw = warp - 2;
   const int quad = warp & 3;
-  const int half = sw >> 2;  // O columns [256 * half, 256 * half + 256)
+  const int g = sw >> 2;  // O columns [256 g, 256 g + 256)
+  const int bar_id = 2 + g;
   const int r = 32 * quad + lane;
   const int head = head0 + r;
   const bool head_ok = head < a.h;
-  const uint32_t tO = tmem + ((uint32_t)(32 * quad) << 16) + 256 * half;
+  const uint32_t tO = tmem + ((uint32_t)(32 * quad) << 16) + 256 * g;
   uint32_t sb = 0;
-  int observed = -1;  // last o_done phase (superblock index) waited on
-  SbWalk pf(a, part);
-  for (int i = 0; i < kLinePrefetchSb; ++i) {
-    prefetch_sb_lines(a, pf, threadIdx.x - 64);
-    pf.advance(a);
-  }
+  int observed = -1;  // last o_done phase (superblock index) of my half waited on
   auto wait_done = [&](int k) -> bool {
     while (observed < k) {
       const int n = observed + 1;
-      if (!wait_bar<false>(c, &b->o_done[n & 1], (n >> 1) & 1, W_O_DONE)) return false;
+      if (!wait_bar<false>(c, &b->o_done[g][n & 1], (n >> 1) & 1, W_O_DONE)) return false;
       observed = n;
     }
     return true;
@@ -786,89 +865,53 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
   Seg s;
   while (walk.next(a, s)) {
     if (s.hi <= s.lo) {  // empty sequence: its output row is zero
-      if (head_ok && s.nsplit == 1) {
-        uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(a.out) +
-                                             (int64_t)s.seq * a.o_batch_stride +
-                                             (int64_t)head * a.o_head_stride + 256 * half);
-        for (int i = 0; i < 32; ++i) o[i] = make_uint4(0, 0, 0, 0);
-      } else if (head_ok) {
-        float4 *o = reinterpret_cast<float4 *>(a.oaccum + ((int64_t)s.split * a.h + head) * 512 +
-                                               256 * half);
-        for (int i = 0; i < 64; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+      if (head_ok) zero_out<T>(a, s.seq, s.split, s.nsplit, head, g);
       continue;
     }
     const int nsb = (s.hi - s.lo + kSB - 1) / kSB;
     for (int j = 0; j < nsb; ++j, ++sb) {
       const int hs = sb & 1;
-      if (kLinePrefetchSb > 0) {
-        prefetch_sb_lines(a, pf, threadIdx.x - 64);
-        pf.advance(a);
-      }
       if (sw == 0 && lane == 0) mbar_arrive_expect_tx(&b->hdr_full[hs], sizeof(Header));
       bool ok = wait_bar<true>(c, &b->hdr_full[hs], (sb >> 1) & 1, W_HDR_FULL);
-      if (sw == 0 && lane == 0) TRACE(1, part, sb, 4);
       const Header *hdr = reinterpret_cast<const Header *>(smem + kOffHdr + hs * sizeof(Header));
       const uint32_t flags = hdr->flags;
       const float alpha = hdr->alpha[r];
       const float lrow = hdr->l[r];
-      if (bar_red_or(2, 256, !ok || c.aborted())) return;
-      if (sw == 0 && lane == 0) mbar_arrive_cluster(&b->hdr_free[hs], 0);
-      // O_done(sb - 2) keeps the o_ready barriers from running two phases ahead
-      if ((int)sb >= 2) ok = wait_done((int)sb - 2);
-      if (ok && (flags & 1u)) ok = wait_done((int)sb - 1);
-      if (bar_red_or(2, 256, !ok || c.aborted())) return;
-      // only warps with a head whose reference max moved touch O
-      if ((flags & 1u) && __any_sync(0xffffffffu, alpha != 1.f)) {
+      if (bar_red_or(bar_id, 128, !ok || c.aborted())) return;
+      if ((sw & 3) == 0 && lane == 0) mbar_arrive_cluster(&b->hdr_free[hs], 0);
+      // O_done(sb - 2) keeps the o_ready barriers from running two phases ahead;
+      // a warp whose heads moved their reference max rescales once the previous
+      // superblock's MMAs into this half are complete
+      const bool resc = __any_sync(0xffffffffu, alpha != 1.f);
+      if (ok && (int)sb >= 2) ok = wait_done((int)sb - 2);
+      if (ok && resc) ok = wait_done((int)sb - 1);
+      if (ok && resc) {
         tc_fence_after();
 #pragma unroll 1
-        for (int i = 0; i < 8; ++i) {
-          uint32_t w[32];
-          tmem_ld32(tO + 32 * i, w);
+        for (int i = 0; i < 4; ++i) {
+          uint32_t w0[32], w1[32];
+          tmem_ld32(tO + 64 * i, w0);
+          tmem_ld32(tO + 64 * i + 32, w1);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
-          tmem_st32(tO + 32 * i, w);
+          for (int e = 0; e < 32; ++e) {
+            w0[e] = __float_as_uint(__uint_as_float(w0[e]) * alpha);
+            w1[e] = __float_as_uint(__uint_as_float(w1[e]) * alpha);
+          }
+          tmem_st32(tO + 64 * i, w0);
+          tmem_st32(tO + 64 * i + 32, w1);
         }
         tmem_wait_st();
         tc_fence_before();
       }
-      mbar_arrive(&b->o_ready[sb & 1]);
-      if (sw == 0 && lane == 0) TRACE(1, part, sb, 5);
+      mbar_arrive(&b->o_ready[g][sb & 1]);
       if (flags & 2u) {  // epilogue
-        ok = wait_done((int)sb);
-        if (bar_red_or(2, 256, !ok || c.aborted())) return;
+        if (ok) ok = wait_done((int)sb);
+        if (bar_red_or(bar_id, 128, !ok || c.aborted())) return;
         tc_fence_after();
-        const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
-#pragma unroll 1
-        for (int i = 0; i < 8; ++i) {
-          uint32_t w[32];
-          tmem_ld32(tO + 32 * i, w);
-          tmem_wait_ld();
-          if (!head_ok) continue;
-          if (s.nsplit == 1) {
-            uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(a.out) +
-                                                 (int64_t)s.seq * a.o_batch_stride +
-                                                 (int64_t)head * a.o_head_stride + 256 * half +
-                                                 32 * i);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float *f = reinterpret_cast<const float *>(&w[8 * k]);
-              o[k] = make_uint4(Pack<T>::two(f[0] * inv, f[1] * inv), Pack<T>::two(f[2] * inv, f[3] * inv),
-                                Pack<T>::two(f[4] * inv, f[5] * inv), Pack<T>::two(f[6] * inv, f[7] * inv));
-            }
-          } else {
-            float4 *o = reinterpret_cast<float4 *>(a.oaccum + ((int64_t)s.split * a.h + head) * 512 +
-                                                   256 * half + 32 * i);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              o[k] = make_float4(__uint_as_float(w[4 * k]) * inv, __uint_as_float(w[4 * k + 1]) * inv,
-                                 __uint_as_float(w[4 * k + 2]) * inv, __uint_as_float(w[4 * k + 3]) * inv);
-          }
-        }
+        write_out<T>(a, s.seq, s.split, s.nsplit, head, head_ok, g, tO, lrow);
         tc_fence_before();
         mbar_arrive(&b->o_free);
-        if (sw == 0 && lane == 0) TRACE(1, part, sb, 6);
       }
     }
   }
@@ -893,20 +936,22 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const FwdArgs a) {
       mbar_init(&b->k_full[i], 1);
       mbar_init(&b->k_empty[i], 1);
     }
-    mbar_init(&b->s_full, 1);
-    mbar_init(&b->s_free, 256);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&b->s_full[i], 1);
+      mbar_init(&b->s_free[i], 256);
+      mbar_init(&b->hdr_free[i], 2);
+      mbar_init(&b->hdr_full[i], 1);
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(&b->o_ready[i][k], 128);
+        mbar_init(&b->o_done[i][k], 1);
+      }
+    }
     mbar_init(&b->q_ready, 256);
-    mbar_init(&b->stage_ready, 256);
-    for (int i = 0; i < kSB; ++i) mbar_init(&b->stage_free[i], 1);
+    for (int i = 0; i < kStages; ++i) mbar_init(&b->stage_ready[i], 256);
+    for (int i = 0; i < kStages * kSB; ++i) mbar_init(&b->stage_free[i], 1);
     for (int i = 0; i < kNPR; ++i) {
       mbar_init(&b->slot_free[i], 1);
       mbar_init(&b->p_full[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&b->hdr_free[i], 1);
-      mbar_init(&b->hdr_full[i], 1);
-      mbar_init(&b->o_ready[i], 256);
-      mbar_init(&b->o_done[i], 1);
     }
     for (int i = 0; i < kNV; ++i) {
       mbar_init(&b->v_full[i], 1);
@@ -927,9 +972,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const FwdArgs a) {
   cluster_sync();  // peer barriers initialised before any remote arrive or copy
   const uint32_t tmem = b->tmem_base;
   const Ctx c{b, a.err};
-#if MLA_TRACE
-  if (threadIdx.x == 0 && role == 0 && part < 1024 && blockIdx.y == 0) g_parts[part][0] = globaltimer_ns();
-#endif
+  prof_role(0);
 
   if (role == 0) {
     // warp 0: K producer, 1: MMA, 2-9: softmax, 10: P/header copier.  Spinning roles
@@ -944,11 +987,12 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const FwdArgs a) {
       if (lane == 0) score_copier(a, smem, c, part);
     }
   } else {
-    // warp 0: V producer, 1: MMA, 2-9: correction / epilogue, 10: P-tile receiver
+    // warp 0: V producer, 1: MMA, 2-5 / 6-9: correction and epilogue of O half 0 / 1,
+    // 10: P-tile receiver
     if (warp == 0) {
       if (lane == 0) value_producer<T>(a, &kv_map, smem, c, part);
     } else if (warp == 1) {
-      value_mma<T>(a, smem, c, part, tmem);
+      if (lane == 0) value_mma<T>(a, smem, c, part, tmem);
     } else if (warp < 10) {
       value_correction<T>(a, smem, c, part, tmem, head0);
     } else {
@@ -956,11 +1000,9 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const FwdArgs a) {
     }
   }
 
+  prof_role(1);
   tc_fence_before();
   __syncthreads();
-#if MLA_TRACE
-  if (threadIdx.x == 0 && part < 1024 && blockIdx.y == 0) g_parts[part][1 + role] = globaltimer_ns();
-#endif
   cluster_sync();
   if (warp == 1) {
     tc_fence_after();
@@ -1022,28 +1064,16 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
 
 }  // namespace
 
-#if MLA_TRACE
-extern "C" int mla_debug_trace(void *dst, size_t bytes) {
-  if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
-  return cudaMemcpyFromSymbol(dst, g_trace, bytes) == cudaSuccess ? 0 : -7;
+#if MLA_WAIT_PROFILE
+extern "C" int mla_debug_wait_profile(void *waits, size_t wbytes, void *roles, size_t rbytes) {
+  if (wbytes > sizeof(g_wait_ns)) wbytes = sizeof(g_wait_ns);
+  if (rbytes > sizeof(g_role_ns)) rbytes = sizeof(g_role_ns);
+  if (cudaMemcpyFromSymbol(waits, g_wait_ns, wbytes) != cudaSuccess) return -7;
+  return cudaMemcpyFromSymbol(roles, g_role_ns, rbytes) == cudaSuccess ? 0 : -7;
 }
-extern "C" int mla_debug_trace_clear(void) {
-  static unsigned long long zero[2 * 256 * 16];
-  if (cudaMemcpyToSymbol(g_trace_k, zero, sizeof(zero)) != cudaSuccess) return -7;
-  if (cudaMemcpyToSymbol(g_trace_v, zero, sizeof(g_trace_v)) != cudaSuccess) return -7;
-  return cudaMemcpyToSymbol(g_trace, zero, sizeof(zero)) == cudaSuccess ? 0 : -7;
-}
-extern "C" int mla_debug_parts(void *dst, size_t bytes) {
-  if (bytes > sizeof(g_parts)) bytes = sizeof(g_parts);
-  return cudaMemcpyFromSymbol(dst, g_parts, bytes) == cudaSuccess ? 0 : -7;
-}
-extern "C" int mla_debug_trace_v(void *dst, size_t bytes) {
-  if (bytes > sizeof(g_trace_v)) bytes = sizeof(g_trace_v);
-  return cudaMemcpyFromSymbol(dst, g_trace_v, bytes) == cudaSuccess ? 0 : -7;
-}
-extern "C" int mla_debug_trace_k(void *dst, size_t bytes) {
-  if (bytes > sizeof(g_trace_k)) bytes = sizeof(g_trace_k);
-  return cudaMemcpyFromSymbol(dst, g_trace_k, bytes) == cudaSuccess ? 0 : -7;
+extern "C" int mla_debug_wait_profile_clear(void) {
+  static unsigned long long zero[sizeof(g_wait_ns) / 8];
+  return cudaMemcpyToSymbol(g_wait_ns, zero, sizeof(g_wait_ns)) == cudaSuccess ? 0 : -7;
 }
 #endif
 
