@@ -219,6 +219,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// One lane of the (fully active) warp; the rest get false.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
+  return p != 0;
+}
+
 // ----------------------------------------------------------------------------- tcgen05
 
 // Allocate `ncols` TMEM columns (power of two >= 32); whole warp; address -> *dst.

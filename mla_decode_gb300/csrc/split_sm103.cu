@@ -128,6 +128,11 @@ enum : int {
 constexpr int kProfParts = 128, kProfSites = 32;
 __device__ unsigned long long g_wait_ns[kProfParts][2][kThreads / 32][kProfSites];
 __device__ unsigned long long g_role_ns[kProfParts][2][kThreads / 32][2];
+__device__ unsigned long long g_chunk_trace[1024][3];  // part 0, score MMA: per chunk before wait, after wait, after commit
+__device__ __forceinline__ void prof_chunk(uint32_t n, int which) {
+  if (blockIdx.x == 0 && blockIdx.y == 0 && (threadIdx.x & 31) == 0 && n < 1024)
+    g_chunk_trace[n][which] = clock64();
+}
 // (SM clock cycles: cheap to read, and every interval is taken on one SM)
 __device__ __forceinline__ uint64_t prof_now() { return clock64(); }
 __device__ __forceinline__ void prof_wait(int where, uint64_t t0) {
@@ -142,6 +147,7 @@ __device__ __forceinline__ void prof_role(int which) {
     g_role_ns[part][blockIdx.x & 1][threadIdx.x >> 5][which] = clock64();
 }
 #else
+__device__ __forceinline__ void prof_chunk(uint32_t, int) {}
 __device__ __forceinline__ uint64_t prof_now() { return 0; }
 __device__ __forceinline__ void prof_wait(int, uint64_t) {}
 __device__ __forceinline__ void prof_role(int) {}
@@ -346,6 +352,7 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *map, uint8_t
                                const Ctx &c, int part) {
   Bars *b = c.bars;
   uint32_t kc = 0;
+  const bool leader = elect_one();
   SbWalk w(a, part);
   SbJob cur{}, nxt{};
   bool hc = false, hn = false;
@@ -354,12 +361,14 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *map, uint8_t
     for (int ch = 0; ch < 9; ++ch, ++kc) {
       const uint32_t slot = kc % kNK, use = kc / kNK;
       if (use > 0 && !wait_bar<false>(c, &b->k_empty[slot], (use - 1) & 1, W_K_EMPTY)) return false;
-      mbar_arrive_expect_tx(&b->k_full[slot], j.np * kChunk);
-      uint8_t *dst = smem + kOffK + slot * kKSlot;
+      if (leader) {
+        mbar_arrive_expect_tx(&b->k_full[slot], j.np * kChunk);
+        uint8_t *dst = smem + kOffK + slot * kKSlot;
 #pragma unroll
-      for (int p = 0; p < kSB; ++p)
-        if (p < j.np)
-          tma_load_3d(dst + p * kChunk, map, &b->k_full[slot], 64 * ch, j.pg.row0[p], j.pg.page[p]);
+        for (int p = 0; p < kSB; ++p)
+          if (p < j.np)
+            tma_load_3d(dst + p * kChunk, map, &b->k_full[slot], 64 * ch, j.pg.row0[p], j.pg.page[p]);
+      }
     }
     return true;
   };
@@ -378,9 +387,13 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *map, uint8_t
   }
 }
 
-// The issue loop is kept short (slot and phase counters, descriptors advanced by
-// adding offsets): with N = 128 one MMA takes 64 tensor-core cycles, and a
-// single thread must issue the next one within that time.
+// With N = 128 one MMA takes 64 tensor-core cycles, and the next must be issued
+// within that time.  So the whole warp runs the loop, which keeps its
+// counters and descriptors warp-uniform, and one elected lane issues the MMAs and
+// commits (the chunk loop stays rolled: unrolled, its code crowds the softmax
+// loop out of the instruction cache); the loop only advances slot / phase counters and adds offsets to
+// precomputed descriptors.  No warp-collective call sits in the loop: a lane that
+// leaves on a failed wait cannot block the others.
 template <typename T>
 __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int part, uint32_t tmem) {
   Bars *b = c.bars;
@@ -391,6 +404,8 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
   const uint32_t kfull = smem_u32(&b->k_full[0]), kempty = smem_u32(&b->k_empty[0]);
   uint32_t slot = 0, phase = 0;  // K ring position of the next chunk and its k_full parity
   uint32_t sb = 0, segn = 0;
+  uint32_t nch = 0;  // chunks issued (profile trace only)
+  const bool leader = elect_one();
   SegWalk walk(a, part);
   Seg s;
   while (walk.next(a, s)) {
@@ -406,23 +421,28 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
       const uint32_t tS = tmem + 256 + kSBTok * buf;
 #pragma unroll 1
       for (int ch = 0; ch < 9; ++ch) {
+        prof_chunk(nch, 0);
         if (!wait_addr<false>(c, kfull + 8 * slot, phase, W_K_FULL)) return;
         tc_fence_after();
+        prof_chunk(nch, 1);
         const uint64_t bd = kdesc + (uint64_t)(slot * (kKSlot >> 4));
+        if (leader) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if (ch < 8)
-            mma_ts(tS, tQ + 32 * ch + 8 * k, bd + 2 * k, idesc, (ch | k) != 0);
-          else
-            mma_ss(tS, qdesc + 2 * k, bd + 2 * k, idesc, 1);
+          for (int k = 0; k < 4; ++k) {
+            if (ch < 8)
+              mma_ts(tS, tQ + 32 * ch + 8 * k, bd + 2 * k, idesc, (ch | k) != 0);
+            else
+              mma_ss(tS, qdesc + 2 * k, bd + 2 * k, idesc, 1);
+          }
+          mma_commit_addr(kempty + 8 * slot);
         }
-        mma_commit_addr(kempty + 8 * slot);
+        prof_chunk(nch++, 2);
         if (++slot == kNK) {
           slot = 0;
           phase ^= 1u;
         }
       }
-      mma_commit(&b->s_full[buf]);
+      if (leader) mma_commit(&b->s_full[buf]);
     }
     ++segn;
   }
@@ -438,6 +458,7 @@ __device__ void score_copier(const FwdArgs &a, uint8_t *smem, const Ctx &c, int 
   const uint32_t peer_hfull = map_to_rank(smem_u32(&b->hdr_full[0]), 1);
   uint32_t pc = 0;  // P tiles shipped so far (ring slot pc % kNPR)
   uint32_t sb = 0;
+  const bool leader = elect_one();
   SbWalk w(a, part);
   while (w.more) {
     const int np = min(kSB, w.s.hi - w.sb0);
@@ -445,13 +466,15 @@ __device__ void score_copier(const FwdArgs &a, uint8_t *smem, const Ctx &c, int 
     if (!wait_bar<false>(c, &b->stage_ready[buf], (sb >> 1) & 1, W_STAGE_READY)) return;
     // the header first: the value CTA can prepare O for this superblock while it
     // is still consuming the previous one's tiles
-    bulk_copy_to_peer(peer_hdr + buf * sizeof(Header), smem + kOffHdrStage + buf * sizeof(Header),
-                      sizeof(Header), peer_hfull + buf * 8);
+    if (leader)
+      bulk_copy_to_peer(peer_hdr + buf * sizeof(Header), smem + kOffHdrStage + buf * sizeof(Header),
+                        sizeof(Header), peer_hfull + buf * 8);
     for (int t = 0; t < np; ++t, ++pc) {
       const uint32_t r = pc % kNPR, use = pc / kNPR;
       if (use > 0 && !wait_bar<true>(c, &b->slot_free[r], (use - 1) & 1, W_SLOT_FREE)) return;
-      bulk_copy_to_peer(peer_pring + r * kPTile, smem + kOffPStage + (buf * kSB + t) * kPTile,
-                        kPTile, peer_pfull + r * 8);
+      if (leader)
+        bulk_copy_to_peer(peer_pring + r * kPTile, smem + kOffPStage + (buf * kSB + t) * kPTile,
+                          kPTile, peer_pfull + r * 8);
     }
     w.advance(a);
     ++sb;
@@ -579,11 +602,17 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
             v[i][e] = __float_as_uint(32 * i + e < lim ? __uint_as_float(v[i][e]) * scale : -INFINITY);
         sc = 1.f;
       }
-      float mloc = -INFINITY;
+      // eight independent partial maxima (and sums below): 64-long dependent
+      // chains would leave the warp waiting on instruction latency
+      float mp[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 2; ++i)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mloc = fmaxf(mloc, __uint_as_float(v[i][e]) * sc);
+        for (int e = 0; e < 32; ++e) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(v[i][e]) * sc);
+      const float mloc = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       red_max[half * 128 + r] = mloc;
       prof_wait(20, tp);
       tp = prof_now();
@@ -600,7 +629,9 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       if (ok && half < np && tu.was_used(tb))
         ok = wait_bar<true>(c, &b->stage_free[tb], tu.parity(tb) ^ 1u, W_STAGE_FREE);
       tp = prof_now();
-      float psum = 0.f;
+      float ps[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ps[e] = 0.f;
       const bool write = ok && half < np;
       const uint32_t row = smem_u32(smem + kOffPStage + tb * kPTile) + r * 128;
       const float nm = -m_ref;
@@ -610,14 +641,14 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           p[e] = fast_exp2(fmaf(__uint_as_float(v[ch >> 2][(ch & 3) * 8 + e]), sc, nm));
-          psum += p[e];
+          ps[e] += p[e];
         }
         if (write)
           st_shared_v4(row + ((ch ^ (r & 7)) << 4), Pack<T>::two(p[0], p[1]),
                        Pack<T>::two(p[2], p[3]), Pack<T>::two(p[4], p[5]),
                        Pack<T>::two(p[6], p[7]));
       }
-      red_sum[half * 128 + r] = psum;
+      red_sum[half * 128 + r] = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       prof_wait(21, tp);
       const int hs = sb & 1;
       Header *hdr = reinterpret_cast<Header *>(smem + kOffHdrStage + hs * sizeof(Header));
@@ -657,6 +688,7 @@ __device__ void value_producer(const FwdArgs &a, const CUtensorMap *map, uint8_t
                                const Ctx &c, int part) {
   Bars *b = c.bars;
   uint32_t vc = 0;
+  const bool leader = elect_one();
   SbWalk w(a, part);
   SbJob cur{}, nxt{};
   bool hc = false, hn = false;
@@ -670,12 +702,14 @@ __device__ void value_producer(const FwdArgs &a, const CUtensorMap *map, uint8_t
         const uint32_t slot = vc % kNV, use = vc / kNV;
         ++vc;
         if (use > 0 && !wait_bar<false>(c, &b->v_empty[slot], (use - 1) & 1, W_V_EMPTY)) return false;
-        mbar_arrive_expect_tx(&b->v_full[slot], kVSlot);
-        uint8_t *dst = smem + kOffV + slot * kVSlot;
+        if (leader) {
+          mbar_arrive_expect_tx(&b->v_full[slot], kVSlot);
+          uint8_t *dst = smem + kOffV + slot * kVSlot;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          tma_load_3d(dst + i * kChunk, map, &b->v_full[slot], 64 * (4 * g + i), j.pg.row0[p],
-                      j.pg.page[p]);
+          for (int i = 0; i < 4; ++i)
+            tma_load_3d(dst + i * kChunk, map, &b->v_full[slot], 64 * (4 * g + i), j.pg.row0[p],
+                        j.pg.page[p]);
+        }
       }
     }
     return true;
@@ -707,8 +741,8 @@ __device__ __noinline__ void zero_rows(uint8_t *vs, int r0, int r1) {
   fence_proxy_async_smem();
 }
 
-// One thread issues; as in the score CTA the loop only advances counters and
-// descriptors between MMAs.
+// As in the score CTA: the whole warp runs the loop, one elected lane issues,
+// and the loop only advances counters and descriptors between MMAs.
 template <typename T>
 __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int part, uint32_t tmem) {
   Bars *b = c.bars;
@@ -720,6 +754,7 @@ __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
   uint32_t vslot = 0, vphase = 0;  // V ring position of the next tile and its v_full parity
   uint32_t pslot = 0, pphase = 0;  // P ring position of this superblock's first tile
   uint32_t sb = 0, segn = 0;
+  const bool leader = elect_one();
   SegWalk walk(a, part);
   Seg s;
   while (walk.next(a, s)) {
@@ -741,17 +776,19 @@ __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
           const int ksteps = (valid + 15) >> 4;
           if (g == 0 && !wait_addr<true>(c, pfull + 8 * r, rph, W_P_FULL)) return;
           if (!wait_addr<false>(c, vfull + 8 * vslot, vphase, W_V_FULL)) return;
-          if (valid & 15) zero_rows(smem + kOffV + vslot * kVSlot, valid, ksteps * 16);
+          if (leader && (valid & 15)) zero_rows(smem + kOffV + vslot * kVSlot, valid, ksteps * 16);
           tc_fence_after();
           const uint64_t pd = pdesc + (uint64_t)(r * (kPTile >> 4));
           const uint64_t vd = vdesc + (uint64_t)(vslot * (kVSlot >> 4));
           const uint32_t acc0 = (first >> g) & 1u ? 0u : 1u;
+          if (leader) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (k < ksteps) mma_ss(tmem + 256 * g, pd + 2 * k, vd + 128 * k, idesc, k == 0 ? acc0 : 1u);
+            for (int k = 0; k < 4; ++k)
+              if (k < ksteps) mma_ss(tmem + 256 * g, pd + 2 * k, vd + 128 * k, idesc, k == 0 ? acc0 : 1u);
+            mma_commit_addr(vempty + 8 * vslot);
+            if (g == 1) mma_commit_multicast_addr(sfree + 8 * r, 1);  // P tile fully used
+          }
           first &= ~(1u << g);
-          mma_commit_addr(vempty + 8 * vslot);
-          if (g == 1) mma_commit_multicast_addr(sfree + 8 * r, 1);  // P tile fully used
           if (++vslot == kNV) {
             vslot = 0;
             vphase ^= 1u;
@@ -761,7 +798,7 @@ __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
             rph ^= 1u;
           }
         }
-        mma_commit(&b->o_done[g][sb & 1]);
+        if (leader) mma_commit(&b->o_done[g][sb & 1]);
         if (g == 1) {
           pslot = r;
           pphase = rph;
@@ -777,14 +814,15 @@ __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
 __device__ void value_receiver(const FwdArgs &a, const Ctx &c, int part) {
   Bars *b = c.bars;
   uint32_t pc = 0, sb = 0;
+  const bool leader = elect_one();
   SbWalk w(a, part);
   while (w.more) {
     const int np = min(kSB, w.s.hi - w.sb0);
     for (int t = 0; t < np; ++t, ++pc) {
       const uint32_t r = pc % kNPR;
-      mbar_arrive_expect_tx(&b->p_full[r], kPTile);
+      if (leader) mbar_arrive_expect_tx(&b->p_full[r], kPTile);
       if (!wait_bar<true>(c, &b->p_full[r], (pc / kNPR) & 1, W_P_FULL)) return;
-      mbar_arrive_cluster(&b->stage_free[(sb & 1) * kSB + t], 0);
+      if (leader) mbar_arrive_cluster(&b->stage_free[(sb & 1) * kSB + t], 0);
     }
     w.advance(a);
     ++sb;
@@ -975,28 +1013,29 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const FwdArgs a) {
   prof_role(0);
 
   if (role == 0) {
-    // warp 0: K producer, 1: MMA, 2-9: softmax, 10: P/header copier.  Spinning roles
-    // never share a warp (a diverged spin loop starves the other lanes' path).
+    // warp 0: K producer, 1: MMA, 2-9: softmax, 10: P/header copier.  Each role has
+    // a whole warp (a diverged spin loop would starve the other lanes' path, and
+    // warp-uniform issue loops let one elected lane issue at full rate).
     if (warp == 0) {
-      if (lane == 0) score_producer<T>(a, &kv_map, smem, c, part);
+      score_producer<T>(a, &kv_map, smem, c, part);
     } else if (warp == 1) {
-      if (lane == 0) score_mma<T>(a, smem, c, part, tmem);
+      score_mma<T>(a, smem, c, part, tmem);
     } else if (warp < 10) {
       score_softmax<T>(a, smem, c, part, tmem, head0);
     } else {
-      if (lane == 0) score_copier(a, smem, c, part);
+      score_copier(a, smem, c, part);
     }
   } else {
     // warp 0: V producer, 1: MMA, 2-5 / 6-9: correction and epilogue of O half 0 / 1,
     // 10: P-tile receiver
     if (warp == 0) {
-      if (lane == 0) value_producer<T>(a, &kv_map, smem, c, part);
+      value_producer<T>(a, &kv_map, smem, c, part);
     } else if (warp == 1) {
-      if (lane == 0) value_mma<T>(a, smem, c, part, tmem);
+      value_mma<T>(a, smem, c, part, tmem);
     } else if (warp < 10) {
       value_correction<T>(a, smem, c, part, tmem, head0);
     } else {
-      if (lane == 0) value_receiver(a, c, part);
+      value_receiver(a, c, part);
     }
   }
 
@@ -1070,6 +1109,10 @@ extern "C" int mla_debug_wait_profile(void *waits, size_t wbytes, void *roles, s
   if (rbytes > sizeof(g_role_ns)) rbytes = sizeof(g_role_ns);
   if (cudaMemcpyFromSymbol(waits, g_wait_ns, wbytes) != cudaSuccess) return -7;
   return cudaMemcpyFromSymbol(roles, g_role_ns, rbytes) == cudaSuccess ? 0 : -7;
+}
+extern "C" int mla_debug_chunk_trace(void *dst, size_t bytes) {
+  if (bytes > sizeof(g_chunk_trace)) bytes = sizeof(g_chunk_trace);
+  return cudaMemcpyFromSymbol(dst, g_chunk_trace, bytes) == cudaSuccess ? 0 : -7;
 }
 extern "C" int mla_debug_wait_profile_clear(void) {
   static unsigned long long zero[sizeof(g_wait_ns) / 8];
