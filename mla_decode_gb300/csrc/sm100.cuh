@@ -304,6 +304,14 @@ __device__ __forceinline__ void mma_commit_multicast_addr(uint32_t bar_addr, uin
       : "memory");
 }
 
+// Copy a 128-row x 256-bit tile from shared memory (matrix descriptor, same
+// layouts as MMA operands) into TMEM: row i -> lane i, 8 consecutive 32-bit
+// columns from `taddr`.  Asynchronous, ordered before later MMAs of this thread,
+// completion tracked by tcgen05.commit.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

@@ -99,7 +99,8 @@ constexpr int kOffBars = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 127)
 struct Bars {
   uint64_t k_full[kNK], k_empty[kNK];   // score
   uint64_t s_full[2], s_free[2];        // score, per S buffer
-  uint64_t q_ready;                     // score
+  uint64_t q_free;                      // score: MMAs of a segment done with Q (MMA commit)
+  uint64_t q8_full;                     // score: Q RoPE tile landed (TMA)
   uint64_t stage_ready[kStages];        // score: P tiles + header staged (softmax -> copier)
   uint64_t stage_free[kStages * kSB];   // score, arrived by the value CTA
   uint64_t slot_free[kNPR];             // score, value-CTA MMA commits (multicast)
@@ -117,8 +118,9 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // wait sites (reported as the error detail on a timeout)
 enum : int {
-  W_K_EMPTY = 1, W_Q_READY, W_S_FREE, W_K_FULL, W_S_FULL, W_STAGE_FREE, W_HDR_FREE, W_SLOT_FREE,
-  W_V_EMPTY, W_O_FREE, W_O_READY, W_P_FULL, W_V_FULL, W_HDR_FULL, W_O_DONE, W_STAGE_READY
+  W_K_EMPTY = 1, W_Q_FREE, W_S_FREE, W_K_FULL, W_S_FULL, W_STAGE_FREE, W_HDR_FREE, W_SLOT_FREE,
+  W_V_EMPTY, W_O_FREE, W_O_READY, W_P_FULL, W_V_FULL, W_HDR_FULL, W_O_DONE, W_STAGE_READY,
+  W_Q8_FULL
 };
 
 // Optional wait profile (build with -DMLA_WAIT_PROFILE=1): per part, CTA, warp
@@ -335,28 +337,50 @@ struct SbWalk {
 // A superblock job with its block-table loads in flight (see issue_sb_pages).
 struct SbJob {
   int seq, sb0, np;
+  bool first;  // first superblock of its segment
   SbPages pg;
 };
 __device__ __forceinline__ void issue_job(const FwdArgs &a, SbWalk &w, SbJob &j) {
   j.seq = w.s.seq;
   j.sb0 = w.sb0;
   j.np = min(kSB, w.s.hi - w.sb0);
+  j.first = w.sb0 == w.s.lo;
   issue_sb_pages(a, j.seq, j.sb0, j.np, j.pg);
   w.advance(a);
 }
 
 // ------------------------------------------------------------------------------ score CTA
 
+// K producer.  At a segment start it first brings that sequence's Q tile: the
+// 512 latent columns as eight [128 heads x 64] boxes through the K ring (the MMA
+// warp moves them into TMEM), the 64 RoPE columns straight into the Q8 tile once
+// the previous segment's MMAs are done with it.  Heads past h read as zeros.
 template <typename T>
-__device__ void score_producer(const FwdArgs &a, const CUtensorMap *map, uint8_t *smem,
-                               const Ctx &c, int part) {
+__device__ void score_producer(const FwdArgs &a, const CUtensorMap *map, const CUtensorMap *qmap,
+                               uint8_t *smem, const Ctx &c, int part, int head0) {
   Bars *b = c.bars;
-  uint32_t kc = 0;
+  uint32_t kc = 0, segn = 0;
   const bool leader = elect_one();
   SbWalk w(a, part);
   SbJob cur{}, nxt{};
   bool hc = false, hn = false;
   auto run = [&](SbJob &j) -> bool {
+    if (j.first) {
+      for (int i = 0; i < 8; ++i, ++kc) {
+        const uint32_t slot = kc % kNK, use = kc / kNK;
+        if (use > 0 && !wait_bar<false>(c, &b->k_empty[slot], (use - 1) & 1, W_K_EMPTY)) return false;
+        if (leader) {
+          mbar_arrive_expect_tx(&b->k_full[slot], kKSlot);
+          tma_load_3d(smem + kOffK + slot * kKSlot, qmap, &b->k_full[slot], 64 * i, head0, j.seq);
+        }
+      }
+      if (segn > 0 && !wait_bar<false>(c, &b->q_free, (segn - 1) & 1, W_Q_FREE)) return false;
+      if (leader) {
+        mbar_arrive_expect_tx(&b->q8_full, kKSlot);
+        tma_load_3d(smem + kOffQ8, qmap, &b->q8_full, 512, head0, j.seq);
+      }
+      ++segn;
+    }
     finish_sb_pages(a, j.seq, j.np, j.pg);
     for (int ch = 0; ch < 9; ++ch, ++kc) {
       const uint32_t slot = kc % kNK, use = kc / kNK;
@@ -410,7 +434,29 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
   Seg s;
   while (walk.next(a, s)) {
     if (s.hi <= s.lo) continue;
-    if (!wait_bar<false>(c, &b->q_ready, segn & 1, W_Q_READY)) return;
+    // this segment's Q: the previous segment's MMAs must be done reading it, then
+    // the eight latent boxes go from the K ring into TMEM (32 bytes of each row
+    // per copy) and the RoPE tile must have landed in Q8
+    if (segn > 0) {
+      if (!wait_bar<false>(c, &b->q_free, (segn - 1) & 1, W_Q_FREE)) return;
+      tc_fence_after();
+    }
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+      if (!wait_addr<false>(c, kfull + 8 * slot, phase, W_K_FULL)) return;
+      tc_fence_after();
+      const uint64_t bd = kdesc + (uint64_t)(slot * (kKSlot >> 4));
+      if (leader) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tmem_cp_128x256b(tQ + 32 * i + 8 * k, bd + 2 * k);
+        mma_commit_addr(kempty + 8 * slot);
+      }
+      if (++slot == kNK) {
+        slot = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!wait_bar<false>(c, &b->q8_full, segn & 1, W_Q8_FULL)) return;
     tc_fence_after();
     for (int sb0 = s.lo; sb0 < s.hi; sb0 += kSB, ++sb) {
       const uint32_t buf = sb & 1;
@@ -444,6 +490,7 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
       }
       if (leader) mma_commit(&b->s_full[buf]);
     }
+    if (leader) mma_commit(&b->q_free);
     ++segn;
   }
 }
@@ -481,55 +528,6 @@ __device__ void score_copier(const FwdArgs &a, uint8_t *smem, const Ctx &c, int 
   }
 }
 
-// Q row `head` of sequence `seq` for one softmax thread: its half of columns
-// 0..511 into TMEM (A operand layout: 16-bit pairs per 32-bit column), and for
-// the second half's threads columns 512..575 into the swizzled Q8 tile.  Once
-// per segment, so out of line.
-template <typename T>
-__device__ __noinline__ void load_q(const FwdArgs &a, uint8_t *smem, int seq, int head, bool head_ok,
-                                    int half, int r, uint32_t tQ) {
-  const T *q = reinterpret_cast<const T *>(a.q);
-  const uint4 *src = reinterpret_cast<const uint4 *>(q + (int64_t)seq * a.q_batch_stride +
-                                                     (int64_t)head * a.q_head_stride);
-#pragma unroll 1
-  for (int bt = 0; bt < 2; ++bt) {  // 16 loads in flight, then 64 TMEM columns
-    uint4 qv[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) qv[i] = head_ok ? src[32 * half + 16 * bt + i] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      uint32_t w[32];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        w[4 * i + 0] = qv[8 * cc + i].x;
-        w[4 * i + 1] = qv[8 * cc + i].y;
-        w[4 * i + 2] = qv[8 * cc + i].z;
-        w[4 * i + 3] = qv[8 * cc + i].w;
-      }
-      tmem_st32(tQ + 32 * (4 * half + 2 * bt + cc), w);
-    }
-  }
-  if (half == 1) {
-    const uint32_t row = smem_u32(smem + kOffQ8) + r * 128;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint4 v = head_ok ? src[64 + i] : make_uint4(0, 0, 0, 0);
-      st_shared_v4(row + ((i ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
-    }
-  }
-  tmem_wait_st();
-  fence_proxy_async_smem();
-  tc_fence_before();
-}
-
-template <typename T>
-__device__ __noinline__ void prefetch_q_row(const FwdArgs &a, int seq, int head, int half) {
-  const char *row = reinterpret_cast<const char *>(reinterpret_cast<const T *>(a.q) +
-                                                   (int64_t)seq * a.q_batch_stride +
-                                                   (int64_t)head * a.q_head_stride);
-  for (int ln = half; ln < 9; ln += 2) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 128 * ln));
-}
-
 template <typename T>
 __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int part,
                               uint32_t tmem, int head0) {
@@ -542,7 +540,6 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
   const int head = head0 + r;
   const bool head_ok = head < a.h;
   const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
-  const uint32_t tQ = tmem + lane_off;
   const uint32_t tS = tmem + 256 + lane_off + 64 * half;
   float *red_max = reinterpret_cast<float *>(smem + kOffRed);  // [2][128]
   float *red_sum = red_max + 256;                               // [2][128]
@@ -559,18 +556,6 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       }
       continue;
     }
-    // ---- Q of this sequence: columns 0..511 into TMEM, 512..575 into shared memory
-    {
-      const uint64_t tq = prof_now();
-      load_q<T>(a, smem, s.seq, head_ok ? head : head0, head_ok, half, r, tQ);
-      mbar_arrive(&b->q_ready);
-      // bring the next segment's Q rows into L2 while this segment runs
-      SegWalk nx = walk;
-      Seg s2;
-      if (head_ok && nx.next(a, s2)) prefetch_q_row<T>(a, s2.seq, head, half);
-      prof_wait(23, tq);
-    }
-
     float m_ref = -INFINITY, l = 0.f;
     const int nsb = (s.hi - s.lo + kSB - 1) / kSB;
     for (int j = 0; j < nsb; ++j, ++sb) {
@@ -959,7 +944,8 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
-split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const FwdArgs a) {
+split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
+                const FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -984,7 +970,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const FwdArgs a) {
         mbar_init(&b->o_done[i][k], 1);
       }
     }
-    mbar_init(&b->q_ready, 256);
+    mbar_init(&b->q_free, 1);
+    mbar_init(&b->q8_full, 1);
     for (int i = 0; i < kStages; ++i) mbar_init(&b->stage_ready[i], 256);
     for (int i = 0; i < kStages * kSB; ++i) mbar_init(&b->stage_free[i], 1);
     for (int i = 0; i < kNPR; ++i) {
@@ -999,7 +986,10 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const FwdArgs a) {
     b->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&kv_map);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&kv_map);
+    tma_prefetch_desc(&q_map);
+  }
   if (warp == 1) {
     tmem_alloc(&b->tmem_base, 512);
     tmem_relinquish();
@@ -1017,7 +1007,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const FwdArgs a) {
     // a whole warp (a diverged spin loop would starve the other lanes' path, and
     // warp-uniform issue loops let one elected lane issue at full rate).
     if (warp == 0) {
-      score_producer<T>(a, &kv_map, smem, c, part);
+      score_producer<T>(a, &kv_map, &q_map, smem, c, part, head0);
     } else if (warp == 1) {
       score_mma<T>(a, smem, c, part, tmem);
     } else if (warp < 10) {
@@ -1079,6 +1069,15 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // Q as [b][h][576]: boxes of 64 columns x 128 heads (rows past h read as zeros)
+  CUtensorMap qmap;
+  cuuint64_t qdims[3] = {(cuuint64_t)MLA_HEAD_DIM, (cuuint64_t)a.h, (cuuint64_t)a.b};
+  cuuint64_t qstrides[2] = {(cuuint64_t)a.q_head_stride * 2, (cuuint64_t)a.q_batch_stride * 2};
+  cuuint32_t qbox[3] = {64, 128, 1};
+  r = enc(&qmap, Pack<T>::kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+          const_cast<void *>(a.q), qdims, qstrides, qbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
@@ -1098,7 +1097,7 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, split_tc_kernel<T>, map, a);
+  return cudaLaunchKernelEx(&cfg, split_tc_kernel<T>, map, qmap, a);
 }
 
 }  // namespace
