@@ -52,9 +52,9 @@ constexpr int kThreads = 352;            // 11 warps (see the role map in the ke
 constexpr int kSB = 2;                   // pages (64 tokens each) per superblock
 constexpr int kSBTok = 64 * kSB;         // tokens per superblock: N of the score MMAs
 #ifndef MLA_NK
-#define MLA_NK 8
+#define MLA_NK 4
 #endif
-constexpr int kNK = MLA_NK;              // K tiles in flight (score CTA)
+constexpr int kNK = MLA_NK;              // K chunks in flight (score CTA)
 #ifndef MLA_NV
 #define MLA_NV 4
 #endif
@@ -69,7 +69,9 @@ constexpr int kStages = 2;               // P staging buffers in the score CTA
 #endif
 constexpr float kTau = MLA_TAU;          // lazy-rescale threshold, log2 units
 constexpr int kChunk = 8192;             // [64 rows][128 B] swizzled TMA box
-constexpr int kKSlot = kSB * kChunk;     // 64 columns of one superblock's tokens
+constexpr int kAtom = kSB * kChunk;      // one superblock's tokens x 64 columns (16 KB)
+constexpr int kKSlot = 2 * kAtom;        // K chunk: 128 columns as two 64-column atoms
+constexpr int kKChunks = 5;              // chunks per superblock: 4 x 128 latent + RoPE
 constexpr int kVSlot = 4 * kChunk;       // 256 value columns of one page
 constexpr int kPTile = 16384;            // [128 heads][64 tokens] 16-bit, swizzled
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -85,7 +87,7 @@ static_assert(sizeof(Header) % 16 == 0, "bulk copies move multiples of 16 bytes"
 
 // shared-memory map (offsets from the 1024-aligned base)
 constexpr int kOffQ8 = 0;                                     // score: Q columns 512..575
-constexpr int kOffK = kOffQ8 + 16384;                         // score: K ring
+constexpr int kOffK = kOffQ8 + kAtom;                         // score: K ring
 constexpr int kOffPStage = kOffK + kNK * kKSlot;              // score: P staging tiles
 constexpr int kOffHdrStage = kOffPStage + kStages * kSB * kPTile;  // score: 2 headers
 constexpr int kOffRed = kOffHdrStage + 2 * (int)sizeof(Header);    // score: [2][2][128] floats
@@ -130,7 +132,8 @@ enum : int {
 constexpr int kProfParts = 128, kProfSites = 32;
 __device__ unsigned long long g_wait_ns[kProfParts][2][kThreads / 32][kProfSites];
 __device__ unsigned long long g_role_ns[kProfParts][2][kThreads / 32][2];
-__device__ unsigned long long g_chunk_trace[1024][3];  // part 0, score MMA: per chunk before wait, after wait, after commit
+__device__ unsigned long long g_chunk_trace[1024][3];
+__device__ unsigned long long g_part_gt[kProfParts][2][3];  // per part and CTA: entry, roles start, roles end (ns)  // part 0, score MMA: per chunk before wait, after wait, after commit
 __device__ __forceinline__ void prof_chunk(uint32_t n, int which) {
   if (blockIdx.x == 0 && blockIdx.y == 0 && (threadIdx.x & 31) == 0 && n < 1024)
     g_chunk_trace[n][which] = clock64();
@@ -148,7 +151,13 @@ __device__ __forceinline__ void prof_role(int which) {
   if ((threadIdx.x & 31) == 0 && blockIdx.y == 0 && part < kProfParts)
     g_role_ns[part][blockIdx.x & 1][threadIdx.x >> 5][which] = clock64();
 }
+__device__ __forceinline__ void prof_part(int which) {
+  const int part = blockIdx.x >> 1;
+  if (threadIdx.x == 0 && blockIdx.y == 0 && part < kProfParts)
+    g_part_gt[part][blockIdx.x & 1][which] = globaltimer_ns();
+}
 #else
+__device__ __forceinline__ void prof_part(int) {}
 __device__ __forceinline__ void prof_chunk(uint32_t, int) {}
 __device__ __forceinline__ uint64_t prof_now() { return 0; }
 __device__ __forceinline__ void prof_wait(int, uint64_t) {}
@@ -366,32 +375,37 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *map, const C
   bool hc = false, hn = false;
   auto run = [&](SbJob &j) -> bool {
     if (j.first) {
-      for (int i = 0; i < 8; ++i, ++kc) {
+      for (int i = 0; i < 4; ++i, ++kc) {  // latent Q: 4 chunks of 128 columns
         const uint32_t slot = kc % kNK, use = kc / kNK;
         if (use > 0 && !wait_bar<false>(c, &b->k_empty[slot], (use - 1) & 1, W_K_EMPTY)) return false;
         if (leader) {
-          mbar_arrive_expect_tx(&b->k_full[slot], kKSlot);
-          tma_load_3d(smem + kOffK + slot * kKSlot, qmap, &b->k_full[slot], 64 * i, head0, j.seq);
+          mbar_arrive_expect_tx(&b->k_full[slot], 2 * kAtom);
+          uint8_t *dst = smem + kOffK + slot * kKSlot;
+          tma_load_3d(dst, qmap, &b->k_full[slot], 128 * i, head0, j.seq);
+          tma_load_3d(dst + kAtom, qmap, &b->k_full[slot], 128 * i + 64, head0, j.seq);
         }
       }
       if (segn > 0 && !wait_bar<false>(c, &b->q_free, (segn - 1) & 1, W_Q_FREE)) return false;
       if (leader) {
-        mbar_arrive_expect_tx(&b->q8_full, kKSlot);
+        mbar_arrive_expect_tx(&b->q8_full, kAtom);
         tma_load_3d(smem + kOffQ8, qmap, &b->q8_full, 512, head0, j.seq);
       }
       ++segn;
     }
     finish_sb_pages(a, j.seq, j.np, j.pg);
-    for (int ch = 0; ch < 9; ++ch, ++kc) {
+    for (int ch = 0; ch < kKChunks; ++ch, ++kc) {
       const uint32_t slot = kc % kNK, use = kc / kNK;
       if (use > 0 && !wait_bar<false>(c, &b->k_empty[slot], (use - 1) & 1, W_K_EMPTY)) return false;
       if (leader) {
-        mbar_arrive_expect_tx(&b->k_full[slot], j.np * kChunk);
+        const int atoms = ch < 4 ? 2 : 1;
+        mbar_arrive_expect_tx(&b->k_full[slot], atoms * j.np * kChunk);
         uint8_t *dst = smem + kOffK + slot * kKSlot;
+        for (int at = 0; at < atoms; ++at)
 #pragma unroll
-        for (int p = 0; p < kSB; ++p)
-          if (p < j.np)
-            tma_load_3d(dst + p * kChunk, map, &b->k_full[slot], 64 * ch, j.pg.row0[p], j.pg.page[p]);
+          for (int p = 0; p < kSB; ++p)
+            if (p < j.np)
+              tma_load_3d(dst + at * kAtom + p * kChunk, map, &b->k_full[slot], 128 * ch + 64 * at,
+                          j.pg.row0[p], j.pg.page[p]);
       }
     }
     return true;
@@ -424,6 +438,7 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
   const uint32_t tQ = tmem;
   const uint32_t idesc = idesc_f16(128, kSBTok, Pack<T>::kBf16, false, false);
   const uint64_t qdesc = desc_kmajor_sw128(smem_u32(smem + kOffQ8));
+  static_assert(kOffQ8 % 1024 == 0 && kOffK % 1024 == 0 && kAtom % 1024 == 0, "swizzle atoms");
   const uint64_t kdesc = desc_kmajor_sw128(smem_u32(smem + kOffK));
   const uint32_t kfull = smem_u32(&b->k_full[0]), kempty = smem_u32(&b->k_empty[0]);
   uint32_t slot = 0, phase = 0;  // K ring position of the next chunk and its k_full parity
@@ -442,13 +457,14 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
       tc_fence_after();
     }
 #pragma unroll 1
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 4; ++i) {
       if (!wait_addr<false>(c, kfull + 8 * slot, phase, W_K_FULL)) return;
       tc_fence_after();
       const uint64_t bd = kdesc + (uint64_t)(slot * (kKSlot >> 4));
       if (leader) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_cp_128x256b(tQ + 32 * i + 8 * k, bd + 2 * k);
+        for (int k = 0; k < 8; ++k)
+          tmem_cp_128x256b(tQ + 64 * i + 8 * k, bd + (uint64_t)((k >> 2) * (kAtom >> 4) + 2 * (k & 3)));
         mma_commit_addr(kempty + 8 * slot);
       }
       if (++slot == kNK) {
@@ -466,19 +482,21 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
       }
       const uint32_t tS = tmem + 256 + kSBTok * buf;
 #pragma unroll 1
-      for (int ch = 0; ch < 9; ++ch) {
+      for (int ch = 0; ch < kKChunks; ++ch) {
         prof_chunk(nch, 0);
         if (!wait_addr<false>(c, kfull + 8 * slot, phase, W_K_FULL)) return;
         tc_fence_after();
         prof_chunk(nch, 1);
         const uint64_t bd = kdesc + (uint64_t)(slot * (kKSlot >> 4));
         if (leader) {
+          if (ch < 4) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            if (ch < 8)
-              mma_ts(tS, tQ + 32 * ch + 8 * k, bd + 2 * k, idesc, (ch | k) != 0);
-            else
-              mma_ss(tS, qdesc + 2 * k, bd + 2 * k, idesc, 1);
+            for (int k = 0; k < 8; ++k)
+              mma_ts(tS, tQ + 64 * ch + 8 * k, bd + (uint64_t)((k >> 2) * (kAtom >> 4) + 2 * (k & 3)), idesc,
+                     (ch | k) != 0);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mma_ss(tS, qdesc + 2 * k, bd + 2 * k, idesc, 1);
           }
           mma_commit_addr(kempty + 8 * slot);
         }
@@ -954,6 +972,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
   const uint32_t role = cluster_ctarank();  // 0: score CTA, 1: value CTA
   const int part = blockIdx.x >> 1;
   const int head0 = blockIdx.y * 128;
+  prof_part(0);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNK; ++i) {
@@ -1001,6 +1020,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
   const uint32_t tmem = b->tmem_base;
   const Ctx c{b, a.err};
   prof_role(0);
+  prof_part(1);
 
   if (role == 0) {
     // warp 0: K producer, 1: MMA, 2-9: softmax, 10: P/header copier.  Each role has
@@ -1032,6 +1052,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
   prof_role(1);
   tc_fence_before();
   __syncthreads();
+  prof_part(2);
   cluster_sync();
   if (warp == 1) {
     tc_fence_after();
@@ -1112,6 +1133,10 @@ extern "C" int mla_debug_wait_profile(void *waits, size_t wbytes, void *roles, s
 extern "C" int mla_debug_chunk_trace(void *dst, size_t bytes) {
   if (bytes > sizeof(g_chunk_trace)) bytes = sizeof(g_chunk_trace);
   return cudaMemcpyFromSymbol(dst, g_chunk_trace, bytes) == cudaSuccess ? 0 : -7;
+}
+extern "C" int mla_debug_part_times(void *dst, size_t bytes) {
+  if (bytes > sizeof(g_part_gt)) bytes = sizeof(g_part_gt);
+  return cudaMemcpyFromSymbol(dst, g_part_gt, bytes) == cudaSuccess ? 0 : -7;
 }
 extern "C" int mla_debug_wait_profile_clear(void) {
   static unsigned long long zero[sizeof(g_wait_ns) / 8];
