@@ -1052,6 +1052,13 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
   prof_role(1);
   tc_fence_before();
   __syncthreads();
+  if (*reinterpret_cast<volatile int *>(&b->abort)) {
+    // a wait gave up: let this CTA's TMA loads and the peer's copies into it land
+    // (they complete within microseconds) before the CTAs exit
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 100000ull) {
+    }
+  }
   prof_part(2);
   cluster_sync();
   if (warp == 1) {
