@@ -54,7 +54,7 @@ def load(path=_LIB):
             ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
             ctypes.c_void_p, ctypes.c_double, ctypes.c_int, ctypes.c_int,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-            ctypes.c_void_p]
+            ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_widen.restype = ctypes.c_double
         lib.oracle_widen.argtypes = [ctypes.c_uint16, ctypes.c_int]
         if path == _LIB:
@@ -67,7 +67,7 @@ def _ptr(a):
 
 
 def decode_rows(q, kv, block_table, cache_seqlens, softmax_scale, dtype, rows,
-                threads=1, lib=None):
+                threads=1, lib=None, with_abs=False):
     """Evaluate the definition for the (seq, head) pairs in `rows`.
 
     q            : uint16 [b, h, 576]   (stored bits; seqlen_q = 1 folded)
@@ -75,7 +75,9 @@ def decode_rows(q, kv, block_table, cache_seqlens, softmax_scale, dtype, rows,
     block_table  : int32  [b, max_blocks]
     cache_seqlens: int32  [b]
     rows         : int array [n, 2] of (seq, head)
-    Returns (out float64 [n, 512], lse float64 [n]).
+    Returns (out float64 [n, 512], lse float64 [n]), and with `with_abs` also
+    absw float64 [n, 512] = sum_t p_t |v_t| per column: the scale of the terms
+    each output sums, which bounds the error of any rounding of them.
     """
     lib = lib or load()
     q = np.ascontiguousarray(q, dtype=np.uint16)
@@ -89,6 +91,7 @@ def decode_rows(q, kv, block_table, cache_seqlens, softmax_scale, dtype, rows,
     n = rows.shape[0]
     out = np.zeros((n, DV), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
+    absw = np.zeros((n, DV), dtype=np.float64) if with_abs else None
     code = DTYPES[dtype]
     max_len = int(max(1, sl.max(initial=1)))
 
@@ -99,11 +102,12 @@ def decode_rows(q, kv, block_table, cache_seqlens, softmax_scale, dtype, rows,
         rh = np.ascontiguousarray(rows[lo:hi, 1])
         o = out[lo:hi]
         ls = lse[lo:hi]
+        ab = _ptr(absw[lo:hi]) if with_abs else None
         scratch = np.empty(max_len, dtype=np.float64)
         return lib.oracle_mla_decode_rows(
             b, h, _ptr(q), _ptr(kv), num_pages, page_size, _ptr(bt), bt.shape[1],
             _ptr(sl), float(softmax_scale), code, hi - lo, _ptr(rb), _ptr(rh),
-            _ptr(o), _ptr(ls), _ptr(scratch))
+            _ptr(o), _ptr(ls), _ptr(scratch), ab)
 
     if threads <= 1 or n < 2:
         rc = run(0, n)
@@ -115,7 +119,7 @@ def decode_rows(q, kv, block_table, cache_seqlens, softmax_scale, dtype, rows,
             rcs = list(ex.map(lambda k: run(bounds[k], bounds[k + 1]), range(threads)))
         if any(rcs):
             raise ValueError("oracle: block table or row index out of range")
-    return out, lse
+    return (out, lse, absw) if with_abs else (out, lse)
 
 
 def decode(q, kv, block_table, cache_seqlens, softmax_scale, dtype, threads=1):

@@ -82,14 +82,18 @@ double oracle_widen(uint16_t x, int dtype) { return widen(x, dtype); }
  *   kv          : [num_pages][page_size][576] stored values
  *   table_row   : this sequence's block_table row
  *   out_row     : 512 doubles
+ *   abs_row     : 512 doubles or NULL: sum_t p_t |v_t[d]|, the scale of the terms
+ *                 that out_row[d] sums (the bound of its rounding error)
  *   scores      : scratch, at least seqlen doubles
  * Returns 0, or -1 if the block table points outside the cache.
  */
 static int one_row(const uint16_t *q_row, const uint16_t *kv, int64_t num_pages,
                    int page_size, const int32_t *table_row, int seqlen,
-                   double softmax_scale, int dtype, double *out_row,
+                   double softmax_scale, int dtype, double *out_row, double *abs_row,
                    double *lse_out, double *scores) {
   for (int d = 0; d < MLA_DV; ++d) out_row[d] = 0.0;
+  if (abs_row)
+    for (int d = 0; d < MLA_DV; ++d) abs_row[d] = 0.0;
   if (seqlen <= 0) {
     *lse_out = -INFINITY;
     return 0;
@@ -113,6 +117,8 @@ static int one_row(const uint16_t *q_row, const uint16_t *kv, int64_t num_pages,
     const uint16_t *v = kv + ((int64_t)page * page_size + t % page_size) * MLA_D;
     double p = exp(scores[t] - m) / z;
     for (int d = 0; d < MLA_DV; ++d) out_row[d] += p * widen(v[d], dtype);
+    if (abs_row)
+      for (int d = 0; d < MLA_DV; ++d) abs_row[d] += p * fabs(widen(v[d], dtype));
   }
   *lse_out = m + log(z);
   return 0;
@@ -127,6 +133,8 @@ static int one_row(const uint16_t *q_row, const uint16_t *kv, int64_t num_pages,
  *   row_b, row_h : n_rows (sequence, head) pairs to evaluate
  *   out          : [n_rows][512] doubles
  *   lse          : [n_rows] doubles
+ *   absw         : [n_rows][512] doubles or NULL: the softmax-weighted mean of
+ *                  |v| per column (see one_row)
  *   scratch      : at least max(cache_seqlens) doubles
  * Returns 0 on success, -1 on an out-of-range page or row index.
  */
@@ -136,7 +144,7 @@ int oracle_mla_decode_rows(int b, int h, const uint16_t *q, const uint16_t *kv,
                            const int32_t *cache_seqlens, double softmax_scale,
                            int dtype, int n_rows, const int32_t *row_b,
                            const int32_t *row_h, double *out, double *lse,
-                           double *scratch) {
+                           double *scratch, double *absw) {
   for (int r = 0; r < n_rows; ++r) {
     int bi = row_b[r], hi = row_h[r];
     if (bi < 0 || bi >= b || hi < 0 || hi >= h) return -1;
@@ -144,7 +152,8 @@ int oracle_mla_decode_rows(int b, int h, const uint16_t *q, const uint16_t *kv,
     if (L > max_blocks * page_size) return -1;
     int rc = one_row(q + ((int64_t)bi * h + hi) * MLA_D, kv, num_pages, page_size,
                      block_table + (int64_t)bi * max_blocks, L, softmax_scale, dtype,
-                     out + (int64_t)r * MLA_DV, lse + r, scratch);
+                     out + (int64_t)r * MLA_DV, absw ? absw + (int64_t)r * MLA_DV : 0, lse + r,
+                     scratch);
     if (rc) return rc;
   }
   return 0;

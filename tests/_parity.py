@@ -5,11 +5,13 @@ Tolerances (bf16/fp16 inputs, fp32 accumulation): out max-abs 2e-2 and
 mean-abs 2e-3; lse max-abs 1e-3 (natural log); an empty sequence must give
 out == 0 and lse == -inf exactly.
 
-The out bounds are applied to the error measured in units of the output's own
-scale, |gpu - ref| / max(1, |ref|): identical to the absolute bound for
-unit-scale outputs (every N(0,1) workload), and still meaningful when rows
-scaled x8 make |out| reach ~30, where merely storing the exact value in bf16
-can be off by 2^-8 * |out| ~ 0.06.
+The out bounds are applied to the error measured in units of the scale of the
+terms each output element sums: |gpu - ref| / max(1, w), w = sum_t p_t |v_t|
+(the oracle's weighted-absolute output, the forward-error bound of a weighted
+sum).  For unit-scale data w < 1 and this is exactly the absolute bound (every
+N(0,1) workload).  Where rows scaled x8 dominate, the terms reach |p v| ~ 24 and
+rounding each weight to 16 bits, at a running max of the kernel's choosing,
+moves an output by ~2^-9 * 24 even when the terms cancel to |out| < 1.
 """
 import os
 
@@ -37,7 +39,8 @@ def run_gpu(inputs, heads, scale, num_sm=None):
 
 
 def oracle_rows(w, inputs, seqs=None):
-    """Oracle out [n_seq, h, 512] and lse [n_seq, h] for sequences `seqs` (all if None)."""
+    """Oracle out [n_seq, h, 512], lse [n_seq, h] and the weighted-absolute scale
+    [n_seq, h, 512] for sequences `seqs` (all if None)."""
     q = inputs["q"]
     kv = inputs["kv_cache"]
     bt = inputs["block_table"].cpu().numpy()
@@ -54,20 +57,22 @@ def oracle_rows(w, inputs, seqs=None):
     q_c = workloads.to_bits(q[torch.as_tensor(seqs, device=q.device), 0])
     rows = np.stack(np.meshgrid(np.arange(len(seqs)), np.arange(w.heads), indexing="ij"),
                     -1).reshape(-1, 2)
-    out, lse = oracle.decode_rows(q_c, kv_c, table_c, sl_c, w.softmax_scale, w.dtype, rows,
-                                  threads=ORACLE_THREADS)
-    return out.reshape(len(seqs), w.heads, -1), lse.reshape(len(seqs), w.heads)
+    out, lse, absw = oracle.decode_rows(q_c, kv_c, table_c, sl_c, w.softmax_scale, w.dtype, rows,
+                                        threads=ORACLE_THREADS, with_abs=True)
+    return (out.reshape(len(seqs), w.heads, -1), lse.reshape(len(seqs), w.heads),
+            absw.reshape(len(seqs), w.heads, -1))
 
 
-def compare(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
-    """out_gpu [n, h, 512] (any float dtype), lse_gpu [n, h]; refs float64 numpy."""
+def compare(out_gpu, lse_gpu, out_ref, lse_ref, abs_ref, what=""):
+    """out_gpu [n, h, 512] (any float dtype), lse_gpu [n, h]; refs float64 numpy
+    (abs_ref: the oracle's weighted-absolute scale of each output)."""
     og = out_gpu.float().cpu().numpy().astype(np.float64)
     lg = lse_gpu.float().cpu().numpy().astype(np.float64)
     empty = np.isneginf(lse_ref)
     assert np.all(np.isneginf(lg[empty])), f"{what}: empty rows must have lse -inf"
     assert np.all(og[empty] == 0), f"{what}: empty rows must be zero"
     assert np.all(np.isfinite(og)), f"{what}: non-finite output"
-    err = np.abs(og - out_ref) / np.maximum(1.0, np.abs(out_ref))
+    err = np.abs(og - out_ref) / np.maximum(1.0, abs_ref)
     mx, mean = float(err.max(initial=0.0)), float(err.mean()) if err.size else 0.0
     full = ~empty
     lerr = float(np.abs(lg[full] - lse_ref[full]).max(initial=0.0))
@@ -82,9 +87,9 @@ def check_workload(w, seqs=None, num_sm=None, poison_tail=False, inputs=None):
     if inputs is None:
         inputs = workloads.make_inputs(w, device="cuda", poison_tail=poison_tail)
     out, lse, meta, ns = run_gpu(inputs, w.heads, w.softmax_scale, num_sm)
-    ref_o, ref_l = oracle_rows(w, inputs, seqs)
+    ref_o, ref_l, ref_a = oracle_rows(w, inputs, seqs)
     idx = torch.as_tensor(list(range(w.batch)) if seqs is None else list(seqs), device=out.device)
-    stats = compare(out[idx, 0], lse[idx], ref_o, ref_l, what=w.name)
+    stats = compare(out[idx, 0], lse[idx], ref_o, ref_l, ref_a, what=w.name)
     log = os.environ.get("MLA_PARITY_LOG")
     if log:
         import json

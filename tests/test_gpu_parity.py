@@ -108,7 +108,7 @@ def test_split_config_full_size_split_vs_unsplit():
     w = workloads.get("split")
     seqs = workloads.sample_seqs(w, 8)
     inputs = workloads.make_inputs(w, "cuda")
-    ref_o, ref_l = P.oracle_rows(w, inputs, seqs)
+    ref_o, ref_l, ref_a = P.oracle_rows(w, inputs, seqs)
     idx = torch.as_tensor(seqs, device="cuda")
     results = {}
     for label, num_sm in (("default", None), ("many", 1024), ("one", 2)):
@@ -118,7 +118,7 @@ def test_split_config_full_size_split_vs_unsplit():
             assert int(per_seq.min()) >= 4   # at least four splits per sequence
         if label == "one":
             assert int(per_seq.max()) == 1   # num_split = 1
-        P.compare(out[idx, 0], lse[idx], ref_o, ref_l, what=f"split/{label}")
+        P.compare(out[idx, 0], lse[idx], ref_o, ref_l, ref_a, what=f"split/{label}")
         results[label] = (out, lse)
     for label in ("default", "many"):
         assert (results[label][0].float() - results["one"][0].float()).abs().max().item() <= P.OUT_MAX_ABS

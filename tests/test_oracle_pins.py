@@ -9,7 +9,9 @@ different statement of the same operation:
   * invariants: page permutation, token permutation, head independence,
     softmax shift, and split + combine (the log-sum-exp merge of the TileLang
     MLA guide's combine kernel) equalling the unsplit result;
-  * the 16-bit widening checked exhaustively against numpy / torch.
+  * the 16-bit widening checked exhaustively against numpy / torch;
+  * the weighted-absolute output (sum_t p_t |v_t|, the scale of the terms each
+    output sums) against brute force, its closed forms and |out| <= absw.
 Finally, mutants of the oracle source (a dropped RoPE term, v from the wrong
 columns, a wrong page index, a missing max in lse, ...) must each fail a pin.
 """
@@ -75,6 +77,15 @@ def run_oracle(lib, q, kv, table, seqlens, scale, dtype):
     out, lse = oracle.decode_rows(qq, kv, table, np.asarray(seqlens, np.int32), scale, dtype,
                                   rows, lib=lib)
     return out.reshape(b, h, DV), lse.reshape(b, h)
+
+
+def run_oracle_abs(lib, q, kv, table, seqlens, scale, dtype):
+    qq = np.asarray(q).reshape(q.shape[0], q.shape[1], D)
+    b, h = qq.shape[:2]
+    rows = np.stack(np.meshgrid(np.arange(b), np.arange(h), indexing="ij"), -1).reshape(-1, 2)
+    out, lse, absw = oracle.decode_rows(qq, kv, table, np.asarray(seqlens, np.int32), scale, dtype,
+                                        rows, lib=lib, with_abs=True)
+    return out.reshape(b, h, DV), absw.reshape(b, h, DV)
 
 
 # ----------------------------------------------------------------------------------------
@@ -297,9 +308,38 @@ def pin_batch_rows(lib):
     return True
 
 
+def pin_abs_weights(lib):
+    """sum_t p_t |v_t| per column: brute force (naive softmax, math.fsum), its closed
+    forms (one token: |v|; identical scores: the mean of |v_t|) and |out| <= absw."""
+    rng = np.random.default_rng(21)
+    lens = (1, 50)
+    scale = 0.07
+    logical = [bits(rng.standard_normal((L, D)), "bf16") for L in lens]
+    q = bits(rng.standard_normal((2, 2, D)), "bf16")
+    kv, table = paged(logical, 16, rng)
+    out, absw = run_oracle_abs(lib, q, kv, table, lens, scale, "bf16")
+    if not np.array_equal(absw[0, 0], np.abs(vals(logical[0][0], "bf16"))[:DV]):
+        return False
+    if np.any(np.abs(out) > absw * (1 + 1e-12) + 1e-300):
+        return False
+    lv = vals(logical[1], "bf16")
+    for j in range(2):
+        qv = vals(q[1, j], "bf16")
+        s_ = [scale * math.fsum(qv * r) for r in lv]
+        w = [math.exp(x) for x in s_]
+        z = math.fsum(w)
+        ref = np.array([math.fsum(w[t] * abs(lv[t][d]) for t in range(len(w))) / z for d in range(DV)])
+        if not np.allclose(absw[1, j], ref, rtol=1e-11, atol=1e-13):
+            return False
+    # identical scores: q = 0 gives every token the same weight
+    q0 = np.zeros((2, 1, D), dtype=np.uint16)
+    _, absw0 = run_oracle_abs(lib, q0, kv, table, lens, scale, "bf16")
+    return np.allclose(absw0[1, 0], np.abs(lv).mean(axis=0)[:DV], rtol=1e-12, atol=1e-14)
+
+
 PINS = [pin_brute_force, pin_len_one, pin_identical_scores, pin_zero_query, pin_two_tokens,
         pin_dominant_token, pin_empty_sequence, pin_page_permutation, pin_token_permutation,
-        pin_head_independence, pin_softmax_shift, pin_split_combine, pin_batch_rows]
+        pin_head_independence, pin_softmax_shift, pin_split_combine, pin_batch_rows, pin_abs_weights]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -355,6 +395,8 @@ MUTANTS = {
     "q_row_transposed": ("q + ((int64_t)bi * h + hi) * MLA_D", "q + ((int64_t)hi * b + bi) * MLA_D"),
     "first_token_skipped": ("for (int t = 0; t < seqlen; ++t) z +=",
                             "for (int t = 1; t < seqlen; ++t) z +="),
+    "abs_sign_kept": ("abs_row[d] += p * fabs(widen(v[d], dtype));", "abs_row[d] += p * widen(v[d], dtype);"),
+    "abs_unweighted": ("abs_row[d] += p * fabs(widen(v[d], dtype));", "abs_row[d] += fabs(widen(v[d], dtype));"),
 }
 
 
