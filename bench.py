@@ -65,7 +65,9 @@ def measured_peaks():
 
 
 def kernel_source_hash():
-    files = sorted(glob.glob(os.path.join(ROOT, "mla_decode_gb300", "csrc", "*")))
+    """Hash of the split kernel's sources (the kernel the roofline line reports)."""
+    csrc = os.path.join(ROOT, "mla_decode_gb300", "csrc")
+    files = [os.path.join(csrc, f) for f in ("common.cuh", "internal.h", "sm100.cuh", "split_sm103.cu")]
     h = hashlib.sha256()
     for f in files:
         h.update(os.path.basename(f).encode())

@@ -44,27 +44,47 @@ combine_kernel(FwdArgs a) {
   float4 acc[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = 0; k < n; ++k) {
-    const int64_t sp = (int64_t)(s0 + k) * a.h + head;
-    const float w = (lse == -INFINITY) ? 0.f : fast_exp2(a.lseaccum[sp] - lse);
-    const float4 *src = reinterpret_cast<const float4 *>(a.oaccum + sp * MLA_HEAD_DIM_V);
+  auto add = [&](float w, const float4 (&v)[4]) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      float4 v = src[lane + 32 * c];
-      acc[c].x = fmaf(w, v.x, acc[c].x);
-      acc[c].y = fmaf(w, v.y, acc[c].y);
-      acc[c].z = fmaf(w, v.z, acc[c].z);
-      acc[c].w = fmaf(w, v.w, acc[c].w);
+      acc[c].x = fmaf(w, v[c].x, acc[c].x);
+      acc[c].y = fmaf(w, v[c].y, acc[c].y);
+      acc[c].z = fmaf(w, v[c].z, acc[c].z);
+      acc[c].w = fmaf(w, v[c].w, acc[c].w);
     }
+  };
+  // two splits per step, all of their loads issued before any use
+  int k = 0;
+  for (; k + 1 < n; k += 2) {
+    const int64_t sp0 = (int64_t)(s0 + k) * a.h + head, sp1 = sp0 + a.h;
+    const float4 *src0 = reinterpret_cast<const float4 *>(a.oaccum + sp0 * MLA_HEAD_DIM_V);
+    const float4 *src1 = reinterpret_cast<const float4 *>(a.oaccum + sp1 * MLA_HEAD_DIM_V);
+    float4 v0[4], v1[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      v0[c] = src0[lane + 32 * c];
+      v1[c] = src1[lane + 32 * c];
+    }
+    const float l0 = a.lseaccum[sp0], l1 = a.lseaccum[sp1];
+    add(lse == -INFINITY ? 0.f : fast_exp2(l0 - lse), v0);
+    add(lse == -INFINITY ? 0.f : fast_exp2(l1 - lse), v1);
   }
+  if (k < n) {
+    const int64_t sp = (int64_t)(s0 + k) * a.h + head;
+    const float4 *src = reinterpret_cast<const float4 *>(a.oaccum + sp * MLA_HEAD_DIM_V);
+    float4 v[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) v[c] = src[lane + 32 * c];
+    add(lse == -INFINITY ? 0.f : fast_exp2(a.lseaccum[sp] - lse), v);
+  }
+  // four consecutive 16-bit outputs per lane and column group: one 8-byte store
   T *o = reinterpret_cast<T *>(a.out) + seq * a.o_batch_stride + (int64_t)head * a.o_head_stride;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int d = 4 * lane + 128 * c;
-    o[d + 0] = Elem<T>::from_f(acc[c].x);
-    o[d + 1] = Elem<T>::from_f(acc[c].y);
-    o[d + 2] = Elem<T>::from_f(acc[c].z);
-    o[d + 3] = Elem<T>::from_f(acc[c].w);
+    T q4[4] = {Elem<T>::from_f(acc[c].x), Elem<T>::from_f(acc[c].y), Elem<T>::from_f(acc[c].z),
+               Elem<T>::from_f(acc[c].w)};
+    *reinterpret_cast<uint2 *>(o + d) = *reinterpret_cast<const uint2 *>(q4);
   }
   if (lane == 0) a.lse[seq * a.lse_stride + head] = lse * kLn2;
 }

@@ -13,7 +13,7 @@
 //   Segments are numbered in (sequence, block) order; the number of segments
 //   before cut k is cut_seq + (distinct interior cuts among cuts[0..k]).
 //
-// One CTA; every phase is a simple loop, so the kernel costs a few us.
+// One CTA; block scans in shared memory, no serial pass over the batch.
 #include <stdint.h>
 
 #include "common.cuh"
@@ -22,6 +22,39 @@ namespace mla {
 namespace {
 
 constexpr int kMetaThreads = 512;
+constexpr int kMetaWarps = kMetaThreads / 32;
+
+__device__ __forceinline__ int cost_of(const int32_t *seqlens, int i, int fixed) {
+  const int L = seqlens[i];
+  return fixed + (L > 0 ? (L + 63) / 64 : 0);
+}
+
+// Exclusive prefix of v over the block (all threads call it); *total gets the sum.
+__device__ int64_t block_exclusive_scan(int64_t v, int64_t *warp_sums, int64_t *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = lane < kMetaWarps ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kMetaWarps) warp_sums[lane] = w;  // inclusive
+  }
+  __syncthreads();
+  const int64_t excl = x - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+  *total = warp_sums[kMetaWarps - 1];
+  __syncthreads();  // warp_sums is reused by the next call
+  return excl;
+}
 
 __global__ void __launch_bounds__(kMetaThreads)
 metadata_kernel(const int32_t *__restrict__ seqlens, int b, int parts, int fixed,
@@ -30,56 +63,46 @@ metadata_kernel(const int32_t *__restrict__ seqlens, int b, int parts, int fixed
   int32_t *cut_seq = sh;                    // [parts + 1]
   int32_t *cut_blk = cut_seq + parts + 1;   // [parts + 1]
   int32_t *rank = cut_blk + parts + 1;      // [parts + 1]
-  __shared__ int64_t chunk_sum[kMetaThreads];
+  __shared__ int64_t chunk_start[kMetaThreads];
+  __shared__ int64_t warp_sums[kMetaWarps];
   const int tid = threadIdx.x;
 
-  // Phase 1: exclusive prefix of per-sequence cost, kept in num_splits[0..b-1]
-  // for the moment; TOTAL in num_splits[b].
+  // Phase 1: thread t owns sequences [t per, (t + 1) per); the block scan of the
+  // chunk costs gives each chunk's start on the cost axis, and TOTAL.
   const int per = (b + kMetaThreads - 1) / kMetaThreads;
+  const int nchunks = (b + per - 1) / per;
   const int lo = min(b, tid * per), hi = min(b, lo + per);
   int64_t s = 0;
-  for (int i = lo; i < hi; ++i) {
-    int L = seqlens[i];
-    s += fixed + (L > 0 ? (L + 63) / 64 : 0);
-  }
-  chunk_sum[tid] = s;
+  for (int i = lo; i < hi; ++i) s += cost_of(seqlens, i, fixed);
+  int64_t total = 0;
+  chunk_start[tid] = block_exclusive_scan(s, warp_sums, &total);
   __syncthreads();
-  if (tid == 0) {
-    int64_t acc = 0;
-    for (int t = 0; t < kMetaThreads; ++t) {
-      int64_t v = chunk_sum[t];
-      chunk_sum[t] = acc;
-      acc += v;
-    }
-    num_splits[b] = (int32_t)acc;
-  }
-  __syncthreads();
-  {
-    int64_t acc = chunk_sum[tid];
-    for (int i = lo; i < hi; ++i) {
-      num_splits[i] = (int32_t)acc;
-      int L = seqlens[i];
-      acc += fixed + (L > 0 ? (L + 63) / 64 : 0);
-    }
-  }
-  __syncthreads();
-  const int64_t total = num_splits[b];
 
-  // Phase 2: the cut of each part.
+  // Phase 2: the cut of each part.  The sequence is the last one whose start is
+  // <= x: the last chunk whose start is <= x, then a walk inside it.
   for (int k = tid; k <= parts; k += kMetaThreads) {
-    int64_t x = (k == parts) ? total : ((int64_t)k * total) / parts;
+    const int64_t x = (k == parts) ? total : ((int64_t)k * total) / parts;
     int ci, cb;
     if (x >= total) {
       ci = b;
       cb = 0;
     } else {
-      int lo_i = 0, hi_i = b - 1;  // last i with start_i <= x
-      while (lo_i < hi_i) {
-        int mid = (lo_i + hi_i + 1) >> 1;
-        if ((int64_t)num_splits[mid] <= x) lo_i = mid; else hi_i = mid - 1;
+      int lo_t = 0, hi_t = nchunks - 1;
+      while (lo_t < hi_t) {
+        const int mid = (lo_t + hi_t + 1) >> 1;
+        if (chunk_start[mid] <= x) lo_t = mid; else hi_t = mid - 1;
       }
-      ci = lo_i;
-      int64_t off = x - (int64_t)num_splits[ci] - fixed;
+      int i = lo_t * per;
+      const int end = min(b, i + per);
+      int64_t start = chunk_start[lo_t];
+      for (;;) {
+        const int64_t next = start + cost_of(seqlens, i, fixed);
+        if (i + 1 >= end || next > x) break;
+        start = next;
+        ++i;
+      }
+      ci = i;
+      const int64_t off = x - start - fixed;
       cb = off > 0 ? (int)off : 0;
     }
     cut_seq[k] = ci;
@@ -87,15 +110,18 @@ metadata_kernel(const int32_t *__restrict__ seqlens, int b, int parts, int fixed
   }
   __syncthreads();
 
-  // Phase 3: running count of distinct interior cuts.
-  if (tid == 0) {
-    int r = 0;
-    for (int k = 0; k <= parts; ++k) {
-      bool inner = cut_blk[k] > 0 &&
-                   (k == 0 || cut_seq[k] != cut_seq[k - 1] || cut_blk[k] != cut_blk[k - 1]);
-      r += inner ? 1 : 0;
-      rank[k] = r;
-    }
+  // Phase 3: running count of distinct interior cuts (a block scan per 512 cuts).
+  int64_t carry = 0;
+  for (int base = 0; base <= parts; base += kMetaThreads) {
+    const int k = base + tid;
+    int inner = 0;
+    if (k <= parts)
+      inner = cut_blk[k] > 0 &&
+              (k == 0 || cut_seq[k] != cut_seq[k - 1] || cut_blk[k] != cut_blk[k - 1]);
+    int64_t sum = 0;
+    const int64_t excl = block_exclusive_scan(inner, warp_sums, &sum);
+    if (k <= parts) rank[k] = (int32_t)(carry + excl + inner);
+    carry += sum;
   }
   __syncthreads();
 
@@ -103,13 +129,13 @@ metadata_kernel(const int32_t *__restrict__ seqlens, int b, int parts, int fixed
   for (int i = tid; i <= b; i += kMetaThreads) {
     int lo_k = 0, hi_k = parts + 1;  // first k with cut_seq[k] >= i
     while (lo_k < hi_k) {
-      int mid = (lo_k + hi_k) >> 1;
+      const int mid = (lo_k + hi_k) >> 1;
       if (cut_seq[mid] < i) lo_k = mid + 1; else hi_k = mid;
     }
     num_splits[i] = i + (lo_k > 0 ? rank[lo_k - 1] : 0);
   }
   for (int k = tid; k < parts; k += kMetaThreads) {
-    int32_t *row = meta + (int64_t)k * MLA_META_STRIDE;
+    int32_t *row = meta + (int64_t)k * MLA_META_STRIDE;  // (4-byte alignment only)
     row[0] = cut_seq[k];
     row[1] = cut_blk[k];
     row[2] = cut_seq[k + 1];
