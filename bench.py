@@ -50,7 +50,20 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (smaller cases for profiler captures)")
+    ap.add_argument("--layout", choices=["fused", "split"], default="fused",
+                    help="fused: 576-column q / kv_cache rows; split: Q / Q_pe and KV / K_pe "
+                         "as separate tensors")
     return ap.parse_args()
+
+
+def as_layout(s, layout):
+    """The decode tensors of input set `s` in the chosen layout (q_pe / k_pe None when fused)."""
+    d = dict(s, q_pe=None, k_pe=None)
+    if layout == "split":
+        q, kv = s["q"], s["kv_cache"]
+        d.update(q=q[..., :512].contiguous(), q_pe=q[..., 512:].contiguous(),
+                 kv_cache=kv[..., :512].contiguous(), k_pe=kv[..., 512:].contiguous())
+    return d
 
 
 # ------------------------------------------------------------------------------- helpers
@@ -302,6 +315,8 @@ def run_ours(args):
     for _ in range(max(0, args.copies - 1)):
         sets.append({"q": base["q"].clone(), "kv_cache": base["kv_cache"].clone(),
                      "block_table": base["block_table"], "cache_seqlens": base["cache_seqlens"]})
+    sets = [as_layout(s, args.layout) for s in sets]
+    base = sets[0]
     num_sm = mla.mla_device_num_sm(local)
     parts, stride = mla.mla_metadata_shape(w.batch, w.heads, num_sm)
     meta = torch.empty((parts, stride), dtype=torch.int32, device=dev)
@@ -311,7 +326,8 @@ def run_ours(args):
     out = torch.empty((w.batch, 1, w.heads, 512), dtype=w.torch_dtype, device=dev)
     lse = torch.empty((w.batch, w.heads), dtype=torch.float32, device=dev)
     calls = [mla.prepare_decode(s["q"], s["kv_cache"], s["block_table"], s["cache_seqlens"],
-                                w.softmax_scale, meta, nsplit, out, lse, ws) for s in sets]
+                                w.softmax_scale, meta, nsplit, out, lse, ws, q_pe=s["q_pe"],
+                                k_pe=s["k_pe"]) for s in sets]
 
     def step(i, events=None):
         s = sets[i % len(sets)]
@@ -357,13 +373,13 @@ def run_ours(args):
         ms = float(t.item())
 
     # ---- end to end through the public API with pinned host buffers
-    host = {k: v.cpu().pin_memory() for k, v in base.items()}
-    dbuf = {k: torch.empty_like(v) for k, v in base.items()}
+    host = {k: v.cpu().pin_memory() for k, v in base.items() if v is not None}
+    dbuf = {k: torch.empty_like(base[k]) for k in host}
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     e2e_call = mla.prepare_decode(dbuf["q"], dbuf["kv_cache"], dbuf["block_table"],
                                   dbuf["cache_seqlens"], w.softmax_scale, meta, nsplit, out, lse,
-                                  ws)
+                                  ws, q_pe=dbuf.get("q_pe"), k_pe=dbuf.get("k_pe"))
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
 
@@ -412,7 +428,8 @@ def run_ours(args):
                    "block_table": "seeded random permutation", "softmax_scale": w.softmax_scale,
                    "l2": f"{len(sets)} rotating input sets, KV "
                          f"{w.total_tokens * 576 * 2 / 1e6:.0f} MB each (> 129 MB L2)",
-                   "parallelism": f"replicas x{world}", "num_sm_parts": parts},
+                   "parallelism": f"replicas x{world}", "num_sm_parts": parts,
+                   "layout": args.layout},
         "effective_hbm_gbs": world * nbytes / (ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic, "kernel": "split",

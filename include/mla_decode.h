@@ -19,8 +19,9 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Work is enqueued asynchronously; no entry point synchronises
  *     except mla_get_device_error.
- *   - Strides are in ELEMENTS.  Element types: q / kv_cache / out are fp16 or
- *     bf16 (the same for all three); lse, the workspace are fp32; tables int32.
+ *   - Strides are in ELEMENTS.  Element types: q / kv_cache / out (and q_pe /
+ *     k_pe) are fp16 or bf16 (the same for all); lse, the workspace are fp32;
+ *     tables int32.
  *   - Argument errors are detected on the host, before any launch, and return
  *     a negative mla_status without touching the GPU.  Launch failures return
  *     MLA_ERR_CUDA.  Faults the kernels detect while running (a block-table
@@ -37,7 +38,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 1
+#define MLA_ABI_VERSION 2
 
 /* Shape contract [TL §先看核心难点]: 576 = 512 latent + 64 RoPE; v = 512. */
 #define MLA_HEAD_DIM 576
@@ -79,6 +80,19 @@ enum { MLA_DTYPE_FP16 = 0, MLA_DTYPE_BF16 = 1 };
  *                                      i is row t % page_block_size of page
  *                                      block_table[i][t / page_block_size]
  *                                      [TL §变体内核].
+ *   q_pe, k_pe   optional split layout [TL §Split Kernel: Q / Q_pe and
+ *                KV / K_pe are separate tensors, and the score is
+ *                Q.KV^T + Q_pe.K_pe^T].  When q_pe is non-NULL, q holds only
+ *                the 512 latent columns ([b][1][h][512], same strides) and
+ *                q_pe [b][1][h][64] the RoPE columns (strides
+ *                q_pe_batch_stride, q_pe_head_stride).  When k_pe is
+ *                non-NULL, kv_cache rows hold only the 512 latent columns
+ *                (which are also the value) and k_pe
+ *                [num_pages][page_block_size][1][64] the RoPE columns (strides
+ *                k_pe_page_stride, k_pe_row_stride; same pages, same block
+ *                table).  Either may be given without the other; NULL means
+ *                the RoPE columns are columns 512..575 of q / kv_cache, and
+ *                the four stride fields of a NULL pointer are ignored.
  *   block_table  int32 [b][max_blocks_per_seq], row stride
  *                block_table_batch_stride.  Only the first
  *                ceil(L_i / page_block_size) entries of row i are read; each
@@ -134,6 +148,12 @@ typedef struct mla_fwd_params {
 
   void *workspace;
   size_t workspace_bytes;
+
+  /* split layout (see above); NULL = RoPE columns inside q / kv_cache */
+  const void *q_pe;
+  int64_t q_pe_batch_stride, q_pe_head_stride;
+  const void *k_pe;
+  int64_t k_pe_page_stride, k_pe_row_stride;
 } mla_fwd_params;
 
 /* ABI version (MLA_ABI_VERSION) and sizeof(mla_fwd_params), for bindings. */
@@ -185,8 +205,11 @@ int mla_workspace_size(int b, int h, int num_sm_parts, size_t *bytes);
  * Paged split-KV MLA decode [TL §Split Kernel, §Combine Kernel, §变体内核;
  * FM §内存访问优化, §Softmax 计算优化].  Enqueues the split kernel (a
  * persistent grid of 2-CTA clusters walking the metadata) and the combine
- * kernel on `stream`.  Alignment: q, kv_cache, out, workspace 16-byte
- * aligned; q/kv/out strides multiples of 8 elements.
+ * kernel on `stream`.  Alignment: q, kv_cache, out, workspace (and q_pe,
+ * k_pe when given) 16-byte aligned; all their strides multiples of 8
+ * elements.  Row strides must cover the row: kv_row_stride >= 576 (>= 512
+ * with k_pe), k_pe_row_stride >= 64, each page stride >= page_block_size
+ * times its row stride.
  */
 int mla_decode_fwd(const mla_fwd_params *params, void *stream);
 

@@ -19,12 +19,14 @@ __all__ = [
     "MlaError", "mla_abi_version", "mla_status_string", "mla_device_num_sm",
     "mla_metadata_shape", "mla_get_metadata", "mla_workspace_size", "mla_decode_fwd",
     "mla_decode_fwd_timed", "prepare_decode", "DecodeCall",
-    "mla_get_device_error", "library_path", "HEAD_DIM", "HEAD_DIM_V", "BLOCK_N",
+    "mla_get_device_error", "library_path", "HEAD_DIM", "HEAD_DIM_V", "ROPE_DIM", "BLOCK_N",
     "META_STRIDE", "SCHED_FIXED_COST",
 ]
 
 HEAD_DIM = 576
 HEAD_DIM_V = 512
+ROPE_DIM = HEAD_DIM - HEAD_DIM_V
+ABI_VERSION = 2
 BLOCK_N = 64
 META_STRIDE = 8
 SCHED_FIXED_COST = 5
@@ -56,6 +58,8 @@ class FwdParams(ctypes.Structure):
         ("lse", _vp), ("lse_batch_stride", _i64),
         ("tile_scheduler_metadata", _vp), ("num_splits", _vp), ("num_sm_parts", _i32),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+        ("q_pe", _vp), ("q_pe_batch_stride", _i64), ("q_pe_head_stride", _i64),
+        ("k_pe", _vp), ("k_pe_page_stride", _i64), ("k_pe_row_stride", _i64),
     ]
 
 
@@ -93,7 +97,7 @@ def _load():
                  "mla_workspace_size", "mla_decode_fwd", "mla_decode_fwd_timed",
                  "mla_get_device_error"):
         getattr(lib, name).restype = ctypes.c_int
-    if lib.mla_abi_version() != 1 or lib.mla_fwd_params_size() != ctypes.sizeof(FwdParams):
+    if lib.mla_abi_version() != ABI_VERSION or lib.mla_fwd_params_size() != ctypes.sizeof(FwdParams):
         raise ImportError("MLA decode library ABI mismatch; rebuild it")
     _lib = lib
     return lib
@@ -171,14 +175,15 @@ def mla_workspace_size(b, h, num_sm_parts):
 
 def mla_decode_fwd(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                    tile_scheduler_metadata, num_splits, out=None, lse=None, workspace=None,
-                   split_events=None):
+                   split_events=None, q_pe=None, k_pe=None):
     """Paged split-KV MLA decode (see prepare_decode for the argument contract).
 
     split_events: optional (begin, end) torch.cuda.Event pair recorded around the
     split kernel (mla_decode_fwd_timed).  Returns (out, lse).
     """
     call = prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
-                          tile_scheduler_metadata, num_splits, out, lse, workspace)
+                          tile_scheduler_metadata, num_splits, out, lse, workspace,
+                          q_pe=q_pe, k_pe=k_pe)
     call(split_events=split_events)
     return call.out, call.lse
 
@@ -209,28 +214,45 @@ class DecodeCall:
 
 
 def prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
-                   tile_scheduler_metadata, num_splits, out=None, lse=None, workspace=None):
+                   tile_scheduler_metadata, num_splits, out=None, lse=None, workspace=None,
+                   q_pe=None, k_pe=None):
     """Paged split-KV MLA decode.
 
     q [b, 1, h, 576], kv_cache [num_pages, page_size, 1, 576] (fp16 or bf16, same
     dtype), block_table int32 [b, max_blocks], cache_seqlens int32 [b], metadata
     from mla_get_metadata.  Returns (out [b, 1, h, 512] in q's dtype, lse fp32 [b, h]
     natural-log).  Launches on the current stream of q's device.
+
+    Split layout: with q_pe [b, 1, h, 64] given, q is [b, 1, h, 512] (latent
+    columns only); with k_pe [num_pages, page_size, 1, 64] given, kv_cache is
+    [num_pages, page_size, 1, 512].  The score is then q . kv + q_pe . k_pe.
     """
-    if q.dim() != 4 or q.shape[1] != 1 or q.shape[3] != HEAD_DIM:
-        raise ValueError("q must be [b, 1, h, 576]")
-    if kv_cache.dim() != 4 or kv_cache.shape[2] != 1 or kv_cache.shape[3] != HEAD_DIM:
-        raise ValueError("kv_cache must be [num_pages, page_size, 1, 576]")
+    q_cols = HEAD_DIM_V if q_pe is not None else HEAD_DIM
+    kv_cols = HEAD_DIM_V if k_pe is not None else HEAD_DIM
+    if q.dim() != 4 or q.shape[1] != 1 or q.shape[3] != q_cols:
+        raise ValueError(f"q must be [b, 1, h, {q_cols}]")
+    if kv_cache.dim() != 4 or kv_cache.shape[2] != 1 or kv_cache.shape[3] != kv_cols:
+        raise ValueError(f"kv_cache must be [num_pages, page_size, 1, {kv_cols}]")
     if q.dtype not in _DTYPE_CODE or kv_cache.dtype != q.dtype:
         raise ValueError("q and kv_cache must share dtype fp16 or bf16")
+    if q_pe is not None and (q_pe.dim() != 4 or tuple(q_pe.shape) != (q.shape[0], 1, q.shape[2],
+                                                                       ROPE_DIM)):
+        raise ValueError("q_pe must be [b, 1, h, 64]")
+    if k_pe is not None and (k_pe.dim() != 4 or tuple(k_pe.shape) != (kv_cache.shape[0],
+                                                                       kv_cache.shape[1], 1,
+                                                                       ROPE_DIM)):
+        raise ValueError("k_pe must be [num_pages, page_size, 1, 64]")
+    for name, t in (("q_pe", q_pe), ("k_pe", k_pe)):
+        if t is not None and (t.dtype != q.dtype or t.stride(3) != 1):
+            raise ValueError(f"{name} must have q's dtype and contiguous columns")
     for name, t in (("q", q), ("kv_cache", kv_cache), ("block_table", block_table),
                     ("cache_seqlens", cache_seqlens), ("tile_scheduler_metadata",
                                                        tile_scheduler_metadata),
-                    ("num_splits", num_splits)):
-        if not t.is_cuda or t.device != q.device:
+                    ("num_splits", num_splits), ("q_pe", q_pe), ("k_pe", k_pe)):
+        if t is not None and (not t.is_cuda or t.device != q.device):
             raise ValueError(f"{name} must be on {q.device}")
     if q.stride(3) != 1 or kv_cache.stride(3) != 1:
-        raise ValueError("the 576 columns of q and kv_cache must be contiguous")
+        raise ValueError("the columns of q and kv_cache must be contiguous")
     if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.stride(1) != 1:
         raise ValueError("block_table must be int32 [b, max_blocks] with unit column stride")
     if cache_seqlens.dtype != torch.int32 or not cache_seqlens.is_contiguous():
@@ -271,8 +293,14 @@ def prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
     p.num_sm_parts = parts
     p.workspace = workspace.data_ptr()
     p.workspace_bytes = workspace.numel() * workspace.element_size()
+    if q_pe is not None:
+        p.q_pe, p.q_pe_batch_stride, p.q_pe_head_stride = (q_pe.data_ptr(), q_pe.stride(0),
+                                                           q_pe.stride(2))
+    if k_pe is not None:
+        p.k_pe, p.k_pe_page_stride, p.k_pe_row_stride = (k_pe.data_ptr(), k_pe.stride(0),
+                                                         k_pe.stride(1))
     keep = (q, kv_cache, block_table, cache_seqlens, tile_scheduler_metadata, num_splits,
-            workspace)
+            workspace, q_pe, k_pe)
     return DecodeCall(p, keep, out, lse)
 
 
@@ -282,13 +310,15 @@ def mla_decode_fwd_timed(*args, split_events, **kw):
 
 
 def mla_decode_fwd_static(q, kv_cache, block_table, cache_seqlens, softmax_scale,
-                          tile_scheduler_metadata, num_splits, out=None, lse=None):
+                          tile_scheduler_metadata, num_splits, out=None, lse=None, q_pe=None,
+                          k_pe=None):
     """mla_decode_fwd with the library's built-in per-device scratch
     (STATIC_WORKSPACE_BYTES) in place of a workspace tensor: the C call allocates
     nothing.  Calls on one device must not overlap on the GPU.  Returns (out, lse)."""
     no_ws = torch.empty((0,), dtype=torch.uint8, device=q.device)
     call = prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
-                          tile_scheduler_metadata, num_splits, out, lse, no_ws)
+                          tile_scheduler_metadata, num_splits, out, lse, no_ws, q_pe=q_pe,
+                          k_pe=k_pe)
     lib = _load()
     with torch.cuda.device(call.device):
         rc = lib.mla_decode_fwd_static(ctypes.byref(call.params), _stream(call.device))

@@ -172,16 +172,26 @@ int mla_decode_fwd_timed(const mla_fwd_params *p, void *stream, void *split_begi
     return MLA_ERR_SHAPE;
   if (p->dtype != MLA_DTYPE_FP16 && p->dtype != MLA_DTYPE_BF16) return MLA_ERR_DTYPE;
   if (p->page_block_size <= 0 || p->page_block_size % MLA_BLOCK_N != 0) return MLA_ERR_PAGE;
+  const bool sep_q = p->q_pe != nullptr, sep_k = p->k_pe != nullptr;
+  const int kv_cols = sep_k ? MLA_HEAD_DIM_V : MLA_HEAD_DIM;
   if (p->num_pages < 1 || p->max_blocks_per_seq < 1 || p->num_sm_parts < 1 ||
-      p->q_head_stride < 1 || p->q_batch_stride < 1 || p->kv_row_stride < MLA_HEAD_DIM ||
+      p->q_head_stride < 1 || p->q_batch_stride < 1 || p->kv_row_stride < kv_cols ||
       p->kv_page_stride < (int64_t)p->page_block_size * p->kv_row_stride ||
       p->o_head_stride < 1 || p->o_batch_stride < 1 || p->lse_batch_stride < p->h ||
       p->block_table_batch_stride < p->max_blocks_per_seq || !isfinite(p->softmax_scale))
+    return MLA_ERR_SHAPE;
+  if (sep_q && (p->q_pe_head_stride < 1 || p->q_pe_batch_stride < 1)) return MLA_ERR_SHAPE;
+  if (sep_k && (p->k_pe_row_stride < MLA_HEAD_DIM - MLA_HEAD_DIM_V ||
+                p->k_pe_page_stride < (int64_t)p->page_block_size * p->k_pe_row_stride))
     return MLA_ERR_SHAPE;
   if (!aligned16(p->q) || !aligned16(p->kv_cache) || !aligned16(p->out) ||
       !aligned16(p->workspace) || (p->q_batch_stride % 8) || (p->q_head_stride % 8) ||
       (p->kv_page_stride % 8) || (p->kv_row_stride % 8) || (p->o_batch_stride % 8) ||
       (p->o_head_stride % 8))
+    return MLA_ERR_ALIGN;
+  if (sep_q && (!aligned16(p->q_pe) || (p->q_pe_batch_stride % 8) || (p->q_pe_head_stride % 8)))
+    return MLA_ERR_ALIGN;
+  if (sep_k && (!aligned16(p->k_pe) || (p->k_pe_page_stride % 8) || (p->k_pe_row_stride % 8)))
     return MLA_ERR_ALIGN;
   if (p->workspace_bytes < workspace_bytes_for(p->b, p->h, p->num_sm_parts))
     return MLA_ERR_WORKSPACE;
@@ -200,6 +210,14 @@ int mla_decode_fwd_timed(const mla_fwd_params *p, void *stream, void *split_begi
   a.kv = p->kv_cache;
   a.kv_page_stride = p->kv_page_stride;
   a.kv_row_stride = p->kv_row_stride;
+  // fused layout: the RoPE columns are 512 elements (1 KB) into each row
+  const int64_t rope_off = MLA_HEAD_DIM_V * 2;
+  a.q_pe = sep_q ? p->q_pe : static_cast<const char *>(p->q) + rope_off;
+  a.q_pe_batch_stride = sep_q ? p->q_pe_batch_stride : p->q_batch_stride;
+  a.q_pe_head_stride = sep_q ? p->q_pe_head_stride : p->q_head_stride;
+  a.k_pe = sep_k ? p->k_pe : static_cast<const char *>(p->kv_cache) + rope_off;
+  a.k_pe_page_stride = sep_k ? p->k_pe_page_stride : p->kv_page_stride;
+  a.k_pe_row_stride = sep_k ? p->k_pe_row_stride : p->kv_row_stride;
   a.num_pages = p->num_pages;
   a.page_size = p->page_block_size;
   a.block_table = p->block_table;

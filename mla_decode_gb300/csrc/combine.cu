@@ -30,20 +30,15 @@ combine_kernel(FwdArgs a) {
   const int head = blockIdx.y * kWarps + warp;
   if (head >= a.h) return;
 
-  float mx = -INFINITY;
-  for (int k = lane; k < n; k += 32) mx = fmaxf(mx, a.lseaccum[(int64_t)(s0 + k) * a.h + head]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  const float mref = (mx == -INFINITY) ? 0.f : mx;
-  float sum = 0.f;
-  for (int k = lane; k < n; k += 32) sum += fast_exp2(a.lseaccum[(int64_t)(s0 + k) * a.h + head] - mref);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  const float lse = sum > 0.f ? fast_log2(sum) + mref : -INFINITY;
-
+  const int64_t base = (int64_t)s0 * a.h + head;
   float4 acc[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto load_row = [&](int64_t sp, float4 (&v)[4]) {
+    const float4 *src = reinterpret_cast<const float4 *>(a.oaccum + sp * MLA_HEAD_DIM_V);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) v[c] = src[lane + 32 * c];
+  };
   auto add = [&](float w, const float4 (&v)[4]) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -53,29 +48,46 @@ combine_kernel(FwdArgs a) {
       acc[c].w = fmaf(w, v[c].w, acc[c].w);
     }
   };
-  // two splits per step, all of their loads issued before any use
-  int k = 0;
-  for (; k + 1 < n; k += 2) {
-    const int64_t sp0 = (int64_t)(s0 + k) * a.h + head, sp1 = sp0 + a.h;
-    const float4 *src0 = reinterpret_cast<const float4 *>(a.oaccum + sp0 * MLA_HEAD_DIM_V);
-    const float4 *src1 = reinterpret_cast<const float4 *>(a.oaccum + sp1 * MLA_HEAD_DIM_V);
-    float4 v0[4], v1[4];
+  // the first two partial rows (n >= 2 here) do not depend on the LSE reduction:
+  // their loads are in flight while it runs
+  float4 v0[4], v1[4];
+  load_row(base, v0);
+  load_row(base + a.h, v1);
+
+  // lane k keeps split k's LSE (k < 32) for the sum and the weights
+  float mine = -INFINITY, mx = -INFINITY;
+  for (int k = lane; k < n; k += 32) {
+    const float l = a.lseaccum[base + (int64_t)k * a.h];
+    if (k == lane) mine = l;
+    mx = fmaxf(mx, l);
+  }
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      v0[c] = src0[lane + 32 * c];
-      v1[c] = src1[lane + 32 * c];
-    }
-    const float l0 = a.lseaccum[sp0], l1 = a.lseaccum[sp1];
-    add(lse == -INFINITY ? 0.f : fast_exp2(l0 - lse), v0);
-    add(lse == -INFINITY ? 0.f : fast_exp2(l1 - lse), v1);
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float mref = (mx == -INFINITY) ? 0.f : mx;
+  float sum = 0.f;
+  for (int k = lane; k < n; k += 32)
+    sum += fast_exp2((k == lane ? mine : a.lseaccum[base + (int64_t)k * a.h]) - mref);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float lse = sum > 0.f ? fast_log2(sum) + mref : -INFINITY;
+  auto weight = [&](int k) {
+    const float l = k < 32 ? __shfl_sync(0xffffffffu, mine, k) : a.lseaccum[base + (int64_t)k * a.h];
+    return lse == -INFINITY ? 0.f : fast_exp2(l - lse);
+  };
+
+  add(weight(0), v0);
+  add(weight(1), v1);
+  // the rest two at a time, both rows' loads issued before either is used
+  int k = 2;
+  for (; k + 1 < n; k += 2) {
+    load_row(base + (int64_t)k * a.h, v0);
+    load_row(base + (int64_t)(k + 1) * a.h, v1);
+    add(weight(k), v0);
+    add(weight(k + 1), v1);
   }
   if (k < n) {
-    const int64_t sp = (int64_t)(s0 + k) * a.h + head;
-    const float4 *src = reinterpret_cast<const float4 *>(a.oaccum + sp * MLA_HEAD_DIM_V);
-    float4 v[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) v[c] = src[lane + 32 * c];
-    add(lse == -INFINITY ? 0.f : fast_exp2(a.lseaccum[sp] - lse), v);
+    load_row(base + (int64_t)k * a.h, v0);
+    add(weight(k), v0);
   }
   // four consecutive 16-bit outputs per lane and column group: one 8-byte store
   T *o = reinterpret_cast<T *>(a.out) + seq * a.o_batch_stride + (int64_t)head * a.o_head_stride;

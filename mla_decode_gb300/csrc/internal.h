@@ -16,6 +16,12 @@ struct FwdArgs {
   int64_t q_batch_stride, q_head_stride;
   const void *kv;
   int64_t kv_page_stride, kv_row_stride;
+  // RoPE columns: separate tensors, or columns 512..575 of q / kv (resolved on
+  // the host, so the kernels see one layout)
+  const void *q_pe;
+  int64_t q_pe_batch_stride, q_pe_head_stride;
+  const void *k_pe;
+  int64_t k_pe_page_stride, k_pe_row_stride;
   int num_pages, page_size;
   const int32_t *block_table;
   int64_t bt_stride;
@@ -43,7 +49,6 @@ int *device_error_word();
 cudaError_t launch_metadata(const int32_t *seqlens, int b, int parts, int fixed,
                             int32_t *meta, int32_t *num_splits, cudaStream_t s);
 cudaError_t launch_split(const FwdArgs &a, cudaStream_t s);
-cudaError_t launch_split_simt(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_split_tc(const FwdArgs &a, cudaStream_t s);
 cudaError_t split_tc_num_sm(int device, int *num_sm);
 cudaError_t launch_combine(const FwdArgs &a, cudaStream_t s);

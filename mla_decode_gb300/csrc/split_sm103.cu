@@ -364,8 +364,11 @@ __device__ __forceinline__ void issue_job(const FwdArgs &a, SbWalk &w, SbJob &j)
 // 512 latent columns as eight [128 heads x 64] boxes through the K ring (the MMA
 // warp moves them into TMEM), the 64 RoPE columns straight into the Q8 tile once
 // the previous segment's MMAs are done with it.  Heads past h read as zeros.
+// The latent and RoPE columns come through separate tensor maps (map / qmap and
+// pemap / qpemap), so Q / Q_pe and KV / K_pe may be separate tensors.
 template <typename T>
 __device__ void score_producer(const FwdArgs &a, const CUtensorMap *map, const CUtensorMap *qmap,
+                               const CUtensorMap *pemap, const CUtensorMap *qpemap,
                                uint8_t *smem, const Ctx &c, int part, int head0) {
   Bars *b = c.bars;
   uint32_t kc = 0, segn = 0;
@@ -388,7 +391,7 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *map, const C
       if (segn > 0 && !wait_bar<false>(c, &b->q_free, (segn - 1) & 1, W_Q_FREE)) return false;
       if (leader) {
         mbar_arrive_expect_tx(&b->q8_full, kAtom);
-        tma_load_3d(smem + kOffQ8, qmap, &b->q8_full, 512, head0, j.seq);
+        tma_load_3d(smem + kOffQ8, qpemap, &b->q8_full, 0, head0, j.seq);
       }
       ++segn;
     }
@@ -398,13 +401,15 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *map, const C
       if (use > 0 && !wait_bar<false>(c, &b->k_empty[slot], (use - 1) & 1, W_K_EMPTY)) return false;
       if (leader) {
         const int atoms = ch < 4 ? 2 : 1;
+        const CUtensorMap *m = ch < 4 ? map : pemap;
+        const int x0 = ch < 4 ? 128 * ch : 0;
         mbar_arrive_expect_tx(&b->k_full[slot], atoms * j.np * kChunk);
         uint8_t *dst = smem + kOffK + slot * kKSlot;
         for (int at = 0; at < atoms; ++at)
 #pragma unroll
           for (int p = 0; p < kSB; ++p)
             if (p < j.np)
-              tma_load_3d(dst + at * kAtom + p * kChunk, map, &b->k_full[slot], 128 * ch + 64 * at,
+              tma_load_3d(dst + at * kAtom + p * kChunk, m, &b->k_full[slot], x0 + 64 * at,
                           j.pg.row0[p], j.pg.page[p]);
       }
     }
@@ -963,7 +968,8 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
-                const FwdArgs a) {
+                const __grid_constant__ CUtensorMap kpe_map,
+                const __grid_constant__ CUtensorMap qpe_map, const FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -1008,6 +1014,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&kv_map);
     tma_prefetch_desc(&q_map);
+    tma_prefetch_desc(&kpe_map);
+    tma_prefetch_desc(&qpe_map);
   }
   if (warp == 1) {
     tmem_alloc(&b->tmem_base, 512);
@@ -1027,7 +1035,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
     // a whole warp (a diverged spin loop would starve the other lanes' path, and
     // warp-uniform issue loops let one elected lane issue at full rate).
     if (warp == 0) {
-      score_producer<T>(a, &kv_map, &q_map, smem, c, part, head0);
+      score_producer<T>(a, &kv_map, &q_map, &kpe_map, &qpe_map, smem, c, part, head0);
     } else if (warp == 1) {
       score_mma<T>(a, smem, c, part, tmem);
     } else if (warp < 10) {
@@ -1083,29 +1091,41 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// One 3-D tiled map over a [outer][mid][cols] 16-bit tensor (strides in elements),
+// 128-byte swizzle, zero fill past the extents.
 template <typename T>
-cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
+cudaError_t make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t mid, uint64_t outer,
+                     int64_t mid_stride, int64_t outer_stride, uint32_t box_mid) {
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  CUtensorMap map;
-  cuuint64_t dims[3] = {(cuuint64_t)MLA_HEAD_DIM, (cuuint64_t)a.page_size, (cuuint64_t)a.num_pages};
-  cuuint64_t strides[2] = {(cuuint64_t)a.kv_row_stride * 2, (cuuint64_t)a.kv_page_stride * 2};
-  cuuint32_t box[3] = {64, 64, 1};
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)mid, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)mid_stride * 2, (cuuint64_t)outer_stride * 2};
+  cuuint32_t box[3] = {64, box_mid, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(&map, Pack<T>::kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                   3, const_cast<void *>(a.kv), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  CUresult r = enc(m, Pack<T>::kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   3, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  // Q as [b][h][576]: boxes of 64 columns x 128 heads (rows past h read as zeros)
-  CUtensorMap qmap;
-  cuuint64_t qdims[3] = {(cuuint64_t)MLA_HEAD_DIM, (cuuint64_t)a.h, (cuuint64_t)a.b};
-  cuuint64_t qstrides[2] = {(cuuint64_t)a.q_head_stride * 2, (cuuint64_t)a.q_batch_stride * 2};
-  cuuint32_t qbox[3] = {64, 128, 1};
-  r = enc(&qmap, Pack<T>::kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-          const_cast<void *>(a.q), qdims, qstrides, qbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <typename T>
+cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
+  constexpr uint64_t kLatent = MLA_HEAD_DIM_V, kRope = MLA_HEAD_DIM - MLA_HEAD_DIM_V;
+  // KV latent columns (also the value) and K_pe as [pages][page rows][cols], boxes
+  // of 64 rows x 64 columns; Q and Q_pe as [b][h][cols], boxes of 128 heads x 64
+  // columns (rows past h read as zeros)
+  CUtensorMap map, qmap, pemap, qpemap;
+  cudaError_t e = make_map<T>(&map, a.kv, kLatent, a.page_size, a.num_pages, a.kv_row_stride,
+                              a.kv_page_stride, 64);
+  if (e == cudaSuccess)
+    e = make_map<T>(&pemap, a.k_pe, kRope, a.page_size, a.num_pages, a.k_pe_row_stride,
+                    a.k_pe_page_stride, 64);
+  if (e == cudaSuccess)
+    e = make_map<T>(&qmap, a.q, kLatent, a.h, a.b, a.q_head_stride, a.q_batch_stride, 128);
+  if (e == cudaSuccess)
+    e = make_map<T>(&qpemap, a.q_pe, kRope, a.h, a.b, a.q_pe_head_stride, a.q_pe_batch_stride, 128);
+  if (e != cudaSuccess) return e;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
@@ -1125,7 +1145,7 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, split_tc_kernel<T>, map, qmap, a);
+  return cudaLaunchKernelEx(&cfg, split_tc_kernel<T>, map, qmap, pemap, qpemap, a);
 }
 
 }  // namespace

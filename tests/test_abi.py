@@ -45,7 +45,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_params_struct_matches(lib):
     import mla_decode_gb300 as m
     assert lib.mla_fwd_params_size() == ctypes.sizeof(m.FwdParams)
-    assert lib.mla_abi_version() == 1
+    assert lib.mla_abi_version() == m.ABI_VERSION == 2
 
 
 def test_status_strings(lib):
@@ -106,6 +106,30 @@ def good_params():
 def test_validation_rejects(lib, field, value, code):
     p = good_params()
     setattr(p, field, value)
+    assert lib.mla_decode_fwd(ctypes.byref(p), None) == code
+
+
+SEP_K = {"k_pe": (1 << 20) + 4096, "k_pe_page_stride": 64 * 64, "k_pe_row_stride": 64,
+         "kv_row_stride": 512, "kv_page_stride": 64 * 512}
+SEP_Q = {"q_pe": (1 << 20) + 8192, "q_pe_batch_stride": 16 * 64, "q_pe_head_stride": 64}
+
+
+@pytest.mark.parametrize("fields,code", [
+    ({**SEP_K, "k_pe_row_stride": 32}, -2),                 # row narrower than 64 columns
+    ({**SEP_K, "k_pe_page_stride": 64 * 64 - 8}, -2),       # page shorter than its rows
+    ({**SEP_K, "kv_row_stride": 504, "kv_page_stride": 64 * 504}, -2),
+    ({**SEP_K, "k_pe": (1 << 20) + 4104}, -4),              # 8-byte aligned only
+    ({**SEP_K, "k_pe_row_stride": 68, "k_pe_page_stride": 64 * 68}, -4),
+    ({**SEP_Q, "q_pe_head_stride": 0}, -2),
+    ({**SEP_Q, "q_pe_batch_stride": 16 * 64 + 4}, -4),
+    ({**SEP_Q, "q_pe": (1 << 20) + 8200}, -4),
+    ({"kv_row_stride": 512, "kv_page_stride": 64 * 512}, -2),  # 512-wide rows need k_pe
+])
+def test_split_layout_rejects(lib, fields, code):
+    """Q / Q_pe and KV / K_pe as separate tensors: the same host-side checks."""
+    p = good_params()
+    for k, v in fields.items():
+        setattr(p, k, v)
     assert lib.mla_decode_fwd(ctypes.byref(p), None) == code
 
 

@@ -135,3 +135,17 @@ def test_varlen_config_full_size():
 def test_mqa_config_full_size():
     w = workloads.get("mqa")
     P.check_workload(w, seqs=workloads.sample_seqs(w, 6))
+
+
+def test_tilelang_example_shape_full_size():
+    """example_mla_decode.py's default shape: b=132, h=128, 8192 tokens, one
+    contiguous 8192-token page per sequence, fp16."""
+    w = workloads.get("tl_example")
+    P.check_workload(w, seqs=workloads.sample_seqs(w, 6))
+
+
+@pytest.mark.parametrize("L", [workloads.BENCH_SEQLENS[0], workloads.BENCH_SEQLENS[-1]])
+def test_benchmark_sweep_ends_full_size(L):
+    """benchmark_mla.py's default b=128, h=128 at the shortest and longest cache."""
+    w = workloads.get(f"tl_bench_{L}")
+    P.check_workload(w, seqs=workloads.sample_seqs(w, 4))

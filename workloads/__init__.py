@@ -83,9 +83,13 @@ def _varlen_lengths(batch, lo, hi, seed):
     return tuple(int(x) for x in lens)
 
 
+# benchmark_mla.py's default cache lengths: 1024 to 32768
+BENCH_SEQLENS = (1024, 2048, 4096, 8192, 16384, 32768)
+
+
 def configs():
-    """The five decode workloads, by name (sizes as the pages' benchmarks use them)."""
-    return {
+    """The decode workloads, by name (sizes as the pages' benchmarks use them)."""
+    out = {
         "tiny": Workload("tiny", 2, 16, (256, 256), "fp16", page_size=256,
                          softmax_scale=576 ** -0.5, seed=0, shuffle=False,
                          notes="contiguous cache: page_size 256, block_table [[0],[1]]"),
@@ -98,7 +102,18 @@ def configs():
         "mqa": Workload("mqa", 256, 16, (32768,) * 256, "bf16", page_size=64,
                         softmax_scale=192 ** -0.5, seed=4, hot_row_frac=0.01,
                         hot_row_mult=8.0),
+        # the TileLang guide's own command lines (section 如何运行、验证与基准测试):
+        # example_mla_decode.py defaults (contiguous cache, fp16 as in its comparison);
+        # its example_mla_decode_paged.py line is the "split" workload above
+        "tl_example": Workload("tl_example", 132, 128, (8192,) * 132, "fp16", page_size=8192,
+                               softmax_scale=576 ** -0.5, seed=5, shuffle=False,
+                               notes="contiguous cache: one 8192-token page per sequence"),
     }
+    for k, L in enumerate(BENCH_SEQLENS):  # benchmark_mla.py default sweep, b=128 h=128
+        name = f"tl_bench_{L}"
+        out[name] = Workload(name, 128, 128, (L,) * 128, "fp16", page_size=64,
+                             softmax_scale=576 ** -0.5, seed=10 + k)
+    return out
 
 
 def get(name, **overrides):
