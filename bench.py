@@ -199,6 +199,22 @@ class ClockSampler:
                 "source": "nvml" if self.nvml else "nvidia-smi"}
 
 
+def max_over_ranks(x, world, device):
+    """The largest of every rank's `x` (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flops_per_rank, ms):
+    """Whole-job throughput: every rank's flops over the slowest rank's step time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -367,10 +383,8 @@ def run_ours(args):
     code, detail = mla.mla_get_device_error()
     if code != 0:
         raise RuntimeError(f"device error {code} detail {detail}")
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
+    split_ms = max_over_ranks(split_ms, world, dev)
 
     # ---- end to end through the public API with pinned host buffers
     host = {k: v.cpu().pin_memory() for k, v in base.items() if v is not None}
@@ -405,10 +419,7 @@ def run_ours(args):
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / E
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
     flops = w.flops()
     nbytes = w.bytes()
@@ -417,7 +428,7 @@ def run_ours(args):
     traffic = ncu_traffic(w.name)
     line = {
         "metric": METRIC,
-        "value": world * flops / (ms * 1e-3) / 1e12,
+        "value": job_tflops(world, flops, ms),
         "unit": UNIT,
         "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms,
@@ -435,7 +446,7 @@ def run_ours(args):
                      "frac": achieved / hbm_peak, "traffic": traffic, "kernel": "split",
                      "kernel_ms": split_ms, "peak_source": f"{peak_src} hbm_gbs",
                      "tensor_frac_of_bf16_peak": flops / (split_ms * 1e-3) / 1e12 / bf16_peak},
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": job_tflops(world, flops, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
                 "ms_per_step": e2e_ms},
         "gpu_launches": 3 * K,
