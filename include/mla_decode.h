@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 2
+#define MLA_ABI_VERSION 3
 
 /* Shape contract [TL §先看核心难点]: 576 = 512 latent + 64 RoPE; v = 512. */
 #define MLA_HEAD_DIM 576
@@ -68,8 +68,21 @@ enum { MLA_DTYPE_FP16 = 0, MLA_DTYPE_BF16 = 1 };
 
 /*
  * Arguments of one decode call.  Follows the field set of FlashMLA's
- * Flash_fwd_mla_params [FM §内存访问优化]; fields for seqlen_q > 1 (is_causal,
- * ngroups, h_h_k_ratio) are not part of this ABI.
+ * Flash_fwd_mla_params [FM §内存访问优化], including seqlen_q and is_causal;
+ * with one KV head, ngroups (query heads per KV head) is h and h_h_k_ratio
+ * is h, so neither is a separate field.
+ *
+ * Several query tokens per sequence (seqlen_q = s > 1, e.g. speculative or
+ * multi-token decoding): the s * h query rows of a sequence are folded into
+ * one run of rows, token-major (row r = qi * h + head), and all read the same
+ * cache.  q's rows are then addressed as q + i*q_batch_stride + r*q_head_stride
+ * (a [b][s][h][576] tensor whose token stride is h * q_head_stride), out's the
+ * same way with o_head_stride, and lse is [b][s * h].  The cache already holds
+ * the s new tokens: query token qi stands at position L_i - s + qi, and with
+ * is_causal it sees the cached tokens t < L_i - (s - 1 - qi) (a row that sees
+ * none gives out = 0, lse = -inf); without it every row sees all L_i tokens.
+ * Pass h_rows = s * h wherever an entry point below asks for h
+ * (mla_metadata_shape, mla_get_metadata, mla_workspace_size).
  *
  * Tensors (device, caller-owned):
  *   q            [b][1][h][576]        strides q_batch_stride, q_head_stride;
@@ -99,9 +112,9 @@ enum { MLA_DTYPE_FP16 = 0, MLA_DTYPE_BF16 = 1 };
  *                must lie in [0, num_pages).
  *   cache_seqlens int32 [b], 0 <= L_i <= max_blocks_per_seq*page_block_size.
  *   out          [b][1][h][512]        strides o_batch_stride, o_head_stride.
- *   lse          fp32 [b][h]           stride lse_batch_stride (heads
+ *   lse          fp32 [b][s * h]       stride lse_batch_stride (rows
  *                contiguous); natural-log log-sum-exp of the scaled scores,
- *                -inf for an empty sequence (whose out row is all zeros).
+ *                -inf for a row that sees no token (whose out row is zeros).
  *   tile_scheduler_metadata, num_splits: as written by mla_get_metadata for
  *                the same cache_seqlens, b, h and num_sm.
  *   workspace    at least mla_workspace_size(b, h, num_sm_parts) bytes, 16-byte
@@ -115,8 +128,8 @@ enum { MLA_DTYPE_FP16 = 0, MLA_DTYPE_BF16 = 1 };
  */
 typedef struct mla_fwd_params {
   int32_t b;              /* sequences (>= 1) */
-  int32_t seqlen_q;       /* query tokens per sequence: must be 1 */
-  int32_t h;              /* query heads (1..1024) */
+  int32_t seqlen_q;       /* query tokens per sequence, s >= 1 */
+  int32_t h;              /* query heads per token; s * h <= 1024 */
   int32_t h_k;            /* KV heads: must be 1 */
   int32_t d;              /* must be MLA_HEAD_DIM */
   int32_t d_v;            /* must be MLA_HEAD_DIM_V */
@@ -154,6 +167,9 @@ typedef struct mla_fwd_params {
   int64_t q_pe_batch_stride, q_pe_head_stride;
   const void *k_pe;
   int64_t k_pe_page_stride, k_pe_row_stride;
+
+  /* seqlen_q > 1 only: nonzero = causal mask among the query tokens (above) */
+  int32_t is_causal;
 } mla_fwd_params;
 
 /* ABI version (MLA_ABI_VERSION) and sizeof(mla_fwd_params), for bindings. */
@@ -171,7 +187,8 @@ const char *mla_status_string(int status);
 int mla_device_num_sm(int device, int *num_sm);
 
 /*
- * Scheduler shape for b sequences and h heads on num_sm SMs (host only, no
+ * Scheduler shape for b sequences and h query rows per sequence (heads, or
+ * seqlen_q * heads) on num_sm SMs (host only, no
  * GPU needed): *num_sm_parts = max(1, (num_sm / 2) / ceil(h / 128)) parts (one
  * 2-CTA cluster per part and 128-head tile), *meta_stride = MLA_META_STRIDE.
  */
@@ -198,7 +215,7 @@ int mla_get_metadata(const int32_t *cache_seqlens, int b, int h, int num_sm,
                      void *stream);
 
 /* Workspace bytes for mla_decode_fwd: fp32 partial outputs and LSEs for up to
- * b + num_sm_parts splits of h heads. */
+ * b + num_sm_parts splits of h query rows (heads, or seqlen_q * heads). */
 int mla_workspace_size(int b, int h, int num_sm_parts, size_t *bytes);
 
 /*

@@ -26,7 +26,7 @@ __all__ = [
 HEAD_DIM = 576
 HEAD_DIM_V = 512
 ROPE_DIM = HEAD_DIM - HEAD_DIM_V
-ABI_VERSION = 2
+ABI_VERSION = 3
 BLOCK_N = 64
 META_STRIDE = 8
 SCHED_FIXED_COST = 5
@@ -60,6 +60,7 @@ class FwdParams(ctypes.Structure):
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
         ("q_pe", _vp), ("q_pe_batch_stride", _i64), ("q_pe_head_stride", _i64),
         ("k_pe", _vp), ("k_pe_page_stride", _i64), ("k_pe_row_stride", _i64),
+        ("is_causal", _i32),
     ]
 
 
@@ -136,12 +137,14 @@ def mla_metadata_shape(b, h, num_sm):
 
 
 def mla_get_metadata(cache_seqlens, h, num_sm=None, tile_scheduler_metadata=None,
-                     num_splits=None):
-    """Scheduler metadata for `cache_seqlens` (int32 [b], on the GPU).
+                     num_splits=None, seqlen_q=1):
+    """Scheduler metadata for `cache_seqlens` (int32 [b], on the GPU), h query heads
+    and seqlen_q query tokens per sequence (the C call gets seqlen_q * h rows).
 
     Returns (tile_scheduler_metadata int32 [num_sm_parts, 8], num_splits int32 [b + 1]),
     writing into the given tensors when they are passed.
     """
+    h = int(h) * int(seqlen_q)
     if cache_seqlens.dtype != torch.int32 or not cache_seqlens.is_cuda or cache_seqlens.dim() != 1:
         raise ValueError("cache_seqlens must be a CUDA int32 vector")
     cache_seqlens = cache_seqlens.contiguous()
@@ -175,7 +178,7 @@ def mla_workspace_size(b, h, num_sm_parts):
 
 def mla_decode_fwd(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                    tile_scheduler_metadata, num_splits, out=None, lse=None, workspace=None,
-                   split_events=None, q_pe=None, k_pe=None):
+                   split_events=None, q_pe=None, k_pe=None, is_causal=False):
     """Paged split-KV MLA decode (see prepare_decode for the argument contract).
 
     split_events: optional (begin, end) torch.cuda.Event pair recorded around the
@@ -183,7 +186,7 @@ def mla_decode_fwd(q, kv_cache, block_table, cache_seqlens, softmax_scale,
     """
     call = prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                           tile_scheduler_metadata, num_splits, out, lse, workspace,
-                          q_pe=q_pe, k_pe=k_pe)
+                          q_pe=q_pe, k_pe=k_pe, is_causal=is_causal)
     call(split_events=split_events)
     return call.out, call.lse
 
@@ -215,7 +218,7 @@ class DecodeCall:
 
 def prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                    tile_scheduler_metadata, num_splits, out=None, lse=None, workspace=None,
-                   q_pe=None, k_pe=None):
+                   q_pe=None, k_pe=None, is_causal=False):
     """Paged split-KV MLA decode.
 
     q [b, 1, h, 576], kv_cache [num_pages, page_size, 1, 576] (fp16 or bf16, same
@@ -223,21 +226,29 @@ def prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
     from mla_get_metadata.  Returns (out [b, 1, h, 512] in q's dtype, lse fp32 [b, h]
     natural-log).  Launches on the current stream of q's device.
 
-    Split layout: with q_pe [b, 1, h, 64] given, q is [b, 1, h, 512] (latent
+    Split layout: with q_pe [b, s, h, 64] given, q is [b, s, h, 512] (latent
     columns only); with k_pe [num_pages, page_size, 1, 64] given, kv_cache is
     [num_pages, page_size, 1, 512].  The score is then q . kv + q_pe . k_pe.
+
+    Several query tokens: q [b, s, h, 576] with s > 1 (token stride h times the
+    head stride), out [b, s, h, 512], lse [b, s, h]; the cache already holds the s
+    new tokens, and with is_causal token qi sees the cached tokens
+    t < L - (s - 1 - qi).  The metadata must be made with seqlen_q = s.
     """
     q_cols = HEAD_DIM_V if q_pe is not None else HEAD_DIM
     kv_cols = HEAD_DIM_V if k_pe is not None else HEAD_DIM
-    if q.dim() != 4 or q.shape[1] != 1 or q.shape[3] != q_cols:
-        raise ValueError(f"q must be [b, 1, h, {q_cols}]")
+    if q.dim() != 4 or q.shape[3] != q_cols:
+        raise ValueError(f"q must be [b, s, h, {q_cols}]")
+    s_q = q.shape[1]
+    if s_q < 1:
+        raise ValueError("q needs at least one query token")
     if kv_cache.dim() != 4 or kv_cache.shape[2] != 1 or kv_cache.shape[3] != kv_cols:
         raise ValueError(f"kv_cache must be [num_pages, page_size, 1, {kv_cols}]")
     if q.dtype not in _DTYPE_CODE or kv_cache.dtype != q.dtype:
         raise ValueError("q and kv_cache must share dtype fp16 or bf16")
-    if q_pe is not None and (q_pe.dim() != 4 or tuple(q_pe.shape) != (q.shape[0], 1, q.shape[2],
-                                                                       ROPE_DIM)):
-        raise ValueError("q_pe must be [b, 1, h, 64]")
+    if q_pe is not None and (q_pe.dim() != 4 or tuple(q_pe.shape) != (q.shape[0], s_q,
+                                                                       q.shape[2], ROPE_DIM)):
+        raise ValueError("q_pe must be [b, s, h, 64]")
     if k_pe is not None and (k_pe.dim() != 4 or tuple(k_pe.shape) != (kv_cache.shape[0],
                                                                        kv_cache.shape[1], 1,
                                                                        ROPE_DIM)):
@@ -258,24 +269,34 @@ def prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
     if cache_seqlens.dtype != torch.int32 or not cache_seqlens.is_contiguous():
         raise ValueError("cache_seqlens must be a contiguous int32 vector")
     b, _, h, _ = q.shape
+    rows = s_q * h
+    for name, t in (("q", q), ("q_pe", q_pe)):
+        if t is not None and s_q > 1 and t.stride(1) != h * t.stride(2):
+            raise ValueError(f"{name}: the s * h query rows must be evenly strided "
+                             "(token stride = h * head stride)")
     if block_table.shape[0] != b or cache_seqlens.numel() != b or num_splits.numel() != b + 1:
         raise ValueError("batch size mismatch among q, block_table, cache_seqlens, num_splits")
     parts = tile_scheduler_metadata.shape[0]
     dev = q.device
+    lse_shape = (b, h) if s_q == 1 else (b, s_q, h)
     if out is None:
-        out = torch.empty((b, 1, h, HEAD_DIM_V), dtype=q.dtype, device=dev)
+        out = torch.empty((b, s_q, h, HEAD_DIM_V), dtype=q.dtype, device=dev)
     if lse is None:
-        lse = torch.empty((b, h), dtype=torch.float32, device=dev)
-    if out.shape != (b, 1, h, HEAD_DIM_V) or out.dtype != q.dtype or out.stride(3) != 1:
-        raise ValueError("out must be [b, 1, h, 512] in q's dtype with contiguous columns")
-    if lse.shape != (b, h) or lse.dtype != torch.float32 or lse.stride(1) != 1:
-        raise ValueError("lse must be fp32 [b, h] with contiguous heads")
-    need = mla_workspace_size(b, h, parts)
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    if (out.shape != (b, s_q, h, HEAD_DIM_V) or out.dtype != q.dtype or out.stride(3) != 1
+            or (s_q > 1 and out.stride(1) != h * out.stride(2))):
+        raise ValueError("out must be [b, s, h, 512] in q's dtype, contiguous columns, "
+                         "evenly strided rows")
+    if (tuple(lse.shape) != lse_shape or lse.dtype != torch.float32 or lse.stride(-1) != 1
+            or (s_q > 1 and lse.stride(1) != h)):
+        raise ValueError(f"lse must be fp32 {list(lse_shape)} with contiguous rows")
+    need = mla_workspace_size(b, rows, parts)
     if workspace is None:
         workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
 
     p = FwdParams()
-    p.b, p.seqlen_q, p.h, p.h_k, p.d, p.d_v = b, 1, h, 1, HEAD_DIM, HEAD_DIM_V
+    p.b, p.seqlen_q, p.h, p.h_k, p.d, p.d_v = b, s_q, h, 1, HEAD_DIM, HEAD_DIM_V
+    p.is_causal = 1 if is_causal else 0
     p.dtype = _DTYPE_CODE[q.dtype]
     p.softmax_scale = float(softmax_scale)
     p.q, p.q_batch_stride, p.q_head_stride = q.data_ptr(), q.stride(0), q.stride(2)
@@ -311,14 +332,14 @@ def mla_decode_fwd_timed(*args, split_events, **kw):
 
 def mla_decode_fwd_static(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                           tile_scheduler_metadata, num_splits, out=None, lse=None, q_pe=None,
-                          k_pe=None):
+                          k_pe=None, is_causal=False):
     """mla_decode_fwd with the library's built-in per-device scratch
     (STATIC_WORKSPACE_BYTES) in place of a workspace tensor: the C call allocates
     nothing.  Calls on one device must not overlap on the GPU.  Returns (out, lse)."""
     no_ws = torch.empty((0,), dtype=torch.uint8, device=q.device)
     call = prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                           tile_scheduler_metadata, num_splits, out, lse, no_ws, q_pe=q_pe,
-                          k_pe=k_pe)
+                          k_pe=k_pe, is_causal=is_causal)
     lib = _load()
     with torch.cuda.device(call.device):
         rc = lib.mla_decode_fwd_static(ctypes.byref(call.params), _stream(call.device))

@@ -150,8 +150,11 @@ int mla_decode_fwd(const mla_fwd_params *p, void *stream) {
 
 int mla_decode_fwd_static(const mla_fwd_params *p, void *stream) {
   if (!p) return MLA_ERR_NULL;
-  if (p->b < 1 || p->h < 1 || p->h > 1024 || p->num_sm_parts < 1) return MLA_ERR_SHAPE;
-  if (workspace_bytes_for(p->b, p->h, p->num_sm_parts) > (size_t)MLA_STATIC_WORKSPACE_BYTES)
+  if (p->b < 1 || p->h < 1 || p->h > 1024 || p->seqlen_q < 1 || p->seqlen_q > 1024 ||
+      p->seqlen_q * p->h > 1024 || p->num_sm_parts < 1)
+    return MLA_ERR_SHAPE;
+  if (workspace_bytes_for(p->b, p->seqlen_q * p->h, p->num_sm_parts) >
+      (size_t)MLA_STATIC_WORKSPACE_BYTES)
     return MLA_ERR_WORKSPACE;
   void *ws = static_workspace();
   if (!ws) return MLA_ERR_CUDA;
@@ -167,9 +170,11 @@ int mla_decode_fwd_timed(const mla_fwd_params *p, void *stream, void *split_begi
   if (!p->q || !p->kv_cache || !p->block_table || !p->cache_seqlens || !p->out || !p->lse ||
       !p->tile_scheduler_metadata || !p->num_splits || !p->workspace)
     return MLA_ERR_NULL;
-  if (p->b < 1 || p->seqlen_q != 1 || p->h < 1 || p->h > 1024 || p->h_k != 1 ||
-      p->d != MLA_HEAD_DIM || p->d_v != MLA_HEAD_DIM_V)
+  if (p->b < 1 || p->seqlen_q < 1 || p->seqlen_q > 1024 || p->h < 1 || p->h > 1024 ||
+      p->h_k != 1 || p->d != MLA_HEAD_DIM || p->d_v != MLA_HEAD_DIM_V)
     return MLA_ERR_SHAPE;
+  const int rows = p->seqlen_q * p->h;  // query rows per sequence, token-major
+  if (rows > 1024) return MLA_ERR_SHAPE;
   if (p->dtype != MLA_DTYPE_FP16 && p->dtype != MLA_DTYPE_BF16) return MLA_ERR_DTYPE;
   if (p->page_block_size <= 0 || p->page_block_size % MLA_BLOCK_N != 0) return MLA_ERR_PAGE;
   const bool sep_q = p->q_pe != nullptr, sep_k = p->k_pe != nullptr;
@@ -177,7 +182,7 @@ int mla_decode_fwd_timed(const mla_fwd_params *p, void *stream, void *split_begi
   if (p->num_pages < 1 || p->max_blocks_per_seq < 1 || p->num_sm_parts < 1 ||
       p->q_head_stride < 1 || p->q_batch_stride < 1 || p->kv_row_stride < kv_cols ||
       p->kv_page_stride < (int64_t)p->page_block_size * p->kv_row_stride ||
-      p->o_head_stride < 1 || p->o_batch_stride < 1 || p->lse_batch_stride < p->h ||
+      p->o_head_stride < 1 || p->o_batch_stride < 1 || p->lse_batch_stride < rows ||
       p->block_table_batch_stride < p->max_blocks_per_seq || !isfinite(p->softmax_scale))
     return MLA_ERR_SHAPE;
   if (sep_q && (p->q_pe_head_stride < 1 || p->q_pe_batch_stride < 1)) return MLA_ERR_SHAPE;
@@ -193,7 +198,7 @@ int mla_decode_fwd_timed(const mla_fwd_params *p, void *stream, void *split_begi
     return MLA_ERR_ALIGN;
   if (sep_k && (!aligned16(p->k_pe) || (p->k_pe_page_stride % 8) || (p->k_pe_row_stride % 8)))
     return MLA_ERR_ALIGN;
-  if (p->workspace_bytes < workspace_bytes_for(p->b, p->h, p->num_sm_parts))
+  if (p->workspace_bytes < workspace_bytes_for(p->b, rows, p->num_sm_parts))
     return MLA_ERR_WORKSPACE;
 
   int *err = device_error_word();
@@ -201,7 +206,10 @@ int mla_decode_fwd_timed(const mla_fwd_params *p, void *stream, void *split_begi
 
   FwdArgs a;
   a.b = p->b;
-  a.h = p->h;
+  a.h = rows;
+  a.q_len = p->seqlen_q;
+  a.heads = p->h;
+  a.causal = p->seqlen_q > 1 && p->is_causal != 0;
   a.dtype = p->dtype;
   a.scale_log2 = p->softmax_scale * 1.4426950408889634f;
   a.q = p->q;
@@ -235,7 +243,7 @@ int mla_decode_fwd_timed(const mla_fwd_params *p, void *stream, void *split_begi
   a.max_splits = max_splits_for(p->b, p->num_sm_parts);
   a.oaccum = static_cast<float *>(p->workspace);
   a.lseaccum = reinterpret_cast<float *>(static_cast<char *>(p->workspace) +
-                                         (size_t)a.max_splits * p->h * MLA_HEAD_DIM_V * sizeof(float));
+                                         (size_t)a.max_splits * rows * MLA_HEAD_DIM_V * sizeof(float));
   a.err = err;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);

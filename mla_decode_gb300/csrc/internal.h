@@ -10,7 +10,10 @@ namespace mla {
 
 // Everything a split / combine kernel needs, resolved and validated on the host.
 struct FwdArgs {
-  int b, h, dtype;
+  int b, h, dtype;   // h: query rows per sequence (seqlen_q * heads, token-major)
+  int q_len;         // query tokens per sequence
+  int heads;         // query heads per token (rows q_len * heads)
+  int causal;        // token qi sees the cached tokens t < L - (q_len - 1 - qi)
   float scale_log2;  // softmax_scale * log2(e): scores are kept in base-2 units
   const void *q;
   int64_t q_batch_stride, q_head_stride;

@@ -562,6 +562,9 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
   const int r = 32 * quad + lane;      // head row within the tile
   const int head = head0 + r;
   const bool head_ok = head < a.h;
+  // several query tokens per sequence (rows token-major): a causal row of token qi
+  // sees q_len - 1 - qi fewer cached tokens than the sequence holds
+  const int hidden = (a.causal && head_ok) ? a.q_len - 1 - head / a.heads : 0;
   const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
   const uint32_t tS = tmem + 256 + lane_off + 64 * half;
   float *red_max = reinterpret_cast<float *>(smem + kOffRed);  // [2][128]
@@ -598,9 +601,10 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       prof_wait(19, tp);
       tp = prof_now();
 
-      // base-2 units; tokens past the sequence end (a suffix of my page) and a page
-      // past the segment end (all of it) become -inf after the scale
-      const int lim = half < np ? min(64, s.L - ((sb0 + half) << 6)) : 0;
+      // base-2 units; tokens this row does not see (a suffix of my page, all of it
+      // when it starts past the row's end) and a page past the segment end (all of
+      // it) become -inf after the scale
+      const int lim = half < np ? min(64, s.L - hidden - ((sb0 + half) << 6)) : 0;
       float sc = scale;
       if (lim < 64) {
 #pragma unroll
@@ -642,7 +646,9 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       for (int e = 0; e < 8; ++e) ps[e] = 0.f;
       const bool write = ok && half < np;
       const uint32_t row = smem_u32(smem + kOffPStage + tb * kPTile) + r * 128;
-      const float nm = -m_ref;
+      // a row that has seen no token yet (causal rows only) has m_ref = -inf: its
+      // weights are exp2(-inf) = 0, not exp2(-inf + inf)
+      const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         float p[8];

@@ -55,6 +55,13 @@ def load(path=_LIB):
             ctypes.c_void_p, ctypes.c_double, ctypes.c_int, ctypes.c_int,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_mla_decode_rows_q.restype = ctypes.c_int
+        lib.oracle_mla_decode_rows_q.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_double, ctypes.c_int, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_widen.restype = ctypes.c_double
         lib.oracle_widen.argtypes = [ctypes.c_uint16, ctypes.c_int]
         if path == _LIB:
@@ -67,14 +74,16 @@ def _ptr(a):
 
 
 def decode_rows(q, kv, block_table, cache_seqlens, softmax_scale, dtype, rows,
-                threads=1, lib=None, with_abs=False):
-    """Evaluate the definition for the (seq, head) pairs in `rows`.
+                threads=1, lib=None, with_abs=False, seqlen_q=1, is_causal=False):
+    """Evaluate the definition for the (seq, row) pairs in `rows`.
 
-    q            : uint16 [b, h, 576]   (stored bits; seqlen_q = 1 folded)
+    q            : uint16 [b, seqlen_q * h, 576]   (stored bits; row = qi * h + head)
     kv           : uint16 [num_pages, page_size, 576]
     block_table  : int32  [b, max_blocks]
     cache_seqlens: int32  [b]
-    rows         : int array [n, 2] of (seq, head)
+    rows         : int array [n, 2] of (seq, row)
+    seqlen_q, is_causal: query tokens per sequence; with is_causal, token qi sees
+                   the cached tokens t < L - (seqlen_q - 1 - qi)
     Returns (out float64 [n, 512], lse float64 [n]), and with `with_abs` also
     absw float64 [n, 512] = sum_t p_t |v_t| per column: the scale of the terms
     each output sums, which bounds the error of any rounding of them.
@@ -85,8 +94,10 @@ def decode_rows(q, kv, block_table, cache_seqlens, softmax_scale, dtype, rows,
     bt = np.ascontiguousarray(block_table, dtype=np.int32)
     sl = np.ascontiguousarray(cache_seqlens, dtype=np.int32)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
-    b, h, d = q.shape
+    b, nrows, d = q.shape
     assert d == D and kv.shape[2] == D and bt.shape[0] == b and sl.shape[0] == b
+    assert seqlen_q >= 1 and nrows % seqlen_q == 0
+    h = nrows // seqlen_q
     num_pages, page_size = kv.shape[0], kv.shape[1]
     n = rows.shape[0]
     out = np.zeros((n, DV), dtype=np.float64)
@@ -104,10 +115,15 @@ def decode_rows(q, kv, block_table, cache_seqlens, softmax_scale, dtype, rows,
         ls = lse[lo:hi]
         ab = _ptr(absw[lo:hi]) if with_abs else None
         scratch = np.empty(max_len, dtype=np.float64)
-        return lib.oracle_mla_decode_rows(
-            b, h, _ptr(q), _ptr(kv), num_pages, page_size, _ptr(bt), bt.shape[1],
-            _ptr(sl), float(softmax_scale), code, hi - lo, _ptr(rb), _ptr(rh),
-            _ptr(o), _ptr(ls), _ptr(scratch), ab)
+        if seqlen_q == 1 and not is_causal:
+            return lib.oracle_mla_decode_rows(
+                b, h, _ptr(q), _ptr(kv), num_pages, page_size, _ptr(bt), bt.shape[1],
+                _ptr(sl), float(softmax_scale), code, hi - lo, _ptr(rb), _ptr(rh),
+                _ptr(o), _ptr(ls), _ptr(scratch), ab)
+        return lib.oracle_mla_decode_rows_q(
+            b, int(seqlen_q), h, int(bool(is_causal)), _ptr(q), _ptr(kv), num_pages, page_size,
+            _ptr(bt), bt.shape[1], _ptr(sl), float(softmax_scale), code, hi - lo, _ptr(rb),
+            _ptr(rh), _ptr(o), _ptr(ls), _ptr(scratch), ab)
 
     if threads <= 1 or n < 2:
         rc = run(0, n)
@@ -122,12 +138,14 @@ def decode_rows(q, kv, block_table, cache_seqlens, softmax_scale, dtype, rows,
     return (out, lse, absw) if with_abs else (out, lse)
 
 
-def decode(q, kv, block_table, cache_seqlens, softmax_scale, dtype, threads=1):
-    """Every (seq, head) pair; returns out [b, h, 512] and lse [b, h] (float64)."""
+def decode(q, kv, block_table, cache_seqlens, softmax_scale, dtype, threads=1, seqlen_q=1,
+           is_causal=False):
+    """Every (seq, row) pair; returns out [b, rows, 512] and lse [b, rows] (float64),
+    rows = seqlen_q * h (token-major)."""
     b, h = q.shape[0], q.shape[1]
     rows = np.stack(np.meshgrid(np.arange(b), np.arange(h), indexing="ij"), -1).reshape(-1, 2)
     out, lse = decode_rows(q, kv, block_table, cache_seqlens, softmax_scale, dtype, rows,
-                           threads=threads)
+                           threads=threads, seqlen_q=seqlen_q, is_causal=is_causal)
     return out.reshape(b, h, DV), lse.reshape(b, h)
 
 

@@ -11,7 +11,8 @@
  *          FlashMLA 级性能的完整实战指南" (lmnt.cn/news/253096)
  *   [FM]  "DeepSeek开源周第一天：FlashMLA 深度分析" (pxiaoer.blog)
  *
- * What is computed (one query token per sequence, one shared latent KV head):
+ * What is computed (one shared latent KV head; seqlen_q query tokens per
+ * sequence, one by default):
  *   [TL §先看核心难点]  q and k rows are 576 wide: 512 latent + 64 RoPE;
  *                       v is 512 wide.
  *   [TL §Split Kernel]  the same cached tile feeds both the score GEMM and the
@@ -125,12 +126,18 @@ static int one_row(const uint16_t *q_row, const uint16_t *kv, int64_t num_pages,
 }
 
 /*
- * Selected rows of the MLA decode definition.
- *   q            : [b][h][576] stored values (seqlen_q = 1 folded away)
+ * Selected rows of the MLA decode definition, with seqlen_q query tokens per
+ * sequence [FM §内存访问优化: Flash_fwd_mla_params carries seqlen_q, ngroups and
+ * is_causal].  With one KV head the seqlen_q * h query rows of a sequence all
+ * read the same cache (ngroups = h); they are stored token-major:
+ *   q            : [b][seqlen_q * h][576] stored values, row r = qi * h + head
  *   kv           : [num_pages][page_size][576] stored values (one KV head)
  *   block_table  : [b][max_blocks]
- *   cache_seqlens: [b]
- *   row_b, row_h : n_rows (sequence, head) pairs to evaluate
+ *   cache_seqlens: [b]; the cache already holds the seqlen_q new tokens, so
+ *                  query token qi stands at position L - seqlen_q + qi
+ *   is_causal    : query token qi sees the cached tokens t < L - (seqlen_q-1-qi)
+ *                  (none if that is <= 0); otherwise every t < L
+ *   row_b, row_r : n_rows (sequence, query row) pairs to evaluate
  *   out          : [n_rows][512] doubles
  *   lse          : [n_rows] doubles
  *   absw         : [n_rows][512] doubles or NULL: the softmax-weighted mean of
@@ -138,6 +145,32 @@ static int one_row(const uint16_t *q_row, const uint16_t *kv, int64_t num_pages,
  *   scratch      : at least max(cache_seqlens) doubles
  * Returns 0 on success, -1 on an out-of-range page or row index.
  */
+int oracle_mla_decode_rows_q(int b, int seqlen_q, int h, int is_causal, const uint16_t *q,
+                             const uint16_t *kv, int64_t num_pages, int page_size,
+                             const int32_t *block_table, int max_blocks,
+                             const int32_t *cache_seqlens, double softmax_scale, int dtype,
+                             int n_rows, const int32_t *row_b, const int32_t *row_r,
+                             double *out, double *lse, double *scratch, double *absw) {
+  if (seqlen_q < 1) return -1;
+  const int rows_per_seq = seqlen_q * h;
+  for (int r = 0; r < n_rows; ++r) {
+    int bi = row_b[r], ri = row_r[r];
+    if (bi < 0 || bi >= b || ri < 0 || ri >= rows_per_seq) return -1;
+    int L = cache_seqlens[bi];
+    if (L > max_blocks * page_size) return -1;
+    int qi = ri / h; /* query token of this row */
+    int visible = is_causal ? L - (seqlen_q - 1 - qi) : L;
+    if (visible < 0) visible = 0;
+    int rc = one_row(q + ((int64_t)bi * rows_per_seq + ri) * MLA_D, kv, num_pages, page_size,
+                     block_table + (int64_t)bi * max_blocks, visible, softmax_scale, dtype,
+                     out + (int64_t)r * MLA_DV, absw ? absw + (int64_t)r * MLA_DV : 0, lse + r,
+                     scratch);
+    if (rc) return rc;
+  }
+  return 0;
+}
+
+/* One query token per sequence: q is [b][h][576] and the rows are (sequence, head). */
 int oracle_mla_decode_rows(int b, int h, const uint16_t *q, const uint16_t *kv,
                            int64_t num_pages, int page_size,
                            const int32_t *block_table, int max_blocks,
@@ -145,16 +178,7 @@ int oracle_mla_decode_rows(int b, int h, const uint16_t *q, const uint16_t *kv,
                            int dtype, int n_rows, const int32_t *row_b,
                            const int32_t *row_h, double *out, double *lse,
                            double *scratch, double *absw) {
-  for (int r = 0; r < n_rows; ++r) {
-    int bi = row_b[r], hi = row_h[r];
-    if (bi < 0 || bi >= b || hi < 0 || hi >= h) return -1;
-    int L = cache_seqlens[bi];
-    if (L > max_blocks * page_size) return -1;
-    int rc = one_row(q + ((int64_t)bi * h + hi) * MLA_D, kv, num_pages, page_size,
-                     block_table + (int64_t)bi * max_blocks, L, softmax_scale, dtype,
-                     out + (int64_t)r * MLA_DV, absw ? absw + (int64_t)r * MLA_DV : 0, lse + r,
-                     scratch);
-    if (rc) return rc;
-  }
-  return 0;
+  return oracle_mla_decode_rows_q(b, 1, h, 0, q, kv, num_pages, page_size, block_table,
+                                  max_blocks, cache_seqlens, softmax_scale, dtype, n_rows,
+                                  row_b, row_h, out, lse, scratch, absw);
 }

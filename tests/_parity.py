@@ -28,19 +28,23 @@ LSE_MAX_ABS = 1e-3
 ORACLE_THREADS = max(1, min(32, os.cpu_count() or 1))
 
 
-def run_gpu(inputs, heads, scale, num_sm=None):
+def run_gpu(inputs, heads, scale, num_sm=None, is_causal=False):
     import mla_decode_gb300 as mla
-    meta, num_splits = mla.mla_get_metadata(inputs["cache_seqlens"], heads, num_sm)
+    s_q = inputs["q"].shape[1]
+    meta, num_splits = mla.mla_get_metadata(inputs["cache_seqlens"], heads, num_sm,
+                                            seqlen_q=s_q)
     out, lse = mla.mla_decode_fwd(inputs["q"], inputs["kv_cache"], inputs["block_table"],
-                                  inputs["cache_seqlens"], scale, meta, num_splits)
+                                  inputs["cache_seqlens"], scale, meta, num_splits,
+                                  is_causal=is_causal)
     code, detail = mla.mla_get_device_error()
     assert code == 0, f"device error {code} ({mla.mla_status_string(code)}), detail {detail}"
     return out, lse, meta, num_splits
 
 
 def oracle_rows(w, inputs, seqs=None):
-    """Oracle out [n_seq, h, 512], lse [n_seq, h] and the weighted-absolute scale
-    [n_seq, h, 512] for sequences `seqs` (all if None)."""
+    """Oracle out [n_seq, rows, 512], lse [n_seq, rows] and the weighted-absolute scale
+    [n_seq, rows, 512] for sequences `seqs` (all if None); rows = seqlen_q * h,
+    token-major."""
     q = inputs["q"]
     kv = inputs["kv_cache"]
     bt = inputs["block_table"].cpu().numpy()
@@ -54,13 +58,15 @@ def oracle_rows(w, inputs, seqs=None):
         return workloads.to_bits(sel[:, :, 0, :])
 
     kv_c, table_c, sl_c = oracle.compact_pages(pages, bt, sl, seqs, w.page_size)
-    q_c = workloads.to_bits(q[torch.as_tensor(seqs, device=q.device), 0])
-    rows = np.stack(np.meshgrid(np.arange(len(seqs)), np.arange(w.heads), indexing="ij"),
+    q_c = workloads.to_bits(q[torch.as_tensor(seqs, device=q.device)]).reshape(len(seqs), w.rows,
+                                                                              -1)
+    rows = np.stack(np.meshgrid(np.arange(len(seqs)), np.arange(w.rows), indexing="ij"),
                     -1).reshape(-1, 2)
     out, lse, absw = oracle.decode_rows(q_c, kv_c, table_c, sl_c, w.softmax_scale, w.dtype, rows,
-                                        threads=ORACLE_THREADS, with_abs=True)
-    return (out.reshape(len(seqs), w.heads, -1), lse.reshape(len(seqs), w.heads),
-            absw.reshape(len(seqs), w.heads, -1))
+                                        threads=ORACLE_THREADS, with_abs=True,
+                                        seqlen_q=w.seqlen_q, is_causal=w.causal)
+    return (out.reshape(len(seqs), w.rows, -1), lse.reshape(len(seqs), w.rows),
+            absw.reshape(len(seqs), w.rows, -1))
 
 
 def compare(out_gpu, lse_gpu, out_ref, lse_ref, abs_ref, what=""):
@@ -86,15 +92,17 @@ def compare(out_gpu, lse_gpu, out_ref, lse_ref, abs_ref, what=""):
 def check_workload(w, seqs=None, num_sm=None, poison_tail=False, inputs=None):
     if inputs is None:
         inputs = workloads.make_inputs(w, device="cuda", poison_tail=poison_tail)
-    out, lse, meta, ns = run_gpu(inputs, w.heads, w.softmax_scale, num_sm)
+    out, lse, meta, ns = run_gpu(inputs, w.heads, w.softmax_scale, num_sm, is_causal=w.causal)
     ref_o, ref_l, ref_a = oracle_rows(w, inputs, seqs)
     idx = torch.as_tensor(list(range(w.batch)) if seqs is None else list(seqs), device=out.device)
-    stats = compare(out[idx, 0], lse[idx], ref_o, ref_l, ref_a, what=w.name)
+    stats = compare(out[idx].reshape(len(idx), w.rows, -1), lse[idx].reshape(len(idx), w.rows),
+                    ref_o, ref_l, ref_a, what=w.name)
     log = os.environ.get("MLA_PARITY_LOG")
     if log:
         import json
         with open(log, "a") as f:
             f.write(json.dumps({"workload": w.name, "batch": w.batch, "heads": w.heads,
-                                "num_sm": num_sm, "rows": int(idx.numel()) * w.heads,
+                                "seqlen_q": w.seqlen_q, "causal": w.causal,
+                                "num_sm": num_sm, "rows": int(idx.numel()) * w.rows,
                                 **stats}) + "\n")
     return stats, out, lse, meta, ns, inputs

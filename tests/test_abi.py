@@ -45,7 +45,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_params_struct_matches(lib):
     import mla_decode_gb300 as m
     assert lib.mla_fwd_params_size() == ctypes.sizeof(m.FwdParams)
-    assert lib.mla_abi_version() == m.ABI_VERSION == 2
+    assert lib.mla_abi_version() == m.ABI_VERSION == 3
 
 
 def test_status_strings(lib):
@@ -97,7 +97,7 @@ def good_params():
 
 @pytest.mark.parametrize("field,value,code", [
     ("q", 0, -1), ("kv_cache", 0, -1), ("workspace", 0, -1), ("lse", 0, -1),
-    ("seqlen_q", 2, -2), ("h_k", 2, -2), ("d", 512, -2), ("d_v", 576, -2), ("h", 0, -2),
+    ("seqlen_q", 0, -2), ("seqlen_q", 2, -2), ("h_k", 2, -2), ("d", 512, -2), ("d_v", 576, -2), ("h", 0, -2),
     ("b", 0, -2), ("dtype", 7, -3), ("page_block_size", 96, -5), ("page_block_size", 0, -5),
     ("q", (1 << 20) + 8, -4), ("q_head_stride", 580, -4), ("kv_page_stride", 64 * 576 + 4, -4),
     ("workspace_bytes", 100, -6), ("num_sm_parts", 0, -2), ("lse_batch_stride", 8, -2),
@@ -127,6 +127,20 @@ SEP_Q = {"q_pe": (1 << 20) + 8192, "q_pe_batch_stride": 16 * 64, "q_pe_head_stri
 ])
 def test_split_layout_rejects(lib, fields, code):
     """Q / Q_pe and KV / K_pe as separate tensors: the same host-side checks."""
+    p = good_params()
+    for k, v in fields.items():
+        setattr(p, k, v)
+    assert lib.mla_decode_fwd(ctypes.byref(p), None) == code
+
+
+@pytest.mark.parametrize("fields,code", [
+    ({"seqlen_q": 2}, -2),                                   # lse rows: 16 < 2 * 16
+    ({"seqlen_q": 65, "lse_batch_stride": 65 * 16}, -2),     # 1040 query rows > 1024
+    ({"seqlen_q": 2, "lse_batch_stride": 32}, -6),           # workspace sized for 16 rows
+    ({"seqlen_q": -1}, -2),
+])
+def test_query_tokens_rejects(lib, fields, code):
+    """seqlen_q > 1: rows = seqlen_q * h size lse and the workspace; at most 1024 rows."""
     p = good_params()
     for k, v in fields.items():
         setattr(p, k, v)

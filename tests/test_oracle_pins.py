@@ -11,7 +11,9 @@ different statement of the same operation:
     MLA guide's combine kernel) equalling the unsplit result;
   * the 16-bit widening checked exhaustively against numpy / torch;
   * the weighted-absolute output (sum_t p_t |v_t|, the scale of the terms each
-    output sums) against brute force, its closed forms and |out| <= absw.
+    output sums) against brute force, its closed forms and |out| <= absw;
+  * several query tokens per sequence, causal and not, against brute force over
+    each token's visible prefix of the logical cache.
 Finally, mutants of the oracle source (a dropped RoPE term, v from the wrong
 columns, a wrong page index, a missing max in lse, ...) must each fail a pin.
 """
@@ -337,9 +339,45 @@ def pin_abs_weights(lib):
     return np.allclose(absw0[1, 0], np.abs(lv).mean(axis=0)[:DV], rtol=1e-12, atol=1e-14)
 
 
+def pin_query_tokens(lib):
+    """seqlen_q query tokens per sequence, rows stored token-major (row = qi * h + head):
+    against brute force over the logical cache.  Non-causal rows see all L tokens;
+    causal token qi sees t < L - (seqlen_q - 1 - qi), nothing when that is <= 0
+    (out = 0, lse = -inf)."""
+    rng = np.random.default_rng(24)
+    s_q, h, scale = 3, 2, 0.06
+    lens = (1, 2, 5, 40)
+    logical = [bits(rng.standard_normal((L, D)), "bf16") for L in lens]
+    q = bits(rng.standard_normal((len(lens), s_q * h, D)), "bf16")
+    kv, table = paged(logical, 16, rng)
+    rows = np.stack(np.meshgrid(np.arange(len(lens)), np.arange(s_q * h), indexing="ij"),
+                    -1).reshape(-1, 2)
+    for causal in (False, True):
+        out, lse = oracle.decode_rows(q, kv, table, np.asarray(lens, np.int32), scale, "bf16",
+                                      rows, lib=lib, seqlen_q=s_q, is_causal=causal)
+        out = out.reshape(len(lens), s_q * h, DV)
+        lse = lse.reshape(len(lens), s_q * h)
+        for i, L in enumerate(lens):
+            lv = vals(logical[i], "bf16")
+            for qi in range(s_q):
+                n = max(0, L - (s_q - 1 - qi)) if causal else L
+                for j in range(h):
+                    r = qi * h + j
+                    if n == 0:
+                        if not (np.all(out[i, r] == 0) and lse[i, r] == -np.inf):
+                            return False
+                        continue
+                    ref_o, ref_l = brute(vals(q[i, r], "bf16"), lv[:n], scale)
+                    if not (np.allclose(out[i, r], ref_o, rtol=1e-11, atol=1e-12)
+                            and abs(lse[i, r] - ref_l) < 1e-11 * max(1.0, abs(ref_l))):
+                        return False
+    return True
+
+
 PINS = [pin_brute_force, pin_len_one, pin_identical_scores, pin_zero_query, pin_two_tokens,
         pin_dominant_token, pin_empty_sequence, pin_page_permutation, pin_token_permutation,
-        pin_head_independence, pin_softmax_shift, pin_split_combine, pin_batch_rows, pin_abs_weights]
+        pin_head_independence, pin_softmax_shift, pin_split_combine, pin_batch_rows, pin_abs_weights,
+        pin_query_tokens]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -392,10 +430,15 @@ MUTANTS = {
     "no_normalise": ("double p = exp(scores[t] - m) / z;", "double p = exp(scores[t] - m);"),
     "bf16_shift": ("(uint32_t)x << 16;", "(uint32_t)x << 15;"),
     "fp16_bias": ("e - 25);", "e - 24);"),
-    "q_row_transposed": ("q + ((int64_t)bi * h + hi) * MLA_D", "q + ((int64_t)hi * b + bi) * MLA_D"),
+    "q_row_transposed": ("q + ((int64_t)bi * rows_per_seq + ri) * MLA_D",
+                         "q + ((int64_t)ri * b + bi) * MLA_D"),
     "first_token_skipped": ("for (int t = 0; t < seqlen; ++t) z +=",
                             "for (int t = 1; t < seqlen; ++t) z +="),
     "abs_sign_kept": ("abs_row[d] += p * fabs(widen(v[d], dtype));", "abs_row[d] += p * widen(v[d], dtype);"),
+    "causal_off_by_one": ("L - (seqlen_q - 1 - qi) : L", "L - (seqlen_q - qi) : L"),
+    "causal_ignored": ("is_causal ? L - (seqlen_q - 1 - qi) : L", "L"),
+    "query_token_reversed": ("int qi = ri / h;", "int qi = seqlen_q - 1 - ri / h;"),
+    "query_rows_head_major": ("int qi = ri / h;", "int qi = ri % seqlen_q;"),
     "abs_unweighted": ("abs_row[d] += p * fabs(widen(v[d], dtype));", "abs_row[d] += fabs(widen(v[d], dtype));"),
 }
 

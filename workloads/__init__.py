@@ -43,6 +43,17 @@ class Workload:
     hot_row_frac: float = 0.0
     hot_row_mult: float = 1.0
     notes: str = ""
+    seqlen_q: int = 1       # query tokens per sequence (rows token-major)
+    causal: bool = False    # token qi sees the cached tokens t < L - (seqlen_q - 1 - qi)
+
+    @property
+    def rows(self):
+        """Query rows per sequence: seqlen_q * heads."""
+        return self.seqlen_q * self.heads
+
+    def visible(self, L, qi):
+        """Cached tokens query token qi of a length-L sequence attends to."""
+        return max(0, int(L) - (self.seqlen_q - 1 - qi)) if self.causal else int(L)
 
     @property
     def torch_dtype(self):
@@ -65,13 +76,15 @@ class Workload:
         return int(sum(int(L) for L in self.seqlens))
 
     def flops(self):
-        """Algorithmic flops: b*h*sum(L)*2*(576+512) summed over sequences."""
-        return float(self.heads) * self.total_tokens * 2 * (D + DV)
+        """Algorithmic flops: 2*(576+512) per (query row, visible token), i.e.
+        b*h*sum(L)*2*(576+512) for one query token per sequence."""
+        pairs = sum(self.visible(L, qi) for L in self.seqlens for qi in range(self.seqlen_q))
+        return float(self.heads) * pairs * 2 * (D + DV)
 
     def bytes(self):
         """Algorithmic bytes: KV rows (token granular) + Q + O."""
         esz = 2
-        return float(self.total_tokens * D * esz + self.batch * self.heads * (D + DV) * esz)
+        return float(self.total_tokens * D * esz + self.batch * self.rows * (D + DV) * esz)
 
 
 def _varlen_lengths(batch, lo, hi, seed):
@@ -102,6 +115,10 @@ def configs():
         "mqa": Workload("mqa", 256, 16, (32768,) * 256, "bf16", page_size=64,
                         softmax_scale=192 ** -0.5, seed=4, hot_row_frac=0.01,
                         hot_row_mult=8.0),
+        # several query tokens per sequence (speculative / multi-token decoding): the
+        # paged shape with two causal query tokens, 256 query rows per sequence
+        "mtp": Workload("mtp", 64, 128, (4096,) * 64, "bf16", page_size=64,
+                        softmax_scale=192 ** -0.5, seed=7, seqlen_q=2, causal=True),
         # the TileLang guide's own command lines (section 如何运行、验证与基准测试):
         # example_mla_decode.py defaults (contiguous cache, fp16 as in its comparison);
         # its example_mla_decode_paged.py line is the "split" workload above
@@ -145,7 +162,7 @@ def make_inputs(w: Workload, device="cpu", poison_tail=False):
     """Build q, kv_cache, block_table, cache_seqlens for workload `w` on `device`.
 
     Layouts (contiguous):
-      q            [b, 1, h, 576]
+      q            [b, seqlen_q, h, 576]
       kv_cache     [num_pages, page_size, 1, 576]
       block_table  int32 [b, max_blocks]
       cache_seqlens int32 [b]
@@ -158,7 +175,7 @@ def make_inputs(w: Workload, device="cpu", poison_tail=False):
     dt = w.torch_dtype
     b, h, P = w.batch, w.heads, w.page_size
 
-    q = torch.empty((b, 1, h, D), dtype=dt, device=device)
+    q = torch.empty((b, w.seqlen_q, h, D), dtype=dt, device=device)
     _randn_into(q, gen)
 
     kv = torch.empty((w.num_pages, P, 1, D), dtype=dt, device=device)
