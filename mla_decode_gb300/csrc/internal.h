@@ -37,7 +37,7 @@ struct FwdArgs {
   const int32_t *meta;
   const int32_t *num_splits;
   int num_parts;
-  float *oaccum;    // [max_splits][h][512]
+  float *oaccum;    // [max_splits][128 column chunks][h][4] (rows interleaved per chunk)
   float *lseaccum;  // [max_splits][h], base-2 units
   int max_splits;
   int *err;         // device error word (two ints: code, detail)

@@ -64,6 +64,10 @@ constexpr int kNV = MLA_NV;              // V half-page tiles in flight (value C
 #endif
 constexpr int kNPR = MLA_NPR;            // P tiles in the value CTA's ring
 constexpr int kStages = 2;               // P staging buffers in the score CTA
+#ifndef MLA_V4D
+#define MLA_V4D 1
+#endif
+constexpr bool kV4d = MLA_V4D != 0;      // V tiles as one 4-D box (else four 3-D boxes)
 #ifndef MLA_TAU
 #define MLA_TAU 0.0f
 #endif
@@ -697,9 +701,13 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
 
 // ------------------------------------------------------------------------------ value CTA
 
+// V producer.  A V tile is one page's 256 value columns of one O half: four
+// swizzled [64 rows x 64 columns] atoms, 8 KB apart.  The 4-D map (columns split
+// into 64-wide blocks) lands all four in one TMA request; per request the SM's
+// TMA unit moves ~84 GB/s with 32 KB boxes, against 36-55 GB/s with 8 KB ones.
 template <typename T>
-__device__ void value_producer(const FwdArgs &a, const CUtensorMap *map, uint8_t *smem,
-                               const Ctx &c, int part) {
+__device__ void value_producer(const FwdArgs &a, const CUtensorMap *map, const CUtensorMap *map4,
+                               uint8_t *smem, const Ctx &c, int part) {
   Bars *b = c.bars;
   uint32_t vc = 0;
   const bool leader = elect_one();
@@ -719,10 +727,14 @@ __device__ void value_producer(const FwdArgs &a, const CUtensorMap *map, uint8_t
         if (leader) {
           mbar_arrive_expect_tx(&b->v_full[slot], kVSlot);
           uint8_t *dst = smem + kOffV + slot * kVSlot;
+          if (kV4d) {
+            tma_load_4d(dst, map4, &b->v_full[slot], 0, j.pg.row0[p], 4 * g, j.pg.page[p]);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            tma_load_3d(dst + i * kChunk, map, &b->v_full[slot], 64 * (4 * g + i), j.pg.row0[p],
-                        j.pg.page[p]);
+            for (int i = 0; i < 4; ++i)
+              tma_load_3d(dst + i * kChunk, map, &b->v_full[slot], 64 * (4 * g + i), j.pg.row0[p],
+                          j.pg.page[p]);
+          }
         }
       }
     }
@@ -845,6 +857,10 @@ __device__ void value_receiver(const FwdArgs &a, const Ctx &c, int part) {
 
 // Epilogue of one thread's head row and O half: O / l from TMEM to `out` (one
 // split) or to the fp32 split workspace.  Once per segment, so out of line.
+// The workspace holds the partial outputs as [split][128 column chunks][h rows]
+// [4 floats]: a warp's 32 consecutive rows write 512 contiguous bytes per chunk.
+// (Row-major partials made every warp store touch 32 rows 2 KB apart, and the
+// epilogue of one segment took ~10 us at ~26 GB/s.)
 template <typename T>
 __device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int nsplit, int head,
                                        bool head_ok, int g, uint32_t tO, float lrow) {
@@ -866,12 +882,13 @@ __device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int
                           Pack<T>::two(f[4] * inv, f[5] * inv), Pack<T>::two(f[6] * inv, f[7] * inv));
       }
     } else {
-      float4 *o = reinterpret_cast<float4 *>(a.oaccum + ((int64_t)split * a.h + head) * 512 + 256 * g + 64 * i);
+      float4 *o = reinterpret_cast<float4 *>(a.oaccum) +
+                  ((int64_t)split * 128 + 64 * g + 16 * i) * a.h + head;
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const uint32_t *x = &w[k >> 3][4 * (k & 7)];
-        o[k] = make_float4(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv,
-                           __uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv);
+        o[(int64_t)k * a.h] = make_float4(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv,
+                                          __uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv);
       }
     }
   }
@@ -885,8 +902,8 @@ __device__ __noinline__ void zero_out(const FwdArgs &a, int seq, int split, int 
                                          (int64_t)head * a.o_head_stride + 256 * g);
     for (int i = 0; i < 32; ++i) o[i] = make_uint4(0, 0, 0, 0);
   } else {
-    float4 *o = reinterpret_cast<float4 *>(a.oaccum + ((int64_t)split * a.h + head) * 512 + 256 * g);
-    for (int i = 0; i < 64; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 *o = reinterpret_cast<float4 *>(a.oaccum) + ((int64_t)split * 128 + 64 * g) * a.h + head;
+    for (int i = 0; i < 64; ++i) o[(int64_t)i * a.h] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
@@ -938,6 +955,7 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
       if (ok && (int)sb >= 2) ok = wait_done((int)sb - 2);
       if (ok && resc) ok = wait_done((int)sb - 1);
       if (ok && resc) {
+        const uint64_t tr = prof_now();
         tc_fence_after();
 #pragma unroll 1
         for (int i = 0; i < 4; ++i) {
@@ -955,13 +973,16 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
         }
         tmem_wait_st();
         tc_fence_before();
+        prof_wait(27, tr);
       }
       mbar_arrive(&b->o_ready[g][sb & 1]);
       if (flags & 2u) {  // epilogue
         if (ok) ok = wait_done((int)sb);
         if (bar_red_or(bar_id, 128, !ok || c.aborted())) return;
         tc_fence_after();
+        const uint64_t te = prof_now();
         write_out<T>(a, s.seq, s.split, s.nsplit, head, head_ok, g, tO, lrow);
+        prof_wait(26, te);
         tc_fence_before();
         mbar_arrive(&b->o_free);
       }
@@ -975,7 +996,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                 const __grid_constant__ CUtensorMap kpe_map,
-                const __grid_constant__ CUtensorMap qpe_map, const FwdArgs a) {
+                const __grid_constant__ CUtensorMap qpe_map,
+                const __grid_constant__ CUtensorMap kv4_map, const FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -1022,6 +1044,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
     tma_prefetch_desc(&q_map);
     tma_prefetch_desc(&kpe_map);
     tma_prefetch_desc(&qpe_map);
+    tma_prefetch_desc(&kv4_map);
   }
   if (warp == 1) {
     tmem_alloc(&b->tmem_base, 512);
@@ -1053,7 +1076,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
     // warp 0: V producer, 1: MMA, 2-5 / 6-9: correction and epilogue of O half 0 / 1,
     // 10: P-tile receiver
     if (warp == 0) {
-      value_producer<T>(a, &kv_map, smem, c, part);
+      value_producer<T>(a, &kv_map, &kv4_map, smem, c, part);
     } else if (warp == 1) {
       value_mma<T>(a, smem, c, part, tmem);
     } else if (warp < 10) {
@@ -1132,6 +1155,21 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
   if (e == cudaSuccess)
     e = make_map<T>(&qpemap, a.q_pe, kRope, a.h, a.b, a.q_pe_head_stride, a.q_pe_batch_stride, 128);
   if (e != cudaSuccess) return e;
+  // the latent columns again as [pages][8 column blocks][page rows][64 columns]
+  // (block stride 128 B): a {64, 64, 4, 1} box is one V tile, four atoms in a row
+  CUtensorMap map4;
+  {
+    auto enc = encode_fn();
+    cuuint64_t dims[4] = {64, (cuuint64_t)a.page_size, kLatent / 64, (cuuint64_t)a.num_pages};
+    cuuint64_t strides[3] = {(cuuint64_t)a.kv_row_stride * 2, 128, (cuuint64_t)a.kv_page_stride * 2};
+    cuuint32_t box[4] = {64, 64, 4, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = enc(&map4, Pack<T>::kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     4, const_cast<void *>(a.kv), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
@@ -1151,7 +1189,7 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, split_tc_kernel<T>, map, qmap, pemap, qpemap, a);
+  return cudaLaunchKernelEx(&cfg, split_tc_kernel<T>, map, qmap, pemap, qpemap, map4, a);
 }
 
 }  // namespace
