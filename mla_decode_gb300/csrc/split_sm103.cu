@@ -99,7 +99,9 @@ constexpr int kScoreEnd = kOffRed + 4 * 128 * 4;
 constexpr int kOffV = 0;                                      // value: V ring
 constexpr int kOffPRing = kOffV + kNV * kVSlot;               // value: P tiles
 constexpr int kOffHdr = kOffPRing + kNPR * kPTile;            // value: 2 headers
-constexpr int kValueEnd = kOffHdr + 2 * (int)sizeof(Header);
+constexpr int kOffEpi = (kOffHdr + 2 * (int)sizeof(Header) + 1023) & ~1023;  // value: 8 x 2 KB
+constexpr int kValueEnd = kOffEpi + 8 * 2048;                 // epilogue staging, one per warp
+static_assert(kValueEnd <= kScoreEnd, "the value CTA's staging fits in the score CTA's footprint");
 constexpr int kOffBars = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 127) & ~127;
 
 struct Bars {
@@ -322,6 +324,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                "r"(d)
                : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
 }
 
 // Walks this part's non-empty superblocks in order.
@@ -857,31 +866,47 @@ __device__ void value_receiver(const FwdArgs &a, const Ctx &c, int part) {
 
 // Epilogue of one thread's head row and O half: O / l from TMEM to `out` (one
 // split) or to the fp32 split workspace.  Once per segment, so out of line.
+// Rows of `out` are 1 KB apart, so the 16-bit results pass through the warp's
+// 2 KB staging tile (`epi`, [32 rows][64 B], 16-byte pieces at j ^ ((row >> 1) & 3):
+// no bank conflicts) and leave as 64-byte row pieces, eight rows per store.
 // The workspace holds the partial outputs as [split][128 column chunks][h rows]
 // [4 floats]: a warp's 32 consecutive rows write 512 contiguous bytes per chunk.
 // (Row-major partials made every warp store touch 32 rows 2 KB apart, and the
 // epilogue of one segment took ~10 us at ~26 GB/s.)
 template <typename T>
 __device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int nsplit, int head,
-                                       bool head_ok, int g, uint32_t tO, float lrow) {
+                                       bool head_ok, int g, uint32_t tO, float lrow, uint32_t epi) {
   const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+  const int lane = threadIdx.x & 31;
+  const int row0 = head - lane;  // the warp's first row
 #pragma unroll 1
   for (int i = 0; i < 4; ++i) {
     uint32_t w[2][32];
     tmem_ld32(tO + 64 * i, w[0]);
     tmem_ld32(tO + 64 * i + 32, w[1]);
     tmem_wait_ld();
-    if (!head_ok) continue;
-    if (nsplit == 1) {
-      uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(a.out) + (int64_t)seq * a.o_batch_stride +
-                                           (int64_t)head * a.o_head_stride + 256 * g + 64 * i);
+    if (nsplit == 1) {  // every lane takes part (the tile is shared by the warp)
+      T *o = reinterpret_cast<T *>(a.out) + (int64_t)seq * a.o_batch_stride + 256 * g + 64 * i;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float *f = reinterpret_cast<const float *>(&w[k >> 2][8 * (k & 3)]);
-        o[k] = make_uint4(Pack<T>::two(f[0] * inv, f[1] * inv), Pack<T>::two(f[2] * inv, f[3] * inv),
-                          Pack<T>::two(f[4] * inv, f[5] * inv), Pack<T>::two(f[6] * inv, f[7] * inv));
+      for (int t = 0; t < 2; ++t) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float *f = reinterpret_cast<const float *>(&w[t][8 * j]);
+          st_shared_v4(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), Pack<T>::two(f[0] * inv, f[1] * inv),
+                       Pack<T>::two(f[2] * inv, f[3] * inv), Pack<T>::two(f[4] * inv, f[5] * inv),
+                       Pack<T>::two(f[6] * inv, f[7] * inv));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int row = 8 * r + (lane >> 2), j = lane & 3;
+          const uint4 v = ld_shared_v4(epi + row * 64 + ((j ^ ((row >> 1) & 3)) << 4));
+          if (row0 + row < a.h)
+            *reinterpret_cast<uint4 *>(o + (int64_t)(row0 + row) * a.o_head_stride + 32 * t + 8 * j) = v;
+        }
+        __syncwarp();
       }
-    } else {
+    } else if (head_ok) {
       float4 *o = reinterpret_cast<float4 *>(a.oaccum) +
                   ((int64_t)split * 128 + 64 * g + 16 * i) * a.h + head;
 #pragma unroll
@@ -981,7 +1006,8 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
         if (bar_red_or(bar_id, 128, !ok || c.aborted())) return;
         tc_fence_after();
         const uint64_t te = prof_now();
-        write_out<T>(a, s.seq, s.split, s.nsplit, head, head_ok, g, tO, lrow);
+        write_out<T>(a, s.seq, s.split, s.nsplit, head, head_ok, g, tO, lrow,
+                     smem_u32(smem + kOffEpi + (warp - 2) * 2048));
         prof_wait(26, te);
         tc_fence_before();
         mbar_arrive(&b->o_free);
