@@ -85,21 +85,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Wait for phase `parity` of `bar`, giving up after ~limit_ns.  Returns false on
-// timeout (the caller records the error and unwinds).
-template <bool kCluster = false>
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          uint64_t limit_ns = 2000000000ull) {
-  const uint32_t a = smem_u32(bar);
-  if (kCluster ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    for (int i = 0; i < 256; ++i)
-      if (kCluster ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
-  }
-}
-
 // ----------------------------------------------------------------------------- fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -111,12 +96,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_id_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %clusterid.x;" : "=r"(r));
   return r;
 }
 
@@ -136,12 +115,6 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local_addr, uint32_t ct
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(cta_rank));
   return r;
-}
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
 }
 
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to the
@@ -169,23 +142,10 @@ __device__ __forceinline__ bool bar_red_or(int id, int count, bool pred) {
   return out != 0;
 }
 
-__device__ __forceinline__ void bar_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // ----------------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_t *bar, int c0,
-                                            int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-      : "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_t *bar, int c0,
@@ -204,28 +164,6 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
       "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d_hint(void *dst, const void *tmap, uint64_t *bar,
-                                                 int c0, int c1, int c2, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
-// Bring a TMA box into L2 without writing shared memory.
-__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
 }
 
 // One lane of the (fully active) warp; the rest get false.
@@ -293,15 +231,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 __device__ __forceinline__ void mma_commit_addr(uint32_t bar_addr) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar_addr)
-      : "memory");
-}
-
-// Same, arriving on the mbarrier at this offset in every CTA of `cta_mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 
