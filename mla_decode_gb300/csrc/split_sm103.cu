@@ -1,12 +1,16 @@
 // Split kernel for sm_103a: tcgen05 tensor cores, TMEM accumulators, TMA loads,
 // a 2-CTA cluster per scheduler part.
 //
-// What it computes (per sequence segment and 128-head tile) is the TileLang
+// What it computes (per sequence segment and 128-row tile of query rows: heads,
+// or seqlen_q x heads token-major) is the TileLang
 // guide's split kernel ("用 TileLang 编写高性能 DeepSeek MLA 内核…", sections
 // 先看核心难点, Split Kernel, 变体内核 (paged), 6. Split-KV) with FlashMLA's
 // softmax form ("DeepSeek开源周第一天：FlashMLA 深度分析", section Softmax 计算优化:
 // exp2 with log2(e) folded into the scale, the -inf guard):
-//   S = Q . K^T over the 576 columns, masked past cache_seqlens; online softmax
+//   S = Q . K^T over the 576 columns (latent and RoPE columns through their own
+//   tensor maps, so Q / Q_pe and KV / K_pe may be separate tensors), masked past
+//   each row's visible length (cache_seqlens, less the later query tokens under
+//   the causal mask); online softmax
 //   in base 2; P rounded to the input dtype; O += P . V with V the first 512
 //   columns of the same cached rows; at the segment end O / l and the base-2 LSE.
 //
@@ -18,20 +22,22 @@
 //     superblock of up to two 64-token pages it issues S = Q K^T as 36 MMAs of
 //     M=128 x N=128 x K=16 into one of two TMEM accumulators (so the MMAs of one
 //     superblock overlap the softmax of the previous one), streaming K through a
-//     ring of [128 tokens x 64 columns] TMA tiles.  Eight softmax warps (one
+//     ring of [128 tokens x 128 columns] entries (two swizzled 64-column atoms).  Eight softmax warps (one
 //     64-token page each per head row) keep the running max with a lazy rescale
 //     (the reference max only moves when a block exceeds it by more than kTau in
 //     log2 units, which is exact in real arithmetic), write P as 16-bit swizzled
 //     tiles into a double-buffered staging area, and a copier warp bulk-copies
 //     them, with the per-head rescale factors, into the value CTA.
 //   * value CTA (rank 1): O lives in TMEM as two 256-column halves.  Its own TMA
-//     stream brings each page's value columns; for each superblock it issues all
+//     stream brings each page's value columns (one 4-D box of four atoms per
+//     256 columns); for each superblock it issues all
 //     M=128 x N=256 x K=16 MMAs of half 0 (P from shared memory, K-major, as A;
 //     V from shared memory, N-major, as B), then those of half 1.  Two groups of
 //     four correction warps, one per half, rescale their half of O when the
 //     score CTA moved its reference max, so one half is rescaled while the
-//     other half's MMAs still run, and write the epilogue (O / l to out, or to
-//     the split workspace).
+//     other half's MMAs still run, and write the epilogue (O / l to out through
+//     a shared-memory staging tile, or to the split workspace, whose rows are
+//     interleaved per 4-column chunk so that a warp writes 512 contiguous bytes).
 // Every wait is bounded; a wait that runs out records MLA_ERR_DEVICE_TIMEOUT
 // with the wait site as detail, and the CTA unwinds.
 #include <cuda.h>
@@ -64,10 +70,6 @@ constexpr int kNV = MLA_NV;              // V half-page tiles in flight (value C
 #endif
 constexpr int kNPR = MLA_NPR;            // P tiles in the value CTA's ring
 constexpr int kStages = 2;               // P staging buffers in the score CTA
-#ifndef MLA_V4D
-#define MLA_V4D 1
-#endif
-constexpr bool kV4d = MLA_V4D != 0;      // V tiles as one 4-D box (else four 3-D boxes)
 #ifndef MLA_TAU
 #define MLA_TAU 0.0f
 #endif
@@ -715,8 +717,8 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
 // into 64-wide blocks) lands all four in one TMA request; per request the SM's
 // TMA unit moves ~84 GB/s with 32 KB boxes, against 36-55 GB/s with 8 KB ones.
 template <typename T>
-__device__ void value_producer(const FwdArgs &a, const CUtensorMap *map, const CUtensorMap *map4,
-                               uint8_t *smem, const Ctx &c, int part) {
+__device__ void value_producer(const FwdArgs &a, const CUtensorMap *map4, uint8_t *smem,
+                               const Ctx &c, int part) {
   Bars *b = c.bars;
   uint32_t vc = 0;
   const bool leader = elect_one();
@@ -735,15 +737,8 @@ __device__ void value_producer(const FwdArgs &a, const CUtensorMap *map, const C
         if (use > 0 && !wait_bar<false>(c, &b->v_empty[slot], (use - 1) & 1, W_V_EMPTY)) return false;
         if (leader) {
           mbar_arrive_expect_tx(&b->v_full[slot], kVSlot);
-          uint8_t *dst = smem + kOffV + slot * kVSlot;
-          if (kV4d) {
-            tma_load_4d(dst, map4, &b->v_full[slot], 0, j.pg.row0[p], 4 * g, j.pg.page[p]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              tma_load_3d(dst + i * kChunk, map, &b->v_full[slot], 64 * (4 * g + i), j.pg.row0[p],
-                          j.pg.page[p]);
-          }
+          tma_load_4d(smem + kOffV + slot * kVSlot, map4, &b->v_full[slot], 0, j.pg.row0[p], 4 * g,
+                      j.pg.page[p]);
         }
       }
     }
@@ -879,13 +874,37 @@ __device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int
   const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
   const int lane = threadIdx.x & 31;
   const int row0 = head - lane;  // the warp's first row
+  if (nsplit != 1) {
+    // partials: the next 32 columns' TMEM load is in flight while the current ones
+    // are stored
+    float4 *o = reinterpret_cast<float4 *>(a.oaccum) + ((int64_t)split * 128 + 64 * g) * a.h + head;
+    uint32_t x[2][32];
+    tmem_ld32(tO, x[0]);
+    tmem_wait_ld_regs(x[0]);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (q < 7) tmem_ld32(tO + 32 * (q + 1), x[(q + 1) & 1]);
+      if (head_ok) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t *v = &x[q & 1][4 * k];
+          o[(int64_t)(8 * q + k) * a.h] = make_float4(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv,
+                                                      __uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
+        }
+      }
+      if (q < 7) tmem_wait_ld_regs(x[(q + 1) & 1]);
+    }
+    return;
+  }
+  // one split: 16-bit rows of `out`, every lane takes part (the tile is shared by
+  // the warp)
 #pragma unroll 1
   for (int i = 0; i < 4; ++i) {
     uint32_t w[2][32];
     tmem_ld32(tO + 64 * i, w[0]);
     tmem_ld32(tO + 64 * i + 32, w[1]);
     tmem_wait_ld();
-    if (nsplit == 1) {  // every lane takes part (the tile is shared by the warp)
+    {
       T *o = reinterpret_cast<T *>(a.out) + (int64_t)seq * a.o_batch_stride + 256 * g + 64 * i;
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
@@ -905,15 +924,6 @@ __device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int
             *reinterpret_cast<uint4 *>(o + (int64_t)(row0 + row) * a.o_head_stride + 32 * t + 8 * j) = v;
         }
         __syncwarp();
-      }
-    } else if (head_ok) {
-      float4 *o = reinterpret_cast<float4 *>(a.oaccum) +
-                  ((int64_t)split * 128 + 64 * g + 16 * i) * a.h + head;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint32_t *x = &w[k >> 3][4 * (k & 7)];
-        o[(int64_t)k * a.h] = make_float4(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv,
-                                          __uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv);
       }
     }
   }
@@ -1102,7 +1112,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
     // warp 0: V producer, 1: MMA, 2-5 / 6-9: correction and epilogue of O half 0 / 1,
     // 10: P-tile receiver
     if (warp == 0) {
-      value_producer<T>(a, &kv_map, &kv4_map, smem, c, part);
+      value_producer<T>(a, &kv4_map, smem, c, part);
     } else if (warp == 1) {
       value_mma<T>(a, smem, c, part, tmem);
     } else if (warp < 10) {
