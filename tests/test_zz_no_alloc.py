@@ -55,6 +55,22 @@ def test_rejects_oversized_problem_before_touching_device(mla):
     assert lib.mla_decode_fwd_static(None, None) == MLA_ERR_NULL
 
 
+def test_rejects_by_query_rows(mla):
+    """With several query tokens the scratch holds seqlen_q * h rows per split: at two
+    tokens of 128 heads, 127 splits fit in 64 MiB and 128 do not; more than 1024
+    rows per sequence is a shape error."""
+    lib = mla._load()
+    rows = 2 * 128
+    parts, _ = mla.mla_metadata_shape(1, rows, 152)
+    assert mla.mla_workspace_size(127 - parts, rows, parts) <= mla.STATIC_WORKSPACE_BYTES
+    assert mla.mla_workspace_size(128 - parts, rows, parts) > mla.STATIC_WORKSPACE_BYTES
+    p = mla.FwdParams()
+    p.b, p.seqlen_q, p.h, p.h_k, p.num_sm_parts = 128 - parts, 2, 128, 1, parts
+    assert lib.mla_decode_fwd_static(ctypes.byref(p), None) == MLA_ERR_WORKSPACE
+    p.b, p.seqlen_q = 1, 9  # 9 x 128 = 1152 rows
+    assert lib.mla_decode_fwd_static(ctypes.byref(p), None) == MLA_ERR_SHAPE
+
+
 def _compare_two_calls(mla, w, num_sm=None):
     inp = workloads.make_inputs(w, device="cuda")
     meta, num_splits = mla.mla_get_metadata(inp["cache_seqlens"], w.heads, num_sm)
