@@ -53,3 +53,26 @@ def test_mtp_workload_full_size():
     """b=64, two causal query tokens, h=128, L=4096: 256 query rows per sequence."""
     w = workloads.get("mtp")
     P.check_workload(w, seqs=workloads.sample_seqs(w, 6))
+
+
+def test_query_tokens_with_split_layout_and_static_entry():
+    """Two causal query tokens with Q / Q_pe and KV / K_pe as separate tensors, through
+    the workspace entry and the no-workspace entry: both bit-identical to the fused
+    call, which matches the oracle."""
+    import torch
+
+    import mla_decode_gb300 as mla
+    w = workloads.custom(3, 128, (2, 700, 1500), "bf16", seed=420, name="qtok_sep",
+                         seqlen_q=2, causal=True)
+    inputs = workloads.make_inputs(w, "cuda")
+    stats, fused_o, fused_l, meta, ns, _ = P.check_workload(w, inputs=inputs)
+    q, kv = inputs["q"], inputs["kv_cache"]
+    sep = dict(q_pe=q[..., 512:].contiguous(), k_pe=kv[..., 512:].contiguous())
+    args = (q[..., :512].contiguous(), kv[..., :512].contiguous(), inputs["block_table"],
+            inputs["cache_seqlens"], w.softmax_scale, meta, ns)
+    out, lse = mla.mla_decode_fwd(*args, is_causal=True, **sep)
+    assert torch.equal(out, fused_o) and torch.equal(lse, fused_l)
+    out_s, lse_s = mla.mla_decode_fwd_static(*args, is_causal=True, **sep)
+    code, detail = mla.mla_get_device_error()
+    assert code == 0, f"device error {code}, detail {detail}"
+    assert torch.equal(out_s, fused_o) and torch.equal(lse_s, fused_l)
