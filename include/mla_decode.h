@@ -242,8 +242,9 @@ int mla_decode_fwd_timed(const mla_fwd_params *params, void *stream, void *split
 
 /*
  * Size of the library's built-in per-device scratch used by
- * mla_decode_fwd_static: 64 MiB, enough for b + num_sm_parts <= 255 at h = 128
- * (b = 128 with 76 parts needs 53.6 MB; see mla_workspace_size).
+ * mla_decode_fwd_static: 64 MiB, enough for b + num_sm_parts <= 255 at 128 query
+ * rows (b = 128 with 76 parts needs 53.6 MB) and <= 127 at 256 rows (two query
+ * tokens of 128 heads); see mla_workspace_size.
  */
 #define MLA_STATIC_WORKSPACE_BYTES (64u << 20)
 
