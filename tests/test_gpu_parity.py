@@ -92,6 +92,22 @@ def test_out_of_range_page_is_reported_and_gpu_stays_usable():
     P.check_workload(w, inputs=inputs)
 
 
+def test_length_past_table_capacity_is_reported_and_gpu_stays_usable():
+    """cache_seqlens beyond max_blocks * page_size: the kernel reports the sequence,
+    reads only clamped, in-range pages, and the next correct call passes parity."""
+    import mla_decode_gb300 as mla
+    w = workloads.custom(2, 16, (100, 100), "bf16", seed=4, name="capacity")
+    inputs = workloads.make_inputs(w, "cuda")
+    bad = dict(inputs)
+    bad["cache_seqlens"] = torch.tensor([100, 300], dtype=torch.int32, device="cuda")  # 300 > 2 * 64
+    meta, ns = mla.mla_get_metadata(bad["cache_seqlens"], w.heads)
+    mla.mla_decode_fwd(bad["q"], bad["kv_cache"], bad["block_table"], bad["cache_seqlens"],
+                       w.softmax_scale, meta, ns)
+    code, detail = mla.mla_get_device_error()
+    assert code == mla_status("MLA_ERR_DEVICE_BOUNDS") and detail == 1
+    P.check_workload(w, inputs=inputs)
+
+
 def mla_status(name):
     return {"MLA_ERR_DEVICE_BOUNDS": -9, "MLA_ERR_DEVICE_TIMEOUT": -8}[name]
 
