@@ -85,7 +85,8 @@ enum { MLA_DTYPE_FP16 = 0, MLA_DTYPE_BF16 = 1 };
  * (mla_metadata_shape, mla_get_metadata, mla_workspace_size).
  *
  * Tensors (device, caller-owned):
- *   q            [b][1][h][576]        strides q_batch_stride, q_head_stride;
+ *   q            [b][s][h][576]        strides q_batch_stride, q_head_stride
+ *                                      (token stride h * q_head_stride);
  *                                      the 576 columns contiguous.
  *   kv_cache     [num_pages][page_block_size][1][576]
  *                                      strides kv_page_stride, kv_row_stride;
@@ -96,8 +97,8 @@ enum { MLA_DTYPE_FP16 = 0, MLA_DTYPE_BF16 = 1 };
  *   q_pe, k_pe   optional split layout [TL §Split Kernel: Q / Q_pe and
  *                KV / K_pe are separate tensors, and the score is
  *                Q.KV^T + Q_pe.K_pe^T].  When q_pe is non-NULL, q holds only
- *                the 512 latent columns ([b][1][h][512], same strides) and
- *                q_pe [b][1][h][64] the RoPE columns (strides
+ *                the 512 latent columns ([b][s][h][512], same strides) and
+ *                q_pe [b][s][h][64] the RoPE columns (strides
  *                q_pe_batch_stride, q_pe_head_stride).  When k_pe is
  *                non-NULL, kv_cache rows hold only the 512 latent columns
  *                (which are also the value) and k_pe
@@ -111,17 +112,20 @@ enum { MLA_DTYPE_FP16 = 0, MLA_DTYPE_BF16 = 1 };
  *                ceil(L_i / page_block_size) entries of row i are read; each
  *                must lie in [0, num_pages).
  *   cache_seqlens int32 [b], 0 <= L_i <= max_blocks_per_seq*page_block_size.
- *   out          [b][1][h][512]        strides o_batch_stride, o_head_stride.
+ *   out          [b][s][h][512]        strides o_batch_stride, o_head_stride
+ *                                      (token stride h * o_head_stride).
  *   lse          fp32 [b][s * h]       stride lse_batch_stride (rows
  *                contiguous); natural-log log-sum-exp of the scaled scores,
  *                -inf for a row that sees no token (whose out row is zeros).
  *   tile_scheduler_metadata, num_splits: as written by mla_get_metadata for
- *                the same cache_seqlens, b, h and num_sm.
- *   workspace    at least mla_workspace_size(b, h, num_sm_parts) bytes, 16-byte
- *                aligned; holds per-split partial outputs and their LSEs.
+ *                the same cache_seqlens, b, s * h and num_sm.
+ *   workspace    at least mla_workspace_size(b, s * h, num_sm_parts) bytes,
+ *                16-byte aligned; holds per-split partial outputs and their
+ *                LSEs (the layout is the library's own).
  *
- * Result: out[i][0][j][:] = sum_t softmax_t(s) * kv[t][0:512] with
- * s_t = softmax_scale * q[i][0][j][:] . kv[t][:] over t < L_i, computed with
+ * Result: out[i][qi][j][:] = sum_t softmax_t(x) * kv[t][0:512] with
+ * x_t = softmax_scale * q[i][qi][j][:] . kv[t][:] over the tokens t that query
+ * token qi sees (all t < L_i, or t < L_i - (s - 1 - qi) with is_causal), computed with
  * exp2-based online softmax, split-KV partials and a combine pass
  * [TL §Split Kernel, §Combine Kernel].  Accumulation is fp32; the softmax
  * weights are rounded to the input dtype before the value product.
