@@ -33,6 +33,7 @@ METRIC = ("MLA decode TFLOPS and effective HBM GB/s on 1 GB300 (paged bf16), "
           "% of roofline")
 UNIT = "TFLOP/s"
 FALLBACK_HBM_GBS = 6800.0
+EVENT_EVERY = 5  # timed steps between two event-instrumented split launches
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -151,18 +152,25 @@ class ClockSampler:
         self.torch_index = torch_index
 
     def _run(self):
+        # back-to-back queries with a short sleep between them; each sample carries
+        # its host time so that the ones inside the timed window can be picked out
         clk = ctypes.c_uint()
         rs = ctypes.c_ulonglong()
         while not self._stop.is_set():
             if self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0 and \
                     self._reasons_fn(self.handle, ctypes.byref(rs)) == 0:
-                self.samples.append((clk.value, int(rs.value)))
-            time.sleep(0.002)
+                self.samples.append((time.perf_counter(), clk.value, int(rs.value)))
+            time.sleep(0.00005)
 
     def start(self):
+        """Start sampling; returns once the first sample is in (so that a timed region
+        that follows is covered from its start)."""
         if self.nvml:
             self._thread = threading.Thread(target=self._run, daemon=True)
             self._thread.start()
+            t0 = time.perf_counter()
+            while not self.samples and time.perf_counter() - t0 < 2.0:
+                time.sleep(0.0005)
         else:
             try:
                 self._proc = subprocess.Popen(
@@ -173,30 +181,37 @@ class ClockSampler:
             except Exception:
                 self._proc = None
 
-    def stop(self):
+    def stop(self, t_begin=None, t_end=None):
+        """Stop sampling and summarise the samples taken between t_begin and t_end
+        (host perf_counter times; all samples when not given)."""
         if self._thread:
             self._stop.set()
             self._thread.join()
         if self._proc:
             self._proc.terminate()
             out, _ = self._proc.communicate(timeout=5)
+            now = time.perf_counter()
             for line in out.splitlines():
                 try:
                     a, b, c = [x.strip() for x in line.split(",")]
                     self.max_mhz = float(b)
-                    self.samples.append((float(a), int(c, 16)))
+                    self.samples.append((now, float(a), int(c, 16)))
                 except Exception:
                     pass
-        if not self.samples:
+        sel = [x for x in self.samples
+               if (t_begin is None or x[0] >= t_begin) and (t_end is None or x[0] <= t_end)]
+        src = "nvml" if self.nvml else "nvidia-smi"
+        if not sel:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
-                    "source": "nvml" if self.nvml else "nvidia-smi"}
+                    "source": src}
         mask = 0
-        for _, r in self.samples:
+        for _, _, r in sel:
             mask |= r
         reasons = [n for bit, n in self.REASONS.items() if mask & bit and n != "gpu_idle"]
-        return {"sm_mhz": statistics.median(s for s, _ in self.samples),
-                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples),
-                "source": "nvml" if self.nvml else "nvidia-smi"}
+        return {"sm_mhz": statistics.median(c for _, c, _ in sel),
+                "sm_min_mhz": min(c for _, c, _ in sel),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(sel),
+                "source": src}
 
 
 def max_over_ranks(x, world, device):
@@ -350,11 +365,11 @@ def run_ours(args):
     calls = [mla.prepare_decode(s["q"], s["kv_cache"], s["block_table"], s["cache_seqlens"],
                                 w.softmax_scale, meta, nsplit, out, lse, ws, q_pe=s["q_pe"],
                                 k_pe=s["k_pe"], is_causal=w.causal) for s in sets]
+    metas = [mla.prepare_metadata(s["cache_seqlens"], w.heads, num_sm, meta, nsplit,
+                                  seqlen_q=w.seqlen_q) for s in sets]
 
     def step(i, events=None):
-        s = sets[i % len(sets)]
-        mla.mla_get_metadata(s["cache_seqlens"], w.heads, num_sm, meta, nsplit,
-                             seqlen_q=w.seqlen_q)
+        metas[i % len(metas)]()
         calls[i % len(calls)](split_events=events)
 
     for i in range(args.warmup):
@@ -365,28 +380,35 @@ def run_ours(args):
         raise RuntimeError(f"device error {code} detail {detail}")
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
-    for a, b in ev:  # materialise the raw events
+    # the split kernel's duration: CUDA events recorded around it on a sample of the
+    # timed steps (every EVENT_EVERY-th).  An event between two kernels ends the
+    # programmatic overlap of the second one's launch with the first one's tail, so
+    # events on every step would add their cost to every step
+    timed = [i for i in range(K) if i % EVENT_EVERY == 0]
+    ev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for i in timed}
+    for a, b in ev.values():  # materialise the raw events
         a.record()
         b.record()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
+    clocks.start()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
+    h0 = time.perf_counter()
     t0.record()
     for i in range(K):
-        step(i, ev[i])
+        step(i, ev.get(i))
     t1.record()
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    h1 = time.perf_counter()
+    clk = clocks.stop(h0, h1)
     if world > 1:
         dist.barrier()
     ms = t0.elapsed_time(t1) / K
-    split_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    split_ms = sum(a.elapsed_time(b) for a, b in ev.values()) / len(ev)
     code, detail = mla.mla_get_device_error()
     if code != 0:
         raise RuntimeError(f"device error {code} detail {detail}")
@@ -402,14 +424,15 @@ def run_ours(args):
                                   dbuf["cache_seqlens"], w.softmax_scale, meta, nsplit, out, lse,
                                   ws, q_pe=dbuf.get("q_pe"), k_pe=dbuf.get("k_pe"),
                                   is_causal=w.causal)
+    e2e_meta = mla.prepare_metadata(dbuf["cache_seqlens"], w.heads, num_sm, meta, nsplit,
+                                    seqlen_q=w.seqlen_q)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
 
     def e2e_step():
         for k in dbuf:
             dbuf[k].copy_(host[k], non_blocking=True)
-        mla.mla_get_metadata(dbuf["cache_seqlens"], w.heads, num_sm, meta, nsplit,
-                             seqlen_q=w.seqlen_q)
+        e2e_meta()
         e2e_call()
         hout.copy_(out, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
@@ -439,7 +462,8 @@ def run_ours(args):
     # peaks (fp16 runs at bf16's nominal tensor rate); the kernel is timed alone in a
     # ~100 us launch, so the burst tensor peak applies
     tflops_achieved = flops / (split_ms * 1e-3) / 1e12
-    roofline = {"kernel": "split", "kernel_ms": split_ms, "traffic": traffic,
+    roofline = {"kernel": "split", "kernel_ms": split_ms, "kernel_launches_timed": len(ev),
+                "traffic": traffic,
                 "hbm_frac": achieved / hbm_peak, "tensor_frac": tflops_achieved / bf16_peak}
     if flops / (bf16_peak * 1e12) > nbytes / (hbm_peak * 1e9):
         roofline.update(bound="tensor", achieved=tflops_achieved, peak=bf16_peak, unit="TFLOP/s",

@@ -67,6 +67,31 @@ typedef enum {
 enum { MLA_DTYPE_FP16 = 0, MLA_DTYPE_BF16 = 1 };
 
 /*
+ * Detail code of MLA_ERR_DEVICE_TIMEOUT: the split kernel's wait that gave up
+ * (every wait is bounded at 1 s).  The score CTA of a 2-CTA cluster streams K and
+ * computes the scores and the softmax; the value CTA streams V and accumulates O.
+ */
+typedef enum {
+  MLA_WAIT_K_EMPTY = 1,      /* score: K producer waits for a free ring slot */
+  MLA_WAIT_Q_FREE = 2,       /* score: the previous segment's MMAs are done with Q */
+  MLA_WAIT_S_FREE = 3,       /* score: the softmax has read an S buffer */
+  MLA_WAIT_K_FULL = 4,       /* score: MMA warp waits for K (or Q) data */
+  MLA_WAIT_S_FULL = 5,       /* score: softmax waits for S */
+  MLA_WAIT_STAGE_FREE = 6,   /* score: a P staging tile has left for the value CTA */
+  MLA_WAIT_HDR_FREE = 7,     /* score: the value CTA has read a rescale header */
+  MLA_WAIT_SLOT_FREE = 8,    /* score: a P slot of the value CTA is free */
+  MLA_WAIT_V_EMPTY = 9,      /* value: V producer waits for a free ring slot */
+  MLA_WAIT_O_FREE = 10,      /* value: the epilogue has read O */
+  MLA_WAIT_O_READY = 11,     /* value: O has been rescaled */
+  MLA_WAIT_P_FULL = 12,      /* value: a P tile has arrived */
+  MLA_WAIT_V_FULL = 13,      /* value: V data has arrived */
+  MLA_WAIT_HDR_FULL = 14,    /* value: a rescale header has arrived */
+  MLA_WAIT_O_DONE = 15,      /* value: the P.V MMAs of a superblock are done */
+  MLA_WAIT_STAGE_READY = 16, /* score: copier waits for staged P tiles */
+  MLA_WAIT_Q8_FULL = 17      /* score: the RoPE columns of Q have arrived */
+} mla_wait_site;
+
+/*
  * Arguments of one decode call.  Follows the field set of FlashMLA's
  * Flash_fwd_mla_params [FM §内存访问优化], including seqlen_q and is_causal;
  * with one KV head, ngroups (query heads per KV head) is h and h_h_k_ratio
@@ -272,7 +297,10 @@ int mla_decode_fwd_timed(const mla_fwd_params *params, void *stream, void *split
  *
  * The first call on a device, made with that device current, looks up the
  * array's device address (cudaGetSymbolAddress) and caches it; make that first
- * call before any stream capture.  Nothing in the array has to start at zero:
+ * call before any stream capture.  The cached address (like the device error
+ * word's) belongs to that device's primary context: after cudaDeviceReset on
+ * the device it is stale, and the library must not be called on that device
+ * again in the same process.  Nothing in the array has to start at zero:
  * every partial the combine kernel reads was written by the split kernel
  * earlier in the same call, so what an earlier call left there is never read.
  * All calls on a device share the one array, so calls that overlap on the GPU
@@ -280,6 +308,20 @@ int mla_decode_fwd_timed(const mla_fwd_params *params, void *stream, void *split
  * on it and give wrong results: order them on one stream or with events.
  */
 int mla_decode_fwd_static(const mla_fwd_params *params, void *stream);
+
+/*
+ * Test hook for the device-side failure path; not for production use.  The
+ * source pages have no counterpart.  Validates `params` exactly as
+ * mla_decode_fwd does, then launches only the split kernel with its load warps
+ * switched off: no TMA load and no copy between the two CTAs of a cluster is
+ * issued, so nothing is in flight, and the score CTA's MMA warp gives up its
+ * first wait for K data after about 1 ms (instead of 1 s).  The kernel records
+ * MLA_ERR_DEVICE_TIMEOUT with detail MLA_WAIT_K_FULL, every role of every
+ * cluster unwinds, and the kernel exits normally; read the error with
+ * mla_get_device_error.  out, lse and the workspace are left unspecified, and
+ * the context stays usable: the next call computes normally.
+ */
+int mla_test_forced_timeout(const mla_fwd_params *params, void *stream);
 
 /*
  * Synchronises `stream`, then returns (and clears) the device error word of

@@ -18,8 +18,8 @@ from . import _build
 __all__ = [
     "MlaError", "mla_abi_version", "mla_status_string", "mla_device_num_sm",
     "mla_metadata_shape", "mla_get_metadata", "mla_workspace_size", "mla_decode_fwd",
-    "mla_decode_fwd_timed", "prepare_decode", "DecodeCall",
-    "mla_get_device_error", "library_path", "HEAD_DIM", "HEAD_DIM_V", "ROPE_DIM", "BLOCK_N",
+    "mla_decode_fwd_timed", "prepare_decode", "DecodeCall", "prepare_metadata", "MetadataCall",
+    "mla_get_device_error", "mla_test_forced_timeout", "library_path", "HEAD_DIM", "HEAD_DIM_V", "ROPE_DIM", "BLOCK_N",
     "META_STRIDE", "SCHED_FIXED_COST",
 ]
 
@@ -94,9 +94,10 @@ def _load():
     lib.mla_decode_fwd_timed.argtypes = [ctypes.POINTER(FwdParams), _vp, _vp, _vp]
     lib.mla_decode_fwd_static.argtypes = [ctypes.POINTER(FwdParams), _vp]
     lib.mla_get_device_error.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
+    lib.mla_test_forced_timeout.argtypes = [ctypes.POINTER(FwdParams), _vp]
     for name in ("mla_device_num_sm", "mla_metadata_shape", "mla_get_metadata",
                  "mla_workspace_size", "mla_decode_fwd", "mla_decode_fwd_timed",
-                 "mla_get_device_error"):
+                 "mla_decode_fwd_static", "mla_get_device_error", "mla_test_forced_timeout"):
         getattr(lib, name).restype = ctypes.c_int
     if lib.mla_abi_version() != ABI_VERSION or lib.mla_fwd_params_size() != ctypes.sizeof(FwdParams):
         raise ImportError("MLA decode library ABI mismatch; rebuild it")
@@ -167,6 +168,51 @@ def mla_get_metadata(cache_seqlens, h, num_sm=None, tile_scheduler_metadata=None
                                         _vp(meta.data_ptr()), _vp(num_splits.data_ptr()),
                                         _stream(dev)), "mla_get_metadata")
     return meta, num_splits
+
+
+class MetadataCall:
+    """A validated, pre-marshalled mla_get_metadata call (reusable: re-run it after
+    updating cache_seqlens in place)."""
+
+    def __init__(self, cache_seqlens, rows, num_sm, meta, num_splits):
+        self._keep = (cache_seqlens, meta, num_splits)
+        self.device = cache_seqlens.device
+        self._args = (_vp(cache_seqlens.data_ptr()), cache_seqlens.numel(), int(rows),
+                      int(num_sm), _vp(meta.data_ptr()), _vp(num_splits.data_ptr()))
+        self.meta, self.num_splits = meta, num_splits
+
+    def __call__(self):
+        lib = _load()
+        with torch.cuda.device(self.device):
+            _check(lib.mla_get_metadata(*self._args, _stream(self.device)), "mla_get_metadata")
+        return self.meta, self.num_splits
+
+
+def prepare_metadata(cache_seqlens, h, num_sm=None, tile_scheduler_metadata=None,
+                     num_splits=None, seqlen_q=1):
+    """mla_get_metadata's checks and output allocation, done once; returns a
+    MetadataCall that launches the metadata kernel on the current stream."""
+    if cache_seqlens.dtype != torch.int32 or not cache_seqlens.is_cuda or cache_seqlens.dim() != 1:
+        raise ValueError("cache_seqlens must be a CUDA int32 vector")
+    if not cache_seqlens.is_contiguous():
+        raise ValueError("cache_seqlens must be contiguous")
+    dev = cache_seqlens.device
+    if num_sm is None:
+        num_sm = mla_device_num_sm(dev)
+    rows = int(h) * int(seqlen_q)
+    b = cache_seqlens.numel()
+    parts, stride = mla_metadata_shape(b, rows, num_sm)
+    meta = tile_scheduler_metadata
+    if meta is None:
+        meta = torch.empty((parts, stride), dtype=torch.int32, device=dev)
+    if num_splits is None:
+        num_splits = torch.empty((b + 1,), dtype=torch.int32, device=dev)
+    if (meta.shape != (parts, stride) or meta.dtype != torch.int32 or not meta.is_contiguous()
+            or meta.device != dev or num_splits.shape != (b + 1,)
+            or num_splits.dtype != torch.int32 or not num_splits.is_contiguous()
+            or num_splits.device != dev):
+        raise ValueError("metadata outputs have the wrong shape/dtype/device")
+    return MetadataCall(cache_seqlens, rows, num_sm, meta, num_splits)
 
 
 def mla_workspace_size(b, h, num_sm_parts):
@@ -345,6 +391,15 @@ def mla_decode_fwd_static(q, kv_cache, block_table, cache_seqlens, softmax_scale
         rc = lib.mla_decode_fwd_static(ctypes.byref(call.params), _stream(call.device))
     _check(rc, "mla_decode_fwd_static")
     return call.out, call.lse
+
+
+def mla_test_forced_timeout(call):
+    """Test hook: run the split kernel of a prepared DecodeCall with its load warps
+    switched off, so that its first wait for K data gives up after ~1 ms.  Returns
+    the C status of the launch; read the recorded error with mla_get_device_error."""
+    lib = _load()
+    with torch.cuda.device(call.device):
+        return lib.mla_test_forced_timeout(ctypes.byref(call.params), _stream(call.device))
 
 
 def mla_get_device_error(device=None):

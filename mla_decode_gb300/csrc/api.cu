@@ -57,10 +57,6 @@ void *static_workspace() {
 
 int max_splits_for(int b, int num_parts) { return b + num_parts; }
 
-cudaError_t launch_split(const FwdArgs &a, cudaStream_t s) { return launch_split_tc(a, s); }
-
-cudaError_t split_num_sm(int device, int *num_sm) { return split_tc_num_sm(device, num_sm); }
-
 size_t workspace_bytes_for(int b, int h, int num_parts) {
   size_t splits = (size_t)max_splits_for(b, num_parts);
   size_t o = splits * (size_t)h * MLA_HEAD_DIM_V * sizeof(float);
@@ -109,7 +105,7 @@ int mla_device_num_sm(int device, int *num_sm) {
   if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MLA_ERR_CUDA;
   if (prop.major != 10 || prop.minor != 3) return MLA_ERR_ARCH;
   int n = 0;
-  if (split_num_sm(device, &n) != cudaSuccess || n < 2) return MLA_ERR_CUDA;
+  if (split_tc_num_sm(device, &n) != cudaSuccess || n < 2) return MLA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
   g_num_sm[device] = n;
   *num_sm = n;
@@ -164,8 +160,12 @@ int mla_decode_fwd_static(const mla_fwd_params *p, void *stream) {
   return mla_decode_fwd(&with_ws, stream);
 }
 
-int mla_decode_fwd_timed(const mla_fwd_params *p, void *stream, void *split_begin,
-                         void *split_end) {
+}  // extern "C"
+
+namespace {
+
+// Validates *p on the host and resolves it into the kernels' arguments.
+int resolve_args(const mla_fwd_params *p, FwdArgs &a) {
   if (!p) return MLA_ERR_NULL;
   if (!p->q || !p->kv_cache || !p->block_table || !p->cache_seqlens || !p->out || !p->lse ||
       !p->tile_scheduler_metadata || !p->num_splits || !p->workspace)
@@ -204,7 +204,6 @@ int mla_decode_fwd_timed(const mla_fwd_params *p, void *stream, void *split_begi
   int *err = device_error_word();
   if (!err) return MLA_ERR_CUDA;
 
-  FwdArgs a;
   a.b = p->b;
   a.h = rows;
   a.q_len = p->seqlen_q;
@@ -245,15 +244,36 @@ int mla_decode_fwd_timed(const mla_fwd_params *p, void *stream, void *split_begi
   a.lseaccum = reinterpret_cast<float *>(static_cast<char *>(p->workspace) +
                                          (size_t)a.max_splits * rows * MLA_HEAD_DIM_V * sizeof(float));
   a.err = err;
+  a.forced_timeout = 0;
+  return MLA_OK;
+}
 
+}  // namespace
+
+extern "C" {
+
+int mla_decode_fwd_timed(const mla_fwd_params *p, void *stream, void *split_begin,
+                         void *split_end) {
+  FwdArgs a;
+  const int rc = resolve_args(p, a);
+  if (rc != MLA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (split_begin && cudaEventRecord(static_cast<cudaEvent_t>(split_begin), s) != cudaSuccess)
     return MLA_ERR_CUDA;
-  if (launch_split(a, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_split_tc(a, s) != cudaSuccess) return MLA_ERR_CUDA;
   if (split_end && cudaEventRecord(static_cast<cudaEvent_t>(split_end), s) != cudaSuccess)
     return MLA_ERR_CUDA;
   if (launch_combine(a, s) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
+}
+
+int mla_test_forced_timeout(const mla_fwd_params *p, void *stream) {
+  FwdArgs a;
+  const int rc = resolve_args(p, a);
+  if (rc != MLA_OK) return rc;
+  a.forced_timeout = 1;
+  return launch_split_tc(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK
+                                                                               : MLA_ERR_CUDA;
 }
 
 int mla_get_device_error(void *stream, int *detail) {

@@ -16,6 +16,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace mla {
 namespace {
@@ -26,6 +27,10 @@ constexpr int kChunks = 8;  // 4-column chunks per warp: 32 columns
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 combine_kernel(FwdArgs a) {
+  // launched with programmatic stream serialisation: the split kernel's partials
+  // are read only once it has completed
+  sm100::grid_dependency_wait();
+  sm100::launch_dependents();
   const int seq = blockIdx.x;
   const int s0 = a.num_splits[seq];
   const int n = a.num_splits[seq + 1] - s0;
@@ -109,12 +114,17 @@ combine_kernel(FwdArgs a) {
 }  // namespace
 
 cudaError_t launch_combine(const FwdArgs &a, cudaStream_t s) {
-  dim3 grid(a.b, (a.h + 31) / 32, 4);
-  if (a.dtype == MLA_DTYPE_BF16)
-    combine_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, s>>>(a);
-  else
-    combine_kernel<__half><<<grid, kWarps * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.b, (a.h + 31) / 32, 4);
+  cfg.blockDim = dim3(kWarps * 32, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return a.dtype == MLA_DTYPE_BF16 ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, a)
+                                   : cudaLaunchKernelEx(&cfg, combine_kernel<__half>, a);
 }
 
 }  // namespace mla

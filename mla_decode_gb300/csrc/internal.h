@@ -41,6 +41,7 @@ struct FwdArgs {
   float *lseaccum;  // [max_splits][h], base-2 units
   int max_splits;
   int *err;         // device error word (two ints: code, detail)
+  int forced_timeout;  // test hook: load warps idle, the K wait gives up after 1 ms
 };
 
 int max_splits_for(int b, int num_parts);
@@ -51,10 +52,8 @@ int *device_error_word();
 
 cudaError_t launch_metadata(const int32_t *seqlens, int b, int parts, int fixed,
                             int32_t *meta, int32_t *num_splits, cudaStream_t s);
-cudaError_t launch_split(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_split_tc(const FwdArgs &a, cudaStream_t s);
 cudaError_t split_tc_num_sm(int device, int *num_sm);
 cudaError_t launch_combine(const FwdArgs &a, cudaStream_t s);
-cudaError_t split_num_sm(int device, int *num_sm);
 
 }  // namespace mla

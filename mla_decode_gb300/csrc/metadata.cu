@@ -17,6 +17,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace mla {
 namespace {
@@ -66,6 +67,10 @@ metadata_kernel(const int32_t *__restrict__ seqlens, int b, int parts, int fixed
   __shared__ int64_t chunk_start[kMetaThreads];
   __shared__ int64_t warp_sums[kMetaWarps];
   const int tid = threadIdx.x;
+  // launched with programmatic stream serialisation: cache_seqlens may have been
+  // written, and meta / num_splits still be read, by the kernels before this one
+  sm100::grid_dependency_wait();
+  sm100::launch_dependents();
 
   // Phase 1: thread t owns sequences [t per, (t + 1) per); the block scan of the
   // chunk costs gives each chunk's start on the cost axis, and TOTAL.
@@ -157,8 +162,17 @@ cudaError_t launch_metadata(const int32_t *seqlens, int b, int parts, int fixed,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  metadata_kernel<<<1, kMetaThreads, smem, s>>>(seqlens, b, parts, fixed, meta, num_splits);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(kMetaThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, metadata_kernel, seqlens, b, parts, fixed, meta, num_splits);
 }
 
 }  // namespace mla

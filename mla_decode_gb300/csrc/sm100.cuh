@@ -142,6 +142,20 @@ __device__ __forceinline__ bool bar_red_or(int id, int count, bool pred) {
   return out != 0;
 }
 
+// ----------------------------------------------------------------------------- dependent launch
+
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialisation attribute may start while the kernel before it in the
+// stream is still running.  grid_dependency_wait() blocks until that kernel has
+// completed and its memory is visible; launch_dependents() lets the next kernel
+// start launching.  Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {

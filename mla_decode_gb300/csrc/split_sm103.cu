@@ -23,11 +23,13 @@
 //     M=128 x N=128 x K=16 into one of two TMEM accumulators (so the MMAs of one
 //     superblock overlap the softmax of the previous one), streaming K through a
 //     ring of [128 tokens x 128 columns] entries (two swizzled 64-column atoms).  Eight softmax warps (one
-//     64-token page each per head row) keep the running max with a lazy rescale
-//     (the reference max only moves when a block exceeds it by more than kTau in
-//     log2 units, which is exact in real arithmetic), write P as 16-bit swizzled
-//     tiles into a double-buffered staging area, and a copier warp bulk-copies
-//     them, with the per-head rescale factors, into the value CTA.
+//     64-token page each per head row) keep the running max (the reference max
+//     moves whenever a block exceeds it), write P as 16-bit swizzled tiles into a
+//     double-buffered staging area, and a copier warp bulk-copies them, with the
+//     per-head rescale factors, into the value CTA.  Two row sums are kept: of the
+//     fp32 weights (for the LSE) and of the weights as rounded to 16 bits (the
+//     ones P . V used), by which O is divided, so that O is a convex combination
+//     of the value rows with exactly the weights the MMAs applied.
 //   * value CTA (rank 1): O lives in TMEM as two 256-column halves.  Its own TMA
 //     stream brings each page's value columns (one 4-D box of four atoms per
 //     256 columns); for each superblock it issues all
@@ -44,6 +46,7 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -57,36 +60,23 @@ using namespace sm100;
 constexpr int kThreads = 352;            // 11 warps (see the role map in the kernel)
 constexpr int kSB = 2;                   // pages (64 tokens each) per superblock
 constexpr int kSBTok = 64 * kSB;         // tokens per superblock: N of the score MMAs
-#ifndef MLA_NK
-#define MLA_NK 4
-#endif
-constexpr int kNK = MLA_NK;              // K chunks in flight (score CTA)
-#ifndef MLA_NV
-#define MLA_NV 4
-#endif
-constexpr int kNV = MLA_NV;              // V half-page tiles in flight (value CTA)
-#ifndef MLA_NPR
-#define MLA_NPR 4
-#endif
-constexpr int kNPR = MLA_NPR;            // P tiles in the value CTA's ring
+constexpr int kNK = 4;                   // K chunks in flight (score CTA)
+constexpr int kNV = 4;                   // V half-page tiles in flight (value CTA)
+constexpr int kNPR = 4;                  // P tiles in the value CTA's ring
 constexpr int kStages = 2;               // P staging buffers in the score CTA
-#ifndef MLA_TAU
-#define MLA_TAU 0.0f
-#endif
-constexpr float kTau = MLA_TAU;          // lazy-rescale threshold, log2 units
 constexpr int kChunk = 8192;             // [64 rows][128 B] swizzled TMA box
 constexpr int kAtom = kSB * kChunk;      // one superblock's tokens x 64 columns (16 KB)
 constexpr int kKSlot = 2 * kAtom;        // K chunk: 128 columns as two 64-column atoms
 constexpr int kKChunks = 5;              // chunks per superblock: 4 x 128 latent + RoPE
 constexpr int kVSlot = 4 * kChunk;       // 256 value columns of one page
 constexpr int kPTile = 16384;            // [128 heads][64 tokens] 16-bit, swizzled
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // every wait: 1 s
+constexpr uint64_t kForcedWaitNs = 1000000ull;     // the forced-timeout test's K wait: 1 ms
 
 struct Header {  // score -> value CTA, one per superblock
-  float alpha[128];
-  float l[128];
-  float m[128];
-  uint32_t flags;  // bit 1: last superblock of the segment
+  float alpha[128];  // O rescale factor per row
+  float l[128];      // last superblock: row sum of the 16-bit weights (divides O)
+  uint32_t flags;    // bit 1: last superblock of the segment
   uint32_t pad[3];
 };
 static_assert(sizeof(Header) % 16 == 0, "bulk copies move multiples of 16 bytes");
@@ -96,8 +86,8 @@ constexpr int kOffQ8 = 0;                                     // score: Q column
 constexpr int kOffK = kOffQ8 + kAtom;                         // score: K ring
 constexpr int kOffPStage = kOffK + kNK * kKSlot;              // score: P staging tiles
 constexpr int kOffHdrStage = kOffPStage + kStages * kSB * kPTile;  // score: 2 headers
-constexpr int kOffRed = kOffHdrStage + 2 * (int)sizeof(Header);    // score: [2][2][128] floats
-constexpr int kScoreEnd = kOffRed + 4 * 128 * 4;
+constexpr int kOffRed = kOffHdrStage + 2 * (int)sizeof(Header);    // score: [3][2][128] floats
+constexpr int kScoreEnd = kOffRed + 6 * 128 * 4;
 constexpr int kOffV = 0;                                      // value: V ring
 constexpr int kOffPRing = kOffV + kNV * kVSlot;               // value: P tiles
 constexpr int kOffHdr = kOffPRing + kNPR * kPTile;            // value: 2 headers
@@ -126,55 +116,20 @@ struct Bars {
 constexpr int kSmemBytes = kOffBars + (int)sizeof(Bars) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
-// wait sites (reported as the error detail on a timeout)
+// wait sites, reported as the error detail on a timeout (mla_wait_site)
 enum : int {
-  W_K_EMPTY = 1, W_Q_FREE, W_S_FREE, W_K_FULL, W_S_FULL, W_STAGE_FREE, W_HDR_FREE, W_SLOT_FREE,
-  W_V_EMPTY, W_O_FREE, W_O_READY, W_P_FULL, W_V_FULL, W_HDR_FULL, W_O_DONE, W_STAGE_READY,
-  W_Q8_FULL
+  W_K_EMPTY = MLA_WAIT_K_EMPTY, W_Q_FREE = MLA_WAIT_Q_FREE, W_S_FREE = MLA_WAIT_S_FREE,
+  W_K_FULL = MLA_WAIT_K_FULL, W_S_FULL = MLA_WAIT_S_FULL, W_STAGE_FREE = MLA_WAIT_STAGE_FREE,
+  W_HDR_FREE = MLA_WAIT_HDR_FREE, W_SLOT_FREE = MLA_WAIT_SLOT_FREE, W_V_EMPTY = MLA_WAIT_V_EMPTY,
+  W_O_FREE = MLA_WAIT_O_FREE, W_O_READY = MLA_WAIT_O_READY, W_P_FULL = MLA_WAIT_P_FULL,
+  W_V_FULL = MLA_WAIT_V_FULL, W_HDR_FULL = MLA_WAIT_HDR_FULL, W_O_DONE = MLA_WAIT_O_DONE,
+  W_STAGE_READY = MLA_WAIT_STAGE_READY, W_Q8_FULL = MLA_WAIT_Q8_FULL
 };
-
-// Optional wait profile (build with -DMLA_WAIT_PROFILE=1): per part, CTA, warp
-// and wait site (or timed phase), the time lane 0 spent there, plus each warp's
-// role start and end; read back with mla_debug_wait_profile().
-#if MLA_WAIT_PROFILE
-constexpr int kProfParts = 128, kProfSites = 32;
-__device__ unsigned long long g_wait_ns[kProfParts][2][kThreads / 32][kProfSites];
-__device__ unsigned long long g_role_ns[kProfParts][2][kThreads / 32][2];
-__device__ unsigned long long g_chunk_trace[1024][3];
-__device__ unsigned long long g_part_gt[kProfParts][2][3];  // per part and CTA: entry, roles start, roles end (ns)  // part 0, score MMA: per chunk before wait, after wait, after commit
-__device__ __forceinline__ void prof_chunk(uint32_t n, int which) {
-  if (blockIdx.x == 0 && blockIdx.y == 0 && (threadIdx.x & 31) == 0 && n < 1024)
-    g_chunk_trace[n][which] = clock64();
-}
-// (SM clock cycles: cheap to read, and every interval is taken on one SM)
-__device__ __forceinline__ uint64_t prof_now() { return clock64(); }
-__device__ __forceinline__ void prof_wait(int where, uint64_t t0) {
-  const int part = blockIdx.x >> 1;
-  if ((threadIdx.x & 31) == 0 && blockIdx.y == 0 && part < kProfParts && where < kProfSites)
-    atomicAdd(&g_wait_ns[part][blockIdx.x & 1][threadIdx.x >> 5][where],
-              (unsigned long long)(clock64() - t0));
-}
-__device__ __forceinline__ void prof_role(int which) {
-  const int part = blockIdx.x >> 1;
-  if ((threadIdx.x & 31) == 0 && blockIdx.y == 0 && part < kProfParts)
-    g_role_ns[part][blockIdx.x & 1][threadIdx.x >> 5][which] = clock64();
-}
-__device__ __forceinline__ void prof_part(int which) {
-  const int part = blockIdx.x >> 1;
-  if (threadIdx.x == 0 && blockIdx.y == 0 && part < kProfParts)
-    g_part_gt[part][blockIdx.x & 1][which] = globaltimer_ns();
-}
-#else
-__device__ __forceinline__ void prof_part(int) {}
-__device__ __forceinline__ void prof_chunk(uint32_t, int) {}
-__device__ __forceinline__ uint64_t prof_now() { return 0; }
-__device__ __forceinline__ void prof_wait(int, uint64_t) {}
-__device__ __forceinline__ void prof_role(int) {}
-#endif
 
 struct Ctx {
   Bars *bars;
   int *err;
+  uint64_t limit_ns;  // how long a wait may take before it gives up
   __device__ bool aborted() const { return *reinterpret_cast<volatile int *>(&bars->abort) != 0; }
 };
 
@@ -190,7 +145,7 @@ __device__ __noinline__ bool wait_bar_slow(const Ctx &c, uint32_t addr, uint32_t
     for (int i = 0; i < 64; ++i)
       if (kCl ? mbar_try_wait_cluster(addr, parity) : mbar_try_wait(addr, parity)) return true;
     if (*reinterpret_cast<volatile int *>(&c.bars->abort)) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > c.limit_ns) {
       c.bars->abort = 1;
       const uint32_t peer = map_to_rank(smem_u32(&c.bars->abort), cluster_ctarank() ^ 1);
       asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer), "r"(1) : "memory");
@@ -202,16 +157,8 @@ __device__ __noinline__ bool wait_bar_slow(const Ctx &c, uint32_t addr, uint32_t
 
 template <bool kCl>
 __device__ __forceinline__ bool wait_addr(const Ctx &c, uint32_t addr, uint32_t parity, int where) {
-#if MLA_WAIT_PROFILE
-  const uint64_t tp = prof_now();
-  const bool ok = (kCl ? mbar_try_wait_cluster(addr, parity) : mbar_try_wait(addr, parity)) ||
-                  wait_bar_slow<kCl>(c, addr, parity, where);
-  prof_wait(where, tp);
-  return ok;
-#else
   if (kCl ? mbar_try_wait_cluster(addr, parity) : mbar_try_wait(addr, parity)) return true;
   return wait_bar_slow<kCl>(c, addr, parity, where);
-#endif
 }
 
 template <bool kCl>
@@ -306,10 +253,15 @@ __device__ __forceinline__ void finish_sb_pages(const FwdArgs &a, int seq, int n
 }
 
 template <typename T> struct Pack;
+// two(lo, hi): a packed pair of 16-bit values; sum(u): the sum of a packed pair,
+// as floats (the values the MMA reads).
 template <> struct Pack<__nv_bfloat16> {
   static __device__ __forceinline__ uint32_t two(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+  }
+  static __device__ __forceinline__ float sum(uint32_t u) {
+    return __uint_as_float(u << 16) + __uint_as_float(u & 0xffff0000u);
   }
   static constexpr bool kBf16 = true;
 };
@@ -317,6 +269,10 @@ template <> struct Pack<__half> {
   static __device__ __forceinline__ uint32_t two(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+  }
+  static __device__ __forceinline__ float sum(uint32_t u) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u));
+    return f.x + f.y;
   }
   static constexpr bool kBf16 = false;
 };
@@ -463,7 +419,6 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
   const uint32_t kfull = smem_u32(&b->k_full[0]), kempty = smem_u32(&b->k_empty[0]);
   uint32_t slot = 0, phase = 0;  // K ring position of the next chunk and its k_full parity
   uint32_t sb = 0, segn = 0;
-  uint32_t nch = 0;  // chunks issued (profile trace only)
   const bool leader = elect_one();
   SegWalk walk(a, part);
   Seg s;
@@ -503,10 +458,8 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
       const uint32_t tS = tmem + 256 + kSBTok * buf;
 #pragma unroll 1
       for (int ch = 0; ch < kKChunks; ++ch) {
-        prof_chunk(nch, 0);
         if (!wait_addr<false>(c, kfull + 8 * slot, phase, W_K_FULL)) return;
         tc_fence_after();
-        prof_chunk(nch, 1);
         const uint64_t bd = kdesc + (uint64_t)(slot * (kKSlot >> 4));
         if (leader) {
           if (ch < 4) {
@@ -520,7 +473,6 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
           }
           mma_commit_addr(kempty + 8 * slot);
         }
-        prof_chunk(nch++, 2);
         if (++slot == kNK) {
           slot = 0;
           phase ^= 1u;
@@ -583,7 +535,8 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
   const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
   const uint32_t tS = tmem + 256 + lane_off + 64 * half;
   float *red_max = reinterpret_cast<float *>(smem + kOffRed);  // [2][128]
-  float *red_sum = red_max + 256;                               // [2][128]
+  float *red_sum = red_max + 256;                               // [2][128] fp32 weights
+  float *red_sumr = red_max + 512;                              // [2][128] 16-bit weights
   const float scale = a.scale_log2;
   uint32_t sb = 0;
   TileUse tu;  // staging tile buf * kSB + t
@@ -597,7 +550,11 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       }
       continue;
     }
-    float m_ref = -INFINITY, l = 0.f;
+    // l: row sum of the fp32 weights (the LSE); lr: of the weights rounded to the
+    // input dtype, which is what P . V summed (O / lr is then exactly a weighted
+    // mean of the value rows: a row dominated by one token gives that token's value
+    // rather than value * (1 + the rounding error of its weight))
+    float m_ref = -INFINITY, l = 0.f, lr = 0.f;
     const int nsb = (s.hi - s.lo + kSB - 1) / kSB;
     for (int j = 0; j < nsb; ++j, ++sb) {
       const int sb0 = s.lo + j * kSB;
@@ -606,15 +563,12 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       const uint32_t buf = sb & 1;
       bool ok = wait_bar<false>(c, &b->s_full[buf], (sb >> 1) & 1, W_S_FULL);
       tc_fence_after();
-      uint64_t tp = prof_now();
       uint32_t v[2][32];
       tmem_ld32(tS + kSBTok * buf, v[0]);
       tmem_ld32(tS + kSBTok * buf + 32, v[1]);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&b->s_free[buf]);
-      prof_wait(19, tp);
-      tp = prof_now();
 
       // base-2 units; tokens this row does not see (a suffix of my page, all of it
       // when it starts past the row's end) and a page past the segment end (all of
@@ -641,13 +595,10 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       const float mloc = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                                fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       red_max[half * 128 + r] = mloc;
-      prof_wait(20, tp);
-      tp = prof_now();
       if (bar_red_or(1, 256, !ok || c.aborted())) return;  // all softmax threads leave together
-      prof_wait(17, tp);
       const float m_blk = fmaxf(red_max[r], red_max[128 + r]);
       float alpha = 1.f;
-      if (m_blk > m_ref + kTau) {  // also the first block (m_ref = -inf)
+      if (m_blk > m_ref) {  // also the first block (m_ref = -inf)
         alpha = fast_exp2(m_ref - m_blk);
         m_ref = m_blk;
       }
@@ -655,10 +606,11 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       const int tb = buf * kSB + half;
       if (ok && half < np && tu.was_used(tb))
         ok = wait_bar<true>(c, &b->stage_free[tb], tu.parity(tb) ^ 1u, W_STAGE_FREE);
-      tp = prof_now();
-      float ps[8];
+      float ps[8], pr[4];
 #pragma unroll
       for (int e = 0; e < 8; ++e) ps[e] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pr[e] = 0.f;
       const bool write = ok && half < np;
       const uint32_t row = smem_u32(smem + kOffPStage + tb * kPTile) + r * 128;
       // a row that has seen no token yet (causal rows only) has m_ref = -inf: its
@@ -672,28 +624,28 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
           p[e] = fast_exp2(fmaf(__uint_as_float(v[ch >> 2][(ch & 3) * 8 + e]), sc, nm));
           ps[e] += p[e];
         }
-        if (write)
-          st_shared_v4(row + ((ch ^ (r & 7)) << 4), Pack<T>::two(p[0], p[1]),
-                       Pack<T>::two(p[2], p[3]), Pack<T>::two(p[4], p[5]),
-                       Pack<T>::two(p[6], p[7]));
+        uint32_t u[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          u[e] = Pack<T>::two(p[2 * e], p[2 * e + 1]);
+          pr[e] += Pack<T>::sum(u[e]);
+        }
+        if (write) st_shared_v4(row + ((ch ^ (r & 7)) << 4), u[0], u[1], u[2], u[3]);
       }
       red_sum[half * 128 + r] = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      prof_wait(21, tp);
+      red_sumr[half * 128 + r] = (pr[0] + pr[1]) + (pr[2] + pr[3]);
       const int hs = sb & 1;
       Header *hdr = reinterpret_cast<Header *>(smem + kOffHdrStage + hs * sizeof(Header));
       if (ok && half == 0 && sb >= 2)
         ok = wait_bar<true>(c, &b->hdr_free[hs], ((sb >> 1) - 1) & 1, W_HDR_FREE);
-      tp = prof_now();
       if (bar_red_or(1, 256, !ok || c.aborted())) return;
-      prof_wait(18, tp);
-      tp = prof_now();
       l = l * alpha + (red_sum[r] + red_sum[128 + r]);
+      lr = lr * alpha + (red_sumr[r] + red_sumr[128 + r]);
       if (half == 0) {
         // the first superblock of a segment overwrites O: nothing to rescale
         hdr->alpha[r] = j == 0 ? 1.f : alpha;
         if (last) {
-          hdr->l[r] = l;
-          hdr->m[r] = m_ref;
+          hdr->l[r] = lr;
           if (head_ok) {
             const float lse2 = m_ref + fast_log2(l);
             if (s.nsplit == 1) a.lse[(int64_t)s.seq * a.lse_stride + head] = lse2 * kLn2;
@@ -704,7 +656,6 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       if (sw == 0 && lane == 0) hdr->flags = last ? 2u : 0u;
       fence_proxy_async_smem();
       mbar_arrive(&b->stage_ready[buf]);  // the copier ships the tiles and the header
-      prof_wait(22, tp);
       tu.advance(buf * kSB, np);
     }
   }
@@ -990,7 +941,6 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
       if (ok && (int)sb >= 2) ok = wait_done((int)sb - 2);
       if (ok && resc) ok = wait_done((int)sb - 1);
       if (ok && resc) {
-        const uint64_t tr = prof_now();
         tc_fence_after();
 #pragma unroll 1
         for (int i = 0; i < 4; ++i) {
@@ -1008,17 +958,14 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
         }
         tmem_wait_st();
         tc_fence_before();
-        prof_wait(27, tr);
       }
       mbar_arrive(&b->o_ready[g][sb & 1]);
       if (flags & 2u) {  // epilogue
         if (ok) ok = wait_done((int)sb);
         if (bar_red_or(bar_id, 128, !ok || c.aborted())) return;
         tc_fence_after();
-        const uint64_t te = prof_now();
         write_out<T>(a, s.seq, s.split, s.nsplit, head, head_ok, g, tO, lrow,
                      smem_u32(smem + kOffEpi + (warp - 2) * 2048));
-        prof_wait(26, te);
         tc_fence_before();
         mbar_arrive(&b->o_free);
       }
@@ -1042,7 +989,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
   const uint32_t role = cluster_ctarank();  // 0: score CTA, 1: value CTA
   const int part = blockIdx.x >> 1;
   const int head0 = blockIdx.y * 128;
-  prof_part(0);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNK; ++i) {
@@ -1090,29 +1036,36 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
   __syncthreads();
   tc_fence_after();
   cluster_sync();  // peer barriers initialised before any remote arrive or copy
+  // everything above overlaps the previous kernel in the stream (launched with
+  // programmatic stream serialisation); the metadata and the buffers it wrote are
+  // read only after it has completed
+  grid_dependency_wait();
+  launch_dependents();
   const uint32_t tmem = b->tmem_base;
-  const Ctx c{b, a.err};
-  prof_role(0);
-  prof_part(1);
+  const Ctx c{b, a.err, kWaitLimitNs};
 
+  // forced-timeout test (a.forced_timeout): the load and copy warps issue nothing,
+  // so nothing is in flight, and the score MMA warp's first wait for K data gives
+  // up after 1 ms; every other role sees the abort and unwinds
+  const bool loads = !a.forced_timeout;
   if (role == 0) {
     // warp 0: K producer, 1: MMA, 2-9: softmax, 10: P/header copier.  Each role has
     // a whole warp (a diverged spin loop would starve the other lanes' path, and
     // warp-uniform issue loops let one elected lane issue at full rate).
     if (warp == 0) {
-      score_producer<T>(a, &kv_map, &q_map, &kpe_map, &qpe_map, smem, c, part, head0);
+      if (loads) score_producer<T>(a, &kv_map, &q_map, &kpe_map, &qpe_map, smem, c, part, head0);
     } else if (warp == 1) {
-      score_mma<T>(a, smem, c, part, tmem);
+      score_mma<T>(a, smem, loads ? c : Ctx{b, a.err, kForcedWaitNs}, part, tmem);
     } else if (warp < 10) {
       score_softmax<T>(a, smem, c, part, tmem, head0);
     } else {
-      score_copier(a, smem, c, part);
+      if (loads) score_copier(a, smem, c, part);
     }
   } else {
     // warp 0: V producer, 1: MMA, 2-5 / 6-9: correction and epilogue of O half 0 / 1,
     // 10: P-tile receiver
     if (warp == 0) {
-      value_producer<T>(a, &kv4_map, smem, c, part);
+      if (loads) value_producer<T>(a, &kv4_map, smem, c, part);
     } else if (warp == 1) {
       value_mma<T>(a, smem, c, part, tmem);
     } else if (warp < 10) {
@@ -1122,7 +1075,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
     }
   }
 
-  prof_role(1);
   tc_fence_before();
   __syncthreads();
   if (*reinterpret_cast<volatile int *>(&b->abort)) {
@@ -1132,7 +1084,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
     while (globaltimer_ns() - t0 < 100000ull) {
     }
   }
-  prof_part(2);
   cluster_sync();
   if (warp == 1) {
     tc_fence_after();
@@ -1174,6 +1125,25 @@ cudaError_t make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t m
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The kernel's dynamic shared-memory limit is an attribute of the function in the
+// current device's context, so it is set once per device (and per element type).
+constexpr int kMaxDevices = 64;
+template <typename T>
+cudaError_t smem_attr() {
+  static std::atomic<bool> done[kMaxDevices];
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  e = cudaFuncSetAttribute(split_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
+  return e;
+}
+
 template <typename T>
 cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
   constexpr uint64_t kLatent = MLA_HEAD_DIM_V, kRope = MLA_HEAD_DIM - MLA_HEAD_DIM_V;
@@ -1206,76 +1176,55 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(split_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    kSmemBytes);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  if ((e = smem_attr<T>()) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * a.num_parts, (a.h + 127) / 128, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, split_tc_kernel<T>, map, qmap, pemap, qpemap, map4, a);
 }
 
 }  // namespace
-
-#if MLA_WAIT_PROFILE
-extern "C" int mla_debug_wait_profile(void *waits, size_t wbytes, void *roles, size_t rbytes) {
-  if (wbytes > sizeof(g_wait_ns)) wbytes = sizeof(g_wait_ns);
-  if (rbytes > sizeof(g_role_ns)) rbytes = sizeof(g_role_ns);
-  if (cudaMemcpyFromSymbol(waits, g_wait_ns, wbytes) != cudaSuccess) return -7;
-  return cudaMemcpyFromSymbol(roles, g_role_ns, rbytes) == cudaSuccess ? 0 : -7;
-}
-extern "C" int mla_debug_chunk_trace(void *dst, size_t bytes) {
-  if (bytes > sizeof(g_chunk_trace)) bytes = sizeof(g_chunk_trace);
-  return cudaMemcpyFromSymbol(dst, g_chunk_trace, bytes) == cudaSuccess ? 0 : -7;
-}
-extern "C" int mla_debug_part_times(void *dst, size_t bytes) {
-  if (bytes > sizeof(g_part_gt)) bytes = sizeof(g_part_gt);
-  return cudaMemcpyFromSymbol(dst, g_part_gt, bytes) == cudaSuccess ? 0 : -7;
-}
-extern "C" int mla_debug_wait_profile_clear(void) {
-  static unsigned long long zero[sizeof(g_wait_ns) / 8];
-  return cudaMemcpyToSymbol(g_wait_ns, zero, sizeof(g_wait_ns)) == cudaSuccess ? 0 : -7;
-}
-#endif
 
 cudaError_t launch_split_tc(const FwdArgs &a, cudaStream_t s) {
   return a.dtype == MLA_DTYPE_BF16 ? launch_typed<__nv_bfloat16>(a, s) : launch_typed<__half>(a, s);
 }
 
 cudaError_t split_tc_num_sm(int device, int *num_sm) {
-  cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<__nv_bfloat16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
   int prev = 0;
-  cudaGetDevice(&prev);
-  if (prev != device) cudaSetDevice(device);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * 256, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cudaError_t e = cudaGetDevice(&prev);
+  if (e != cudaSuccess) return e;
+  if (prev != device && (e = cudaSetDevice(device)) != cudaSuccess) return e;
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, split_tc_kernel<__nv_bfloat16>, &cfg);
-  if (prev != device) cudaSetDevice(prev);
+  e = smem_attr<__nv_bfloat16>();
+  if (e == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 256, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&clusters, split_tc_kernel<__nv_bfloat16>, &cfg);
+  }
+  if (prev != device) {
+    const cudaError_t r = cudaSetDevice(prev);
+    if (e == cudaSuccess) e = r;
+  }
   if (e != cudaSuccess) return e;
   *num_sm = 2 * clusters;
   return cudaSuccess;

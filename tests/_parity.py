@@ -2,17 +2,29 @@
 oracle on host copies of the very same inputs, compare with the stated bar.
 
 Tolerances (bf16/fp16 inputs, fp32 accumulation): out max-abs 2e-2 and
-mean-abs 2e-3; lse max-abs 1e-3 (natural log); an empty sequence must give
-out == 0 and lse == -inf exactly.
+mean-abs 2e-3, lse max-abs 1e-3 (natural log).  An empty row (a sequence of
+length 0, or a causal row that sees no token) must give out == 0 and lse == -inf
+exactly.
 
-The out bounds are applied to the error measured in units of the scale of the
-terms each output element sums: |gpu - ref| / max(1, w), w = sum_t p_t |v_t|
-(the oracle's weighted-absolute output, the forward-error bound of a weighted
-sum).  For unit-scale data w < 1 and this is exactly the absolute bound (every
-N(0,1) workload).  Where rows scaled x8 dominate, the terms reach |p v| ~ 24 and
-rounding each weight to 16 bits, at a running max of the kernel's choosing,
-moves an output by ~2^-9 * 24 even when the terms cancel to |out| < 1.
+How the out bar is read.  Each element's error is taken in units of the scale
+of the terms it sums:  e = |gpu - ref| / max(1, w),  w = sum_t p_t |v_t| (the
+oracle's weighted-absolute output, the forward-error bound of a weighted sum);
+max(e) <= 2e-2 and mean(e) <= 2e-3 on every element.  Where w <= 1 (unit-scale
+terms) this is the absolute error itself.  Two things the method fixes make the
+error grow with w rather than stay absolute: P is rounded to the input dtype
+before P.V (TileLang's split kernel casts acc_s to the input dtype), which moves
+an output by up to about 2^-9 w in bf16, and `out` is returned in the input
+dtype, whose own rounding at |out| = 8..16 is already 2^-5 in bf16.  Both bite
+only on the workload whose cache has rows scaled x8 (|out| up to ~40).  So, in
+addition, wherever the output format can hold the values to the bar (every
+|ref| below 8 for bf16, 64 for fp16: all the N(0, 1) workloads), the plain
+|gpu - ref| must meet max 2e-2 and mean 2e-3 too.  The log records the plain
+error, the weighted one and the error beyond the output format's rounding.
+
+Whole workloads are compared in chunks of sequences, so that the host copy of
+the pages a chunk reads stays within a fixed budget.
 """
+import json
 import os
 
 import numpy as np
@@ -26,6 +38,7 @@ OUT_MEAN_ABS = 2e-3
 LSE_MAX_ABS = 1e-3
 
 ORACLE_THREADS = max(1, min(32, os.cpu_count() or 1))
+HOST_KV_BUDGET = 1 << 30  # bytes of cache pages copied to the host per chunk
 
 
 def run_gpu(inputs, heads, scale, num_sm=None, is_causal=False):
@@ -69,40 +82,141 @@ def oracle_rows(w, inputs, seqs=None):
             absw.reshape(len(seqs), w.rows, -1))
 
 
+def seq_chunks(w, seqs, budget=HOST_KV_BUDGET):
+    """Consecutive groups of `seqs` whose pages take at most `budget` bytes on the host
+    (a sequence larger than the budget forms a group of its own)."""
+    page_bytes = w.page_size * workloads.D * 2
+    chunk, used = [], 0
+    for s in seqs:
+        b = max(1, w.blocks_per_seq[s]) * page_bytes
+        if chunk and used + b > budget:
+            yield chunk
+            chunk, used = [], 0
+        chunk.append(s)
+        used += b
+    if chunk:
+        yield chunk
+
+
+def half_ulp(x, dtype):
+    """Half the spacing of the 16-bit format `dtype` at |x| (0 at x = 0)."""
+    x = np.abs(x)
+    _, e = np.frexp(x)                    # x = m * 2^e, 0.5 <= m < 1
+    bits = 8 if dtype == "bf16" else 11   # significand bits, the implicit one included
+    h = np.ldexp(0.5, e - bits)
+    if dtype == "fp16":
+        h = np.maximum(h, 2.0 ** -25)     # subnormal spacing
+    return np.where(x == 0, 0.0, h)
+
+
+def representable_bar(dtype):
+    """Largest |out| below which half an ulp of `dtype` stays within the max-abs bar."""
+    return 8.0 if dtype == "bf16" else 64.0
+
+
+class ErrorStats:
+    """Running max and mean of the out error over every element compared (in units of
+    max(1, w); plain; beyond the output format's rounding), and the lse error."""
+
+    def __init__(self, dtype):
+        self.dtype = dtype
+        self.w_max = 0.0        # |gpu - ref| / max(1, w)
+        self.w_sum = 0.0
+        self.raw_max = 0.0      # |gpu - ref|
+        self.raw_sum = 0.0
+        self.fmt_max = 0.0      # max(0, |gpu - ref| - ulp/2)
+        self.count = 0
+        self.lse_max = 0.0
+        self.ref_max = 0.0
+        self.rows = 0
+
+    def add(self, out_gpu, lse_gpu, out_ref, lse_ref, abs_ref, what=""):
+        og = out_gpu.float().cpu().numpy().astype(np.float64)
+        lg = lse_gpu.float().cpu().numpy().astype(np.float64)
+        empty = np.isneginf(lse_ref)
+        assert np.all(np.isneginf(lg[empty])), f"{what}: empty rows must have lse -inf"
+        assert np.all(og[empty] == 0), f"{what}: empty rows must be zero"
+        assert np.all(np.isfinite(og)), f"{what}: non-finite output"
+        raw = np.abs(og - out_ref)
+        ew = raw / np.maximum(1.0, abs_ref)
+        self.w_max = max(self.w_max, float(ew.max(initial=0.0)))
+        self.w_sum += float(ew.sum())
+        self.raw_max = max(self.raw_max, float(raw.max(initial=0.0)))
+        self.raw_sum += float(raw.sum())
+        fmt = raw - half_ulp(np.maximum(np.abs(og), np.abs(out_ref)), self.dtype)
+        self.fmt_max = max(self.fmt_max, float(fmt.max(initial=0.0)))
+        self.count += raw.size
+        self.ref_max = max(self.ref_max, float(np.abs(out_ref).max(initial=0.0)))
+        full = ~empty
+        self.lse_max = max(self.lse_max, float(np.abs(lg[full] - lse_ref[full]).max(initial=0.0)))
+        self.rows += lse_ref.size
+
+    def mean(self, total):
+        return total / self.count if self.count else 0.0
+
+    def as_dict(self):
+        return {"out_max_abs": self.raw_max, "out_mean_abs": self.mean(self.raw_sum),
+                "out_max_weighted": self.w_max, "out_mean_weighted": self.mean(self.w_sum),
+                "out_max_beyond_format": self.fmt_max, "lse_max_abs": self.lse_max,
+                "ref_max_abs": self.ref_max, "rows": self.rows}
+
+    def check(self, what=""):
+        d = self.as_dict()
+        msg = (f"{what}: out max {d['out_max_abs']:.3e} mean {d['out_mean_abs']:.3e} "
+               f"(in units of max(1, w): max {d['out_max_weighted']:.3e} mean "
+               f"{d['out_mean_weighted']:.3e}; beyond the {self.dtype} rounding: max "
+               f"{d['out_max_beyond_format']:.3e}; |ref| up to {self.ref_max:.3g}); "
+               f"lse {self.lse_max:.3e}; {self.rows} rows")
+        assert d["out_max_weighted"] <= OUT_MAX_ABS, msg
+        assert d["out_mean_weighted"] <= OUT_MEAN_ABS, msg
+        assert self.lse_max <= LSE_MAX_ABS, msg
+        if self.ref_max < representable_bar(self.dtype):
+            assert d["out_max_abs"] <= OUT_MAX_ABS, msg
+            assert d["out_mean_abs"] <= OUT_MEAN_ABS, msg
+        return d
+
+
 def compare(out_gpu, lse_gpu, out_ref, lse_ref, abs_ref, what=""):
-    """out_gpu [n, h, 512] (any float dtype), lse_gpu [n, h]; refs float64 numpy
+    """out_gpu [n, rows, 512] (bf16 or fp16), lse_gpu [n, rows]; refs float64 numpy
     (abs_ref: the oracle's weighted-absolute scale of each output)."""
-    og = out_gpu.float().cpu().numpy().astype(np.float64)
-    lg = lse_gpu.float().cpu().numpy().astype(np.float64)
-    empty = np.isneginf(lse_ref)
-    assert np.all(np.isneginf(lg[empty])), f"{what}: empty rows must have lse -inf"
-    assert np.all(og[empty] == 0), f"{what}: empty rows must be zero"
-    assert np.all(np.isfinite(og)), f"{what}: non-finite output"
-    err = np.abs(og - out_ref) / np.maximum(1.0, abs_ref)
-    mx, mean = float(err.max(initial=0.0)), float(err.mean()) if err.size else 0.0
-    full = ~empty
-    lerr = float(np.abs(lg[full] - lse_ref[full]).max(initial=0.0))
-    msg = f"{what}: out max {mx:.3e} mean {mean:.3e} lse {lerr:.3e}"
-    assert mx <= OUT_MAX_ABS, msg
-    assert mean <= OUT_MEAN_ABS, msg
-    assert lerr <= LSE_MAX_ABS, msg
-    return {"out_max_abs": mx, "out_mean_abs": mean, "lse_max_abs": lerr}
+    st = ErrorStats("bf16" if out_gpu.dtype == torch.bfloat16 else "fp16")
+    st.add(out_gpu, lse_gpu, out_ref, lse_ref, abs_ref, what)
+    return st.check(what)
+
+
+def compare_chunked(w, inputs, outs, seqs=None, what=None):
+    """Compare GPU results with the oracle over `seqs` (all by default), a chunk of
+    sequences at a time.  outs: list of (label, out [b, s, h, 512], lse) to check
+    against the same oracle values.  Returns {label: stats}."""
+    seqs = list(range(w.batch)) if seqs is None else list(seqs)
+    stats = {label: ErrorStats(w.dtype) for label, _, _ in outs}
+    for chunk in seq_chunks(w, seqs):
+        ref_o, ref_l, ref_a = oracle_rows(w, inputs, chunk)
+        for label, out, lse in outs:
+            idx = torch.as_tensor(chunk, device=out.device)
+            stats[label].add(out[idx].reshape(len(chunk), w.rows, -1),
+                             lse[idx].reshape(len(chunk), w.rows), ref_o, ref_l, ref_a,
+                             what=f"{what or w.name}/{label}")
+    result = {}
+    for label, st in stats.items():
+        name = f"{what or w.name}/{label}" if len(stats) > 1 else (what or w.name)
+        _log(w, name, st.as_dict())
+        result[label] = st.check(name)
+    return result
+
+
+def _log(w, name, stats, num_sm=None):
+    log = os.environ.get("MLA_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"workload": name, "batch": w.batch, "heads": w.heads,
+                                "seqlen_q": w.seqlen_q, "causal": w.causal,
+                                "num_sm": num_sm, **stats}) + "\n")
 
 
 def check_workload(w, seqs=None, num_sm=None, poison_tail=False, inputs=None):
     if inputs is None:
         inputs = workloads.make_inputs(w, device="cuda", poison_tail=poison_tail)
     out, lse, meta, ns = run_gpu(inputs, w.heads, w.softmax_scale, num_sm, is_causal=w.causal)
-    ref_o, ref_l, ref_a = oracle_rows(w, inputs, seqs)
-    idx = torch.as_tensor(list(range(w.batch)) if seqs is None else list(seqs), device=out.device)
-    stats = compare(out[idx].reshape(len(idx), w.rows, -1), lse[idx].reshape(len(idx), w.rows),
-                    ref_o, ref_l, ref_a, what=w.name)
-    log = os.environ.get("MLA_PARITY_LOG")
-    if log:
-        import json
-        with open(log, "a") as f:
-            f.write(json.dumps({"workload": w.name, "batch": w.batch, "heads": w.heads,
-                                "seqlen_q": w.seqlen_q, "causal": w.causal,
-                                "num_sm": num_sm, "rows": int(idx.numel()) * w.rows,
-                                **stats}) + "\n")
+    stats = compare_chunked(w, inputs, [("out", out, lse)], seqs)["out"]
     return stats, out, lse, meta, ns, inputs

@@ -22,7 +22,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 MLA_ERR_NULL = -1
 MLA_ERR_SHAPE = -2
 MLA_ERR_WORKSPACE = -6
-OUT_MAX = 2e-2    # same bars as the parity tests, relative to max(1, |ref|)
+OUT_MAX = 2e-2    # same bars as the parity tests (absolute)
 LSE_MAX = 1e-3
 
 
@@ -88,7 +88,7 @@ def _compare_two_calls(mla, w, num_sm=None):
         code, detail = mla.mla_get_device_error()
         assert code == 0, f"call {call}: device error {code}, detail {detail}"
         ro, o = ref_out.float(), out.float()
-        err = ((o - ro).abs() / ro.abs().clamp_min(1.0)).max().item()
+        err = (o - ro).abs().max().item()
         assert err <= OUT_MAX, f"call {call}: out error {err}"
         fin = torch.isfinite(ref_lse)
         assert torch.equal(fin, torch.isfinite(lse)), f"call {call}: lse finiteness"
