@@ -47,8 +47,13 @@ extern "C" {
 #define MLA_BLOCK_N 64
 /* Integers per part in tile_scheduler_metadata. */
 #define MLA_META_STRIDE 8
-/* Fixed per-split cost, in 64-token blocks, used by the scheduler. */
+/* Fixed per-sequence cost, in 64-token blocks, on the scheduler's cost axis. */
 #define MLA_SCHED_FIXED_COST 5
+/* Cost of one segment (a part's share of one sequence), in 64-token blocks, by
+ * which the scheduler chooses how many parts to use. */
+#define MLA_SCHED_SEGMENT_COST 16
+/* Largest num_sm the scheduler accepts. */
+#define MLA_MAX_NUM_SM 2046
 
 typedef enum {
   MLA_OK = 0,
@@ -74,7 +79,7 @@ enum { MLA_DTYPE_FP16 = 0, MLA_DTYPE_BF16 = 1 };
 typedef enum {
   MLA_WAIT_K_EMPTY = 1,      /* score: K producer waits for a free ring slot */
   MLA_WAIT_Q_FREE = 2,       /* score: the previous segment's MMAs are done with Q */
-  MLA_WAIT_S_FREE = 3,       /* score: the softmax has read an S buffer */
+  MLA_WAIT_S_FREE = 3,       /* score: the softmax has read an S page buffer */
   MLA_WAIT_K_FULL = 4,       /* score: MMA warp waits for K (or Q) data */
   MLA_WAIT_S_FULL = 5,       /* score: softmax waits for S */
   MLA_WAIT_STAGE_FREE = 6,   /* score: a P staging tile has left for the value CTA */
@@ -87,8 +92,7 @@ typedef enum {
   MLA_WAIT_V_FULL = 13,      /* value: V data has arrived */
   MLA_WAIT_HDR_FULL = 14,    /* value: a rescale header has arrived */
   MLA_WAIT_O_DONE = 15,      /* value: the P.V MMAs of a superblock are done */
-  MLA_WAIT_STAGE_READY = 16, /* score: copier waits for staged P tiles */
-  MLA_WAIT_Q8_FULL = 17      /* score: the RoPE columns of Q have arrived */
+  MLA_WAIT_STAGE_READY = 16  /* score: copier waits for staged P tiles */
 } mla_wait_site;
 
 /*
@@ -235,9 +239,13 @@ int mla_metadata_shape(int b, int h, int num_sm, int *num_sm_parts, int *meta_st
  *   num_splits              device int32 [b + 1]: prefix sums; sequence i owns
  *       split slots num_splits[i] .. num_splits[i+1]-1 of the workspace.
  * Partition: sequences are laid end to end on a cost axis, each costing
- * MLA_SCHED_FIXED_COST + ceil(L_i/64) blocks; part k starts at cost position
- * floor(k*TOTAL/num_sm_parts).  Deterministic; the decode result does not
- * depend on it beyond rounding.
+ * MLA_SCHED_FIXED_COST + ceil(L_i/64) blocks; with P parts, part k starts at
+ * cost position floor(k*TOTAL/P).  P is chosen from ceil(num_sm_parts / 2) to
+ * num_sm_parts: part k of P costs MLA_SCHED_SEGMENT_COST per segment it holds
+ * (a sequence it touches) plus one per block, and the P whose most expensive
+ * part is cheapest is used (the larger on a tie).  Parts P..num_sm_parts-1 are
+ * empty: {b, 0, b, 0, num_splits[b], 0, 0, 0}.  Deterministic; the decode
+ * result does not depend on it beyond rounding.  num_sm <= MLA_MAX_NUM_SM.
  */
 int mla_get_metadata(const int32_t *cache_seqlens, int b, int h, int num_sm,
                      int32_t *tile_scheduler_metadata, int32_t *num_splits,

@@ -114,7 +114,7 @@ int mla_device_num_sm(int device, int *num_sm) {
 
 int mla_metadata_shape(int b, int h, int num_sm, int *num_sm_parts, int *meta_stride) {
   if (!num_sm_parts || !meta_stride) return MLA_ERR_NULL;
-  if (b < 1 || h < 1 || h > 1024 || num_sm < 1) return MLA_ERR_SHAPE;
+  if (b < 1 || h < 1 || h > 1024 || num_sm < 1 || num_sm > MLA_MAX_NUM_SM) return MLA_ERR_SHAPE;
   int parts = (num_sm / 2) / head_tiles(h);
   *num_sm_parts = parts < 1 ? 1 : parts;
   *meta_stride = MLA_META_STRIDE;
@@ -128,7 +128,7 @@ int mla_get_metadata(const int32_t *cache_seqlens, int b, int h, int num_sm,
   int rc = mla_metadata_shape(b, h, num_sm, &parts, &stride);
   if (rc != MLA_OK) return rc;
   cudaError_t e = launch_metadata(cache_seqlens, b, parts, MLA_SCHED_FIXED_COST,
-                                  tile_scheduler_metadata, num_splits,
+                                  MLA_SCHED_SEGMENT_COST, tile_scheduler_metadata, num_splits,
                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -225,6 +225,7 @@ int resolve_args(const mla_fwd_params *p, FwdArgs &a) {
   a.k_pe = sep_k ? p->k_pe : static_cast<const char *>(p->kv_cache) + rope_off;
   a.k_pe_page_stride = sep_k ? p->k_pe_page_stride : p->kv_page_stride;
   a.k_pe_row_stride = sep_k ? p->k_pe_row_stride : p->kv_row_stride;
+  a.k_fused = sep_k ? 0 : 1;
   a.num_pages = p->num_pages;
   a.page_size = p->page_block_size;
   a.block_table = p->block_table;

@@ -25,6 +25,7 @@ struct FwdArgs {
   int64_t q_pe_batch_stride, q_pe_head_stride;
   const void *k_pe;
   int64_t k_pe_page_stride, k_pe_row_stride;
+  int k_fused;       // the RoPE columns are columns 512..575 of each kv_cache row
   int num_pages, page_size;
   const int32_t *block_table;
   int64_t bt_stride;
@@ -50,7 +51,7 @@ size_t workspace_bytes_for(int b, int h, int num_parts);
 // device error word of the current device
 int *device_error_word();
 
-cudaError_t launch_metadata(const int32_t *seqlens, int b, int parts, int fixed,
+cudaError_t launch_metadata(const int32_t *seqlens, int b, int parts, int fixed, int seg_cost,
                             int32_t *meta, int32_t *num_splits, cudaStream_t s);
 cudaError_t launch_split_tc(const FwdArgs &a, cudaStream_t s);
 cudaError_t split_tc_num_sm(int device, int *num_sm);

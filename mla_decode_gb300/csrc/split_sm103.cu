@@ -17,14 +17,15 @@
 // How it is laid out on the GPU (this library's design, not the pages'): the
 // fp32 accumulator O[128 heads][512] fills an SM's whole tensor memory, so each
 // part is served by a cluster of two CTAs with different roles:
-//   * score CTA (cluster rank 0): Q columns 0..511 live in TMEM as the A operand
-//     (packed 16-bit pairs), the RoPE columns 512..575 in shared memory.  For a
-//     superblock of up to two 64-token pages it issues S = Q K^T as 36 MMAs of
-//     M=128 x N=128 x K=16 into one of two TMEM accumulators (so the MMAs of one
-//     superblock overlap the softmax of the previous one), streaming K through a
-//     ring of [128 tokens x 128 columns] entries (two swizzled 64-column atoms).  Eight softmax warps (one
-//     64-token page each per head row) keep the running max (the reference max
-//     moves whenever a block exceeds it), write P as 16-bit swizzled tiles into a
+//   * score CTA (cluster rank 0): all 576 Q columns live in TMEM as the A operand
+//     (packed 16-bit pairs, columns 0..287).  K streams through a ring of whole
+//     pages (one TMA request per page: 64 rows x 576 columns as nine swizzled
+//     64-column atoms), and per page S = Q K^T is 36 MMAs of M=128 x N=64 x K=16
+//     into one of three page accumulators in TMEM (so the MMAs run a superblock
+//     ahead of the softmax).  A superblock is two pages.  Eight softmax warps (one
+//     64-token page each per head row) keep a lazy running max (the reference max
+//     moves only when a block exceeds it by more than 2^8, so P <= 256 and O is
+//     rarely rescaled; exact in real arithmetic), write P as 16-bit swizzled tiles into a
 //     double-buffered staging area, and a copier warp bulk-copies them, with the
 //     per-head rescale factors, into the value CTA.  Two row sums are kept: of the
 //     fp32 weights (for the LSE) and of the weights as rounded to 16 bits (the
@@ -59,17 +60,23 @@ using namespace sm100;
 
 constexpr int kThreads = 352;            // 11 warps (see the role map in the kernel)
 constexpr int kSB = 2;                   // pages (64 tokens each) per superblock
-constexpr int kSBTok = 64 * kSB;         // tokens per superblock: N of the score MMAs
-constexpr int kNK = 4;                   // K chunks in flight (score CTA)
+constexpr int kNK = 2;                   // K ring entries (score CTA): one page each
 constexpr int kNV = 4;                   // V half-page tiles in flight (value CTA)
 constexpr int kNPR = 4;                  // P tiles in the value CTA's ring
-constexpr int kStages = 2;               // P staging buffers in the score CTA
-constexpr int kChunk = 8192;             // [64 rows][128 B] swizzled TMA box
-constexpr int kAtom = kSB * kChunk;      // one superblock's tokens x 64 columns (16 KB)
-constexpr int kKSlot = 2 * kAtom;        // K chunk: 128 columns as two 64-column atoms
-constexpr int kKChunks = 5;              // chunks per superblock: 4 x 128 latent + RoPE
+constexpr int kStageTiles = 4;           // P staging tiles in the score CTA (a ring)
+constexpr int kSBufs = 3;                // S accumulators in the score CTA's TMEM, one page each
+// score CTA TMEM columns: Q as packed 16-bit pairs (latent 0..255, RoPE 256..287),
+// then the S page accumulators (64 columns each)
+constexpr uint32_t kTQpe = 256;
+constexpr uint32_t kTS0 = 320;
+static_assert(kTS0 + 64 * kSBufs <= 512, "score TMEM budget");
+constexpr int kChunk = 8192;             // [64 rows][128 B] swizzled atom
+constexpr int kKPage = 9 * kChunk;       // K entry: one page's 576 columns as nine atoms (72 KB)
+constexpr int kQBox = 2 * kChunk;        // [128 rows][64 columns] of Q (16 KB)
 constexpr int kVSlot = 4 * kChunk;       // 256 value columns of one page
 constexpr int kPTile = 16384;            // [128 heads][64 tokens] 16-bit, swizzled
+constexpr float kTau = 8.f;              // lazy rescale: the reference max moves only when a
+                                         // block exceeds it by more than this (log2 units)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // every wait: 1 s
 constexpr uint64_t kForcedWaitNs = 1000000ull;     // the forced-timeout test's K wait: 1 ms
 
@@ -82,10 +89,9 @@ struct Header {  // score -> value CTA, one per superblock
 static_assert(sizeof(Header) % 16 == 0, "bulk copies move multiples of 16 bytes");
 
 // shared-memory map (offsets from the 1024-aligned base)
-constexpr int kOffQ8 = 0;                                     // score: Q columns 512..575
-constexpr int kOffK = kOffQ8 + kAtom;                         // score: K ring
-constexpr int kOffPStage = kOffK + kNK * kKSlot;              // score: P staging tiles
-constexpr int kOffHdrStage = kOffPStage + kStages * kSB * kPTile;  // score: 2 headers
+constexpr int kOffK = 0;                                      // score: K ring (whole pages)
+constexpr int kOffPStage = kOffK + kNK * kKPage;              // score: P staging tiles
+constexpr int kOffHdrStage = kOffPStage + kStageTiles * kPTile;    // score: 2 headers
 constexpr int kOffRed = kOffHdrStage + 2 * (int)sizeof(Header);    // score: [3][2][128] floats
 constexpr int kScoreEnd = kOffRed + 6 * 128 * 4;
 constexpr int kOffV = 0;                                      // value: V ring
@@ -98,11 +104,11 @@ constexpr int kOffBars = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 127)
 
 struct Bars {
   uint64_t k_full[kNK], k_empty[kNK];   // score
-  uint64_t s_full[2], s_free[2];        // score, per S buffer
+  uint64_t s_full[kSBufs], s_free[kSBufs];  // score, per S page buffer
   uint64_t q_free;                      // score: MMAs of a segment done with Q (MMA commit)
-  uint64_t q8_full;                     // score: Q RoPE tile landed (TMA)
-  uint64_t stage_ready[kStages];        // score: P tiles + header staged (softmax -> copier)
-  uint64_t stage_free[kStages * kSB];   // score, arrived by the value CTA
+  uint64_t qs_full;                     // score: first segment's Q columns 0..255 in staging
+  uint64_t stage_ready[2];              // score: a superblock's P tiles + header staged
+  uint64_t stage_free[kStageTiles];     // score: a staging tile's copy landed (value CTA)
   uint64_t slot_free[kNPR];             // score, value-CTA MMA commits (multicast)
   uint64_t hdr_free[2];                 // score, arrived by the value CTA (both groups)
   uint64_t v_full[kNV], v_empty[kNV];   // value
@@ -123,7 +129,7 @@ enum : int {
   W_HDR_FREE = MLA_WAIT_HDR_FREE, W_SLOT_FREE = MLA_WAIT_SLOT_FREE, W_V_EMPTY = MLA_WAIT_V_EMPTY,
   W_O_FREE = MLA_WAIT_O_FREE, W_O_READY = MLA_WAIT_O_READY, W_P_FULL = MLA_WAIT_P_FULL,
   W_V_FULL = MLA_WAIT_V_FULL, W_HDR_FULL = MLA_WAIT_HDR_FULL, W_O_DONE = MLA_WAIT_O_DONE,
-  W_STAGE_READY = MLA_WAIT_STAGE_READY, W_Q8_FULL = MLA_WAIT_Q8_FULL
+  W_STAGE_READY = MLA_WAIT_STAGE_READY
 };
 
 struct Ctx {
@@ -331,57 +337,78 @@ __device__ __forceinline__ void issue_job(const FwdArgs &a, SbWalk &w, SbJob &j)
 
 // ------------------------------------------------------------------------------ score CTA
 
-// K producer.  At a segment start it first brings that sequence's Q tile: the
-// 512 latent columns as eight [128 heads x 64] boxes through the K ring (the MMA
-// warp moves them into TMEM), the 64 RoPE columns straight into the Q8 tile once
-// the previous segment's MMAs are done with it.  Heads past h read as zeros.
-// The latent and RoPE columns come through separate tensor maps (map / qmap and
-// pemap / qpemap), so Q / Q_pe and KV / K_pe may be separate tensors.
+// K producer.  Each 64-token page of K arrives as ONE TMA request: a 4-D box of
+// the page's rows x all 576 columns, landing as nine swizzled [64 rows x 64
+// columns] atoms back to back (72 KB, one ring entry).  A TMA request carries a
+// fixed cost of a few hundred nanoseconds, so one SM streams whole pages at
+// 80-90 GB/s where [64 x 64] boxes (8 KB) reach about 24.  With Q_pe / K_pe as
+// separate tensors the entry is two requests: the 512 latent columns (eight
+// atoms) and the 64 RoPE columns.  At a segment start the ring first carries
+// that sequence's Q, which the MMA warp moves into TMEM: the 512 latent columns
+// as eight [128 heads x 64] boxes, four per entry, then the 64 RoPE columns.
+// Heads past h read as zeros.  The part's first segment starts from an empty
+// pipeline, and its P staging tiles are still free: latent columns 0..255 land
+// there while the RoPE columns and columns 256..511 take two ring entries, so
+// all of Q is in flight at once and the first K page follows the small RoPE box.
 template <typename T>
-__device__ void score_producer(const FwdArgs &a, const CUtensorMap *map, const CUtensorMap *qmap,
+__device__ void score_producer(const FwdArgs &a, const CUtensorMap *kmap, const CUtensorMap *qmap,
                                const CUtensorMap *pemap, const CUtensorMap *qpemap,
                                uint8_t *smem, const Ctx &c, int part, int head0) {
   Bars *b = c.bars;
-  uint32_t kc = 0, segn = 0;
+  uint32_t kc = 0;      // ring entries filled so far
+  bool first_seg = true;  // the part's first (non-empty) segment
   const bool leader = elect_one();
   SbWalk w(a, part);
   SbJob cur{}, nxt{};
   bool hc = false, hn = false;
+  // the next ring entry, once the MMAs of its previous use are done with it
+  auto next_entry = [&](uint32_t &slot) -> bool {
+    slot = kc % kNK;
+    const uint32_t use = kc / kNK;
+    ++kc;
+    return use == 0 || wait_bar<false>(c, &b->k_empty[slot], (use - 1) & 1, W_K_EMPTY);
+  };
   auto run = [&](SbJob &j) -> bool {
     if (j.first) {
-      for (int i = 0; i < 4; ++i, ++kc) {  // latent Q: 4 chunks of 128 columns
-        const uint32_t slot = kc % kNK, use = kc / kNK;
-        if (use > 0 && !wait_bar<false>(c, &b->k_empty[slot], (use - 1) & 1, W_K_EMPTY)) return false;
+      // ring uses: first segment: RoPE box, latent 256..511 (latent 0..255 go to the
+      // staging tiles); later segments: latent 0..255, latent 256..511, RoPE box
+      if (first_seg && leader) {
+        mbar_arrive_expect_tx(&b->qs_full, 4 * kQBox);
+#pragma unroll
+        for (int bx = 0; bx < 4; ++bx)
+          tma_load_3d(smem + kOffPStage + bx * kQBox, qmap, &b->qs_full, 64 * bx, head0, j.seq);
+      }
+      for (int i = first_seg ? 1 : 0; i < 3; ++i) {
+        const int what = first_seg ? (i == 1 ? 2 : 1) : i;  // 0, 1: latent halves; 2: RoPE
+        uint32_t slot;
+        if (!next_entry(slot)) return false;
         if (leader) {
-          mbar_arrive_expect_tx(&b->k_full[slot], 2 * kAtom);
-          uint8_t *dst = smem + kOffK + slot * kKSlot;
-          tma_load_3d(dst, qmap, &b->k_full[slot], 128 * i, head0, j.seq);
-          tma_load_3d(dst + kAtom, qmap, &b->k_full[slot], 128 * i + 64, head0, j.seq);
+          uint8_t *dst = smem + kOffK + slot * kKPage;
+          if (what < 2) {
+            mbar_arrive_expect_tx(&b->k_full[slot], 4 * kQBox);
+#pragma unroll
+            for (int bx = 0; bx < 4; ++bx)
+              tma_load_3d(dst + bx * kQBox, qmap, &b->k_full[slot], 64 * (4 * what + bx), head0, j.seq);
+          } else {
+            mbar_arrive_expect_tx(&b->k_full[slot], kQBox);
+            tma_load_3d(dst, qpemap, &b->k_full[slot], 0, head0, j.seq);
+          }
         }
       }
-      if (segn > 0 && !wait_bar<false>(c, &b->q_free, (segn - 1) & 1, W_Q_FREE)) return false;
-      if (leader) {
-        mbar_arrive_expect_tx(&b->q8_full, kAtom);
-        tma_load_3d(smem + kOffQ8, qpemap, &b->q8_full, 0, head0, j.seq);
-      }
-      ++segn;
+      first_seg = false;
     }
     finish_sb_pages(a, j.seq, j.np, j.pg);
-    for (int ch = 0; ch < kKChunks; ++ch, ++kc) {
-      const uint32_t slot = kc % kNK, use = kc / kNK;
-      if (use > 0 && !wait_bar<false>(c, &b->k_empty[slot], (use - 1) & 1, W_K_EMPTY)) return false;
-      if (leader) {
-        const int atoms = ch < 4 ? 2 : 1;
-        const CUtensorMap *m = ch < 4 ? map : pemap;
-        const int x0 = ch < 4 ? 128 * ch : 0;
-        mbar_arrive_expect_tx(&b->k_full[slot], atoms * j.np * kChunk);
-        uint8_t *dst = smem + kOffK + slot * kKSlot;
-        for (int at = 0; at < atoms; ++at)
 #pragma unroll
-          for (int p = 0; p < kSB; ++p)
-            if (p < j.np)
-              tma_load_3d(dst + at * kAtom + p * kChunk, m, &b->k_full[slot], x0 + 64 * at,
-                          j.pg.row0[p], j.pg.page[p]);
+    for (int p = 0; p < kSB; ++p) {
+      if (p >= j.np) break;
+      uint32_t slot;
+      if (!next_entry(slot)) return false;
+      if (leader) {
+        mbar_arrive_expect_tx(&b->k_full[slot], kKPage);
+        uint8_t *dst = smem + kOffK + slot * kKPage;
+        tma_load_4d(dst, kmap, &b->k_full[slot], 0, j.pg.row0[p], 0, j.pg.page[p]);
+        if (!a.k_fused)
+          tma_load_3d(dst + 8 * kChunk, pemap, &b->k_full[slot], 0, j.pg.row0[p], j.pg.page[p]);
       }
     }
     return true;
@@ -401,84 +428,98 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *map, const C
   }
 }
 
-// With N = 128 one MMA takes 64 tensor-core cycles, and the next must be issued
-// within that time.  So the whole warp runs the loop, which keeps its
-// counters and descriptors warp-uniform, and one elected lane issues the MMAs and
-// commits (the chunk loop stays rolled: unrolled, its code crowds the softmax
-// loop out of the instruction cache); the loop only advances slot / phase counters and adds offsets to
-// precomputed descriptors.  No warp-collective call sits in the loop: a lane that
-// leaves on a failed wait cannot block the others.
+// Per page, 36 MMAs of M=128 x N=64 x K=16 with A (Q) from TMEM: 32 over the
+// latent atoms, 4 over the RoPE atom, into one of the three page accumulators.
+// That is a budget of 32 tensor-core cycles per MMA, so the whole warp runs the
+// loop, which keeps its counters and descriptors warp-uniform, one elected lane
+// issues the MMAs and commits, and the unrolled page body only adds immediate
+// offsets to precomputed descriptors.  No warp-collective call sits in the loop:
+// a lane that leaves on a failed wait cannot block the others.
 template <typename T>
 __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int part, uint32_t tmem) {
   Bars *b = c.bars;
   const uint32_t tQ = tmem;
-  const uint32_t idesc = idesc_f16(128, kSBTok, Pack<T>::kBf16, false, false);
-  const uint64_t qdesc = desc_kmajor_sw128(smem_u32(smem + kOffQ8));
-  static_assert(kOffQ8 % 1024 == 0 && kOffK % 1024 == 0 && kAtom % 1024 == 0, "swizzle atoms");
+  const uint32_t idesc = idesc_f16(128, 64, Pack<T>::kBf16, false, false);
+  static_assert(kOffK % 1024 == 0 && kKPage % 1024 == 0, "swizzle atoms");
   const uint64_t kdesc = desc_kmajor_sw128(smem_u32(smem + kOffK));
   const uint32_t kfull = smem_u32(&b->k_full[0]), kempty = smem_u32(&b->k_empty[0]);
-  uint32_t slot = 0, phase = 0;  // K ring position of the next chunk and its k_full parity
-  uint32_t sb = 0, segn = 0;
+  uint32_t slot = 0, phase = 0;  // ring position of the next entry and its k_full parity
+  uint32_t pgc = 0, segn = 0;    // pages issued (S page buffer pgc % kSBufs), segments
   const bool leader = elect_one();
+  auto advance = [&]() {
+    if (++slot == kNK) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  };
   SegWalk walk(a, part);
   Seg s;
   while (walk.next(a, s)) {
     if (s.hi <= s.lo) continue;
     // this segment's Q: the previous segment's MMAs must be done reading it, then
-    // the eight latent boxes go from the K ring into TMEM (32 bytes of each row
-    // per copy) and the RoPE tile must have landed in Q8
+    // the eight latent boxes and the RoPE box go from the ring into TMEM (32 bytes
+    // of each row per copy)
     if (segn > 0) {
       if (!wait_bar<false>(c, &b->q_free, (segn - 1) & 1, W_Q_FREE)) return;
       tc_fence_after();
     }
+    // the order the producer filled them in (see score_producer)
 #pragma unroll 1
-    for (int i = 0; i < 4; ++i) {
-      if (!wait_addr<false>(c, kfull + 8 * slot, phase, W_K_FULL)) return;
-      tc_fence_after();
-      const uint64_t bd = kdesc + (uint64_t)(slot * (kKSlot >> 4));
-      if (leader) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          tmem_cp_128x256b(tQ + 64 * i + 8 * k, bd + (uint64_t)((k >> 2) * (kAtom >> 4) + 2 * (k & 3)));
-        mma_commit_addr(kempty + 8 * slot);
-      }
-      if (++slot == kNK) {
-        slot = 0;
-        phase ^= 1u;
-      }
-    }
-    if (!wait_bar<false>(c, &b->q8_full, segn & 1, W_Q8_FULL)) return;
-    tc_fence_after();
-    for (int sb0 = s.lo; sb0 < s.hi; sb0 += kSB, ++sb) {
-      const uint32_t buf = sb & 1;
-      if (sb >= 2) {  // the softmax has read this buffer's previous superblock
-        if (!wait_bar<false>(c, &b->s_free[buf], ((sb >> 1) - 1) & 1, W_S_FREE)) return;
+    for (int i = 0; i < 3; ++i) {
+      // 0, 1: latent columns 0..255 / 256..511 from the ring, 2: RoPE columns from
+      // the ring, 3: latent columns 0..255 from the staging tiles
+      const int what = segn == 0 ? (i == 0 ? 2 : (i == 1 ? 3 : 1)) : i;
+      uint64_t bd;
+      if (what == 3) {  // latent 0..255 in the staging tiles (first segment)
+        if (!wait_bar<false>(c, &b->qs_full, 0, W_K_FULL)) return;
         tc_fence_after();
-      }
-      const uint32_t tS = tmem + 256 + kSBTok * buf;
-#pragma unroll 1
-      for (int ch = 0; ch < kKChunks; ++ch) {
+        bd = desc_kmajor_sw128(smem_u32(smem + kOffPStage));
+      } else {
         if (!wait_addr<false>(c, kfull + 8 * slot, phase, W_K_FULL)) return;
         tc_fence_after();
-        const uint64_t bd = kdesc + (uint64_t)(slot * (kKSlot >> 4));
-        if (leader) {
-          if (ch < 4) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mma_ts(tS, tQ + 64 * ch + 8 * k, bd + (uint64_t)((k >> 2) * (kAtom >> 4) + 2 * (k & 3)), idesc,
-                     (ch | k) != 0);
-          } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mma_ss(tS, qdesc + 2 * k, bd + 2 * k, idesc, 1);
-          }
-          mma_commit_addr(kempty + 8 * slot);
-        }
-        if (++slot == kNK) {
-          slot = 0;
-          phase ^= 1u;
-        }
+        bd = kdesc + (uint64_t)(slot * (kKPage >> 4));
       }
-      if (leader) mma_commit(&b->s_full[buf]);
+      if (leader) {
+        if (what != 2) {
+          const uint32_t t0 = tQ + (what == 1 ? 128 : 0);
+#pragma unroll
+          for (int bx = 0; bx < 4; ++bx)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tmem_cp_128x256b(t0 + 32 * bx + 8 * k, bd + (uint64_t)(bx * (kQBox >> 4) + 2 * k));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tmem_cp_128x256b(tQ + kTQpe + 8 * k, bd + (uint64_t)(2 * k));
+        }
+        if (what != 3) mma_commit_addr(kempty + 8 * slot);
+      }
+      if (what != 3) advance();
+    }
+#pragma unroll 1
+    for (int pg = s.lo; pg < s.hi; ++pg, ++pgc) {
+      const uint32_t sbuf = pgc % kSBufs, use = pgc / kSBufs;
+      if (use > 0) {  // the softmax has read this buffer's previous page
+        if (!wait_bar<false>(c, &b->s_free[sbuf], (use - 1) & 1, W_S_FREE)) return;
+        tc_fence_after();
+      }
+      const uint32_t tS = tmem + kTS0 + 64 * sbuf;
+      if (!wait_addr<false>(c, kfull + 8 * slot, phase, W_K_FULL)) return;
+      tc_fence_after();
+      const uint64_t bd = kdesc + (uint64_t)(slot * (kKPage >> 4));
+      if (leader) {
+#pragma unroll
+        for (int blk = 0; blk < 8; ++blk)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tS, tQ + 32 * blk + 8 * k, bd + (uint64_t)(blk * (kChunk >> 4) + 2 * k), idesc,
+                   (blk | k) != 0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ts(tS, tQ + kTQpe + 8 * k, bd + (uint64_t)(8 * (kChunk >> 4) + 2 * k), idesc, 1);
+        mma_commit_addr(kempty + 8 * slot);
+        mma_commit(&b->s_full[sbuf]);
+      }
+      advance();
     }
     if (leader) mma_commit(&b->q_free);
     ++segn;
@@ -493,7 +534,7 @@ __device__ void score_copier(const FwdArgs &a, uint8_t *smem, const Ctx &c, int 
   const uint32_t peer_hdr = map_to_rank(smem_u32(smem + kOffHdr), 1);
   const uint32_t peer_pfull = map_to_rank(smem_u32(&b->p_full[0]), 1);
   const uint32_t peer_hfull = map_to_rank(smem_u32(&b->hdr_full[0]), 1);
-  uint32_t pc = 0;  // P tiles shipped so far (ring slot pc % kNPR)
+  uint32_t pc = 0;  // P tiles shipped so far (staging tile pc % kStageTiles, ring slot pc % kNPR)
   uint32_t sb = 0;
   const bool leader = elect_one();
   SbWalk w(a, part);
@@ -510,7 +551,7 @@ __device__ void score_copier(const FwdArgs &a, uint8_t *smem, const Ctx &c, int 
       const uint32_t r = pc % kNPR, use = pc / kNPR;
       if (use > 0 && !wait_bar<true>(c, &b->slot_free[r], (use - 1) & 1, W_SLOT_FREE)) return;
       if (leader)
-        bulk_copy_to_peer(peer_pring + r * kPTile, smem + kOffPStage + (buf * kSB + t) * kPTile,
+        bulk_copy_to_peer(peer_pring + r * kPTile, smem + kOffPStage + (pc % kStageTiles) * kPTile,
                           kPTile, peer_pfull + r * 8);
     }
     w.advance(a);
@@ -533,13 +574,14 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
   // sees q_len - 1 - qi fewer cached tokens than the sequence holds
   const int hidden = (a.causal && head_ok) ? a.q_len - 1 - head / a.heads : 0;
   const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
-  const uint32_t tS = tmem + 256 + lane_off + 64 * half;
   float *red_max = reinterpret_cast<float *>(smem + kOffRed);  // [2][128]
   float *red_sum = red_max + 256;                               // [2][128] fp32 weights
   float *red_sumr = red_max + 512;                              // [2][128] 16-bit weights
   const float scale = a.scale_log2;
   uint32_t sb = 0;
-  TileUse tu;  // staging tile buf * kSB + t
+  uint32_t pgs = 0;  // pages read so far: page p of a superblock is in S buffer (pgs + p) % kSBufs
+  uint32_t pt = 0;   // P tiles written so far: page p of a superblock uses staging tile (pt + p) % 4
+  TileUse tu;        // per staging tile
   SegWalk walk(a, part);
   Seg s;
   while (walk.next(a, s)) {
@@ -560,15 +602,26 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       const int sb0 = s.lo + j * kSB;
       const int np = min(kSB, s.hi - sb0);
       const bool last = j == nsb - 1;
-      const uint32_t buf = sb & 1;
-      bool ok = wait_bar<false>(c, &b->s_full[buf], (sb >> 1) & 1, W_S_FULL);
-      tc_fence_after();
+      const uint32_t buf = sb & 1;  // header / staging-stage parity
+      bool ok = true;
       uint32_t v[2][32];
-      tmem_ld32(tS + kSBTok * buf, v[0]);
-      tmem_ld32(tS + kSBTok * buf + 32, v[1]);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&b->s_free[buf]);
+      if (half < np) {  // my page's scores (a half without a page sees only -inf)
+        const uint32_t pb = (pgs + half) % kSBufs;
+        ok = wait_bar<false>(c, &b->s_full[pb], ((pgs + half) / kSBufs) & 1, W_S_FULL);
+        tc_fence_after();
+        const uint32_t tS = tmem + lane_off + kTS0 + 64 * pb;
+        tmem_ld32(tS, v[0]);
+        tmem_ld32(tS + 32, v[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&b->s_free[pb]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[i][e] = 0u;
+      }
+      pgs += np;
 
       // base-2 units; tokens this row does not see (a suffix of my page, all of it
       // when it starts past the row's end) and a page past the segment end (all of
@@ -598,12 +651,12 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       if (bar_red_or(1, 256, !ok || c.aborted())) return;  // all softmax threads leave together
       const float m_blk = fmaxf(red_max[r], red_max[128 + r]);
       float alpha = 1.f;
-      if (m_blk > m_ref) {  // also the first block (m_ref = -inf)
+      if (m_blk > m_ref + kTau) {  // also the first block (m_ref = -inf)
         alpha = fast_exp2(m_ref - m_blk);
         m_ref = m_blk;
       }
       // my staging tile must have left for the value CTA
-      const int tb = buf * kSB + half;
+      const int tb = (int)((pt + half) % kStageTiles);
       if (ok && half < np && tu.was_used(tb))
         ok = wait_bar<true>(c, &b->stage_free[tb], tu.parity(tb) ^ 1u, W_STAGE_FREE);
       float ps[8], pr[4];
@@ -656,7 +709,10 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       if (sw == 0 && lane == 0) hdr->flags = last ? 2u : 0u;
       fence_proxy_async_smem();
       mbar_arrive(&b->stage_ready[buf]);  // the copier ships the tiles and the header
-      tu.advance(buf * kSB, np);
+#pragma unroll
+      for (int t = 0; t < kSB; ++t)
+        if (t < np) tu.advance((int)((pt + t) % kStageTiles), 1);
+      pt += np;
     }
   }
 }
@@ -665,8 +721,8 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
 
 // V producer.  A V tile is one page's 256 value columns of one O half: four
 // swizzled [64 rows x 64 columns] atoms, 8 KB apart.  The 4-D map (columns split
-// into 64-wide blocks) lands all four in one TMA request; per request the SM's
-// TMA unit moves ~84 GB/s with 32 KB boxes, against 36-55 GB/s with 8 KB ones.
+// into 64-wide blocks) lands all four in one TMA request.  The rows were fetched
+// by the score CTA's K stream just before, so they come from L2.
 template <typename T>
 __device__ void value_producer(const FwdArgs &a, const CUtensorMap *map4, uint8_t *smem,
                                const Ctx &c, int part) {
@@ -676,6 +732,7 @@ __device__ void value_producer(const FwdArgs &a, const CUtensorMap *map4, uint8_
   SbWalk w(a, part);
   SbJob cur{}, nxt{};
   bool hc = false, hn = false;
+
   // the MMA warp's order: all pages' O-half-0 columns, then all pages' half-1 columns
   auto run = [&](SbJob &j) -> bool {
     finish_sb_pages(a, j.seq, j.np, j.pg);
@@ -794,7 +851,7 @@ __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
 // has landed, so it can reuse the staging tile.
 __device__ void value_receiver(const FwdArgs &a, const Ctx &c, int part) {
   Bars *b = c.bars;
-  uint32_t pc = 0, sb = 0;
+  uint32_t pc = 0;  // P tiles received so far
   const bool leader = elect_one();
   SbWalk w(a, part);
   while (w.more) {
@@ -803,10 +860,9 @@ __device__ void value_receiver(const FwdArgs &a, const Ctx &c, int part) {
       const uint32_t r = pc % kNPR;
       if (leader) mbar_arrive_expect_tx(&b->p_full[r], kPTile);
       if (!wait_bar<true>(c, &b->p_full[r], (pc / kNPR) & 1, W_P_FULL)) return;
-      if (leader) mbar_arrive_cluster(&b->stage_free[(sb & 1) * kSB + t], 0);
+      if (leader) mbar_arrive_cluster(&b->stage_free[pc % kStageTiles], 0);
     }
     w.advance(a);
-    ++sb;
   }
 }
 
@@ -977,7 +1033,7 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
-split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
+split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap q_map,
                 const __grid_constant__ CUtensorMap kpe_map,
                 const __grid_constant__ CUtensorMap qpe_map,
                 const __grid_constant__ CUtensorMap kv4_map, const FwdArgs a) {
@@ -996,8 +1052,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
       mbar_init(&b->k_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&b->s_full[i], 1);
-      mbar_init(&b->s_free[i], 256);
+
       mbar_init(&b->hdr_free[i], 2);
       mbar_init(&b->hdr_full[i], 1);
       for (int k = 0; k < 2; ++k) {
@@ -1006,9 +1061,13 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
       }
     }
     mbar_init(&b->q_free, 1);
-    mbar_init(&b->q8_full, 1);
-    for (int i = 0; i < kStages; ++i) mbar_init(&b->stage_ready[i], 256);
-    for (int i = 0; i < kStages * kSB; ++i) mbar_init(&b->stage_free[i], 1);
+    mbar_init(&b->qs_full, 1);
+    for (int i = 0; i < kSBufs; ++i) {
+      mbar_init(&b->s_full[i], 1);
+      mbar_init(&b->s_free[i], 128);  // the four warps of the half that reads the page
+    }
+    for (int i = 0; i < 2; ++i) mbar_init(&b->stage_ready[i], 256);
+    for (int i = 0; i < kStageTiles; ++i) mbar_init(&b->stage_free[i], 1);
     for (int i = 0; i < kNPR; ++i) {
       mbar_init(&b->slot_free[i], 1);
       mbar_init(&b->p_full[i], 1);
@@ -1022,7 +1081,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&kv_map);
+    tma_prefetch_desc(&k_map);
     tma_prefetch_desc(&q_map);
     tma_prefetch_desc(&kpe_map);
     tma_prefetch_desc(&qpe_map);
@@ -1053,7 +1112,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constan
     // a whole warp (a diverged spin loop would starve the other lanes' path, and
     // warp-uniform issue loops let one elected lane issue at full rate).
     if (warp == 0) {
-      if (loads) score_producer<T>(a, &kv_map, &q_map, &kpe_map, &qpe_map, smem, c, part, head0);
+      if (loads) score_producer<T>(a, &k_map, &q_map, &kpe_map, &qpe_map, smem, c, part, head0);
     } else if (warp == 1) {
       score_mma<T>(a, smem, loads ? c : Ctx{b, a.err, kForcedWaitNs}, part, tmem);
     } else if (warp < 10) {
@@ -1144,15 +1203,36 @@ cudaError_t smem_attr() {
   return e;
 }
 
+// A 4-D tiled map over the cache's rows as [pages][64-column blocks][page rows]
+// [64 columns] (block stride 128 B, so a box of several blocks lands as that many
+// swizzled [64 rows x 64 columns] atoms back to back).
+template <typename T>
+cudaError_t make_block_map(CUtensorMap *m, const void *base, uint64_t blocks, uint32_t box_blocks,
+                           const FwdArgs &a) {
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[4] = {64, (cuuint64_t)a.page_size, blocks, (cuuint64_t)a.num_pages};
+  cuuint64_t strides[3] = {(cuuint64_t)a.kv_row_stride * 2, 128, (cuuint64_t)a.kv_page_stride * 2};
+  cuuint32_t box[4] = {64, 64, box_blocks, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, Pack<T>::kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   4, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <typename T>
 cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
   constexpr uint64_t kLatent = MLA_HEAD_DIM_V, kRope = MLA_HEAD_DIM - MLA_HEAD_DIM_V;
-  // KV latent columns (also the value) and K_pe as [pages][page rows][cols], boxes
-  // of 64 rows x 64 columns; Q and Q_pe as [b][h][cols], boxes of 128 heads x 64
-  // columns (rows past h read as zeros)
-  CUtensorMap map, qmap, pemap, qpemap;
-  cudaError_t e = make_map<T>(&map, a.kv, kLatent, a.page_size, a.num_pages, a.kv_row_stride,
-                              a.kv_page_stride, 64);
+  // K: one box per page over all nine 64-column blocks of a 576-column row, or,
+  // with K_pe separate, the eight latent blocks plus a [64 rows x 64] K_pe box.
+  // V: the latent blocks again, four per box (one O half of one page).
+  // Q and Q_pe as [b][h][cols], boxes of 128 heads x 64 columns (rows past h read
+  // as zeros).
+  CUtensorMap kmap, qmap, pemap, qpemap, map4;
+  cudaError_t e = make_block_map<T>(&kmap, a.kv, a.k_fused ? 9 : 8, a.k_fused ? 9 : 8, a);
+  if (e == cudaSuccess) e = make_block_map<T>(&map4, a.kv, kLatent / 64, 4, a);
   if (e == cudaSuccess)
     e = make_map<T>(&pemap, a.k_pe, kRope, a.page_size, a.num_pages, a.k_pe_row_stride,
                     a.k_pe_page_stride, 64);
@@ -1161,21 +1241,6 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
   if (e == cudaSuccess)
     e = make_map<T>(&qpemap, a.q_pe, kRope, a.h, a.b, a.q_pe_head_stride, a.q_pe_batch_stride, 128);
   if (e != cudaSuccess) return e;
-  // the latent columns again as [pages][8 column blocks][page rows][64 columns]
-  // (block stride 128 B): a {64, 64, 4, 1} box is one V tile, four atoms in a row
-  CUtensorMap map4;
-  {
-    auto enc = encode_fn();
-    cuuint64_t dims[4] = {64, (cuuint64_t)a.page_size, kLatent / 64, (cuuint64_t)a.num_pages};
-    cuuint64_t strides[3] = {(cuuint64_t)a.kv_row_stride * 2, 128, (cuuint64_t)a.kv_page_stride * 2};
-    cuuint32_t box[4] = {64, 64, 4, 1};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    CUresult r = enc(&map4, Pack<T>::kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                     4, const_cast<void *>(a.kv), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  }
   if ((e = smem_attr<T>()) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * a.num_parts, (a.h + 127) / 128, 1);
@@ -1191,7 +1256,7 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, split_tc_kernel<T>, map, qmap, pemap, qpemap, map4, a);
+  return cudaLaunchKernelEx(&cfg, split_tc_kernel<T>, kmap, qmap, pemap, qpemap, map4, a);
 }
 
 }  // namespace

@@ -29,6 +29,19 @@ segment per part that touches it; segments are numbered globally in
 Outputs (the layout the C ABI documents):
   metadata[k] = [begin_seq, begin_blk, end_seq, end_blk, first_split, 0, 0, 0]
   num_splits  = prefix sums, num_splits[i+1] - num_splits[i] = segments of i
+
+How many parts
+--------------
+A segment costs far more than the F of the cost axis suggests once it is run
+(loading the query, filling and draining the pipeline, writing its output), so
+cutting a sequence into more segments can lose more than the extra parts gain.
+`schedule_auto` therefore tries a few part counts, charges each part G per
+segment plus one per block, and keeps the count whose most expensive part is
+cheapest (the larger count on a tie).  The counts tried are P_max and, from
+P_max - 1 down to ceil(P_max / 2), the first seven that divide b or are a
+multiple of it: on a batch of equal sequences those are the counts whose cuts
+fall on sequence boundaries or split every sequence alike.  Parts P..P_max-1
+are left empty: [b, 0, b, 0, num_splits[b], 0, 0, 0].
 """
 
 BLOCK_N = 64
@@ -79,6 +92,50 @@ def schedule(seqlens, num_parts, fixed_cost):
             first = num_splits[b]
         meta.append([bi, bb, ei, eb, first, 0, 0, 0])
     return meta, num_splits
+
+
+def part_costs(meta, seqlens, segment_cost):
+    """Cost of each part: `segment_cost` per segment it holds plus one per block."""
+    return [sum(segment_cost + (hi - lo) for (_, lo, hi, _) in segments_of_part(row, seqlens))
+            for row in meta]
+
+
+MAX_CANDIDATES = 8
+
+
+def candidate_parts(b, max_parts):
+    """max_parts, then the first MAX_CANDIDATES - 1 counts below it, down to
+    ceil(max_parts / 2), that divide b or are a multiple of b (descending)."""
+    out = [max_parts]
+    for p in range(max_parts - 1, (max_parts + 1) // 2 - 1, -1):
+        if len(out) == MAX_CANDIDATES:
+            break
+        if b % p == 0 or p % b == 0:
+            out.append(p)
+    return out
+
+
+def choose_parts(seqlens, max_parts, fixed_cost, segment_cost):
+    """Among candidate_parts(), the count whose partition has the cheapest most
+    expensive part; ties go to the larger count."""
+    best, best_p = None, max_parts
+    for p in candidate_parts(len(seqlens), max_parts):
+        meta, _ = schedule(seqlens, p, fixed_cost)
+        t = max(part_costs(meta, seqlens, segment_cost))
+        if best is None or t < best:
+            best, best_p = t, p
+    return best_p
+
+
+def schedule_auto(seqlens, max_parts, fixed_cost, segment_cost):
+    """schedule() with the part count chosen by choose_parts(); the metadata has
+    max_parts rows, the ones past the chosen count empty.  Returns (metadata rows,
+    num_splits prefix list, parts used)."""
+    b = len(seqlens)
+    p = choose_parts(seqlens, max_parts, fixed_cost, segment_cost)
+    meta, num_splits = schedule(seqlens, p, fixed_cost)
+    meta = meta + [[b, 0, b, 0, num_splits[b], 0, 0, 0] for _ in range(max_parts - p)]
+    return meta, num_splits, p
 
 
 def segments_of_part(meta_row, seqlens):

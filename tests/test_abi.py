@@ -66,6 +66,10 @@ def test_metadata_shape(lib):
         m.mla_metadata_shape(0, 128, 152)
     with pytest.raises(m.MlaError):
         m.mla_metadata_shape(4, 0, 152)
+    # the scheduler evaluates at most 512 part counts: num_sm is bounded
+    assert m.mla_metadata_shape(4, 128, m.MAX_NUM_SM) == (m.MAX_NUM_SM // 2, 8)
+    with pytest.raises(m.MlaError):
+        m.mla_metadata_shape(4, 128, m.MAX_NUM_SM + 1)
 
 
 def test_workspace_size(lib):

@@ -70,7 +70,8 @@ def test_metadata_bit_exact(seed):
     h = int(rng.choice([1, 16, 128, 200]))
     meta, ns = mla.mla_get_metadata(torch.from_numpy(lens).cuda(), h, num_sm)
     parts, _ = mla.mla_metadata_shape(b, h, num_sm)
-    ref_meta, ref_ns = sch.schedule([int(x) for x in lens], parts, mla.SCHED_FIXED_COST)
+    ref_meta, ref_ns, _ = sch.schedule_auto([int(x) for x in lens], parts, mla.SCHED_FIXED_COST,
+                                            mla.SCHED_SEGMENT_COST)
     assert meta.cpu().tolist() == ref_meta
     assert ns.cpu().tolist() == ref_ns
 

@@ -90,3 +90,65 @@ def test_hand_example():
     meta, ns = sch.schedule([128, 0, 150], 3, 1)
     assert [m[:5] for m in meta] == [[0, 0, 0, 1, 0], [0, 1, 2, 0, 1], [2, 0, 3, 0, 3]]
     assert ns == [0, 2, 3, 4]
+
+
+# ---- choosing the part count ----------------------------------------------------------
+
+def test_part_costs_count_segments_and_blocks():
+    # two sequences of 3 and 2 blocks, cut inside the first: part 0 holds one
+    # segment of 2 blocks, part 1 two segments (1 + 2 blocks)
+    meta, _ = sch.schedule([192, 128], 2, 0)
+    assert [r[:4] for r in meta] == [[0, 0, 0, 2], [0, 2, 2, 0]]
+    assert sch.part_costs(meta, [192, 128], 10) == [10 + 2, 20 + 3]
+
+
+def test_candidate_parts():
+    assert sch.candidate_parts(64, 76) == [76, 64]
+    assert sch.candidate_parts(128, 76) == [76, 64]
+    assert sch.candidate_parts(20, 76) == [76, 60, 40]
+    assert sch.candidate_parts(1, 76) == [76, 75, 74, 73, 72, 71, 70, 69]
+    assert sch.candidate_parts(7, 1) == [1]
+    assert sch.candidate_parts(5, 10) == [10, 5]
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_choose_parts_is_the_cheapest_worst_part(seed):
+    """Brute force over the candidate counts: the chosen one has the smallest most
+    expensive part, and no larger candidate ties with it."""
+    rng = np.random.default_rng(1000 + seed)
+    b = int(rng.integers(1, 120))
+    lens = [int(x) for x in rng.integers(0, 9000, size=b)]
+    if seed % 3 == 0:
+        lens = [int(rng.integers(1, 9000))] * b       # equal sequences
+    max_parts = int(rng.integers(1, 90))
+    G = int(rng.choice([0, 4, 16, 40]))
+    p = sch.choose_parts(lens, max_parts, FIXED, G)
+    cands = sch.candidate_parts(b, max_parts)
+    assert p in cands and (max_parts + 1) // 2 <= p <= max_parts
+    worst = {q: max(sch.part_costs(sch.schedule(lens, q, FIXED)[0], lens, G)) for q in cands}
+    assert worst[p] == min(worst.values())
+    assert all(worst[q] > worst[p] for q in cands if q > p)
+
+
+def test_equal_sequences_get_one_part_each_when_segments_are_dear():
+    # 64 sequences of 64 blocks on up to 76 parts: 76 parts cut most sequences in
+    # two (two segments in most parts); 64 parts give each part one whole sequence
+    lens = [4096] * 64
+    assert sch.choose_parts(lens, 76, FIXED, 16) == 64
+    # with free segments the largest count wins
+    assert sch.choose_parts(lens, 76, FIXED, 0) == 76
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_schedule_auto_pads_with_empty_parts(seed):
+    rng = np.random.default_rng(2000 + seed)
+    b = int(rng.integers(1, 100))
+    lens = [int(x) for x in rng.integers(0, 20000, size=b)]
+    max_parts = int(rng.integers(2, 80))
+    meta, ns, p = sch.schedule_auto(lens, max_parts, FIXED, 16)
+    assert len(meta) == max_parts
+    ref_meta, ref_ns = check_partition(lens, p, FIXED)
+    assert meta[:p] == ref_meta and ns == ref_ns
+    for row in meta[p:]:
+        assert row == [b, 0, b, 0, ns[b], 0, 0, 0]
+        assert sch.segments_of_part(row, lens) == []
