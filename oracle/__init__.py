@@ -6,7 +6,8 @@ code with the CUDA path and imports nothing from it.
 
 `decode_rows` evaluates the plain definition in `mla_oracle.c` for chosen
 (sequence, head) pairs; `decode` evaluates every pair.  Inputs are numpy
-arrays holding the stored 16-bit patterns (fp16 or bf16) and int32 tables.
+arrays holding the stored 16-bit patterns (fp16 or bf16), or the stored e4m3
+bytes with one dequantisation scale each for q and the cache, and int32 tables.
 """
 import ctypes
 import os
@@ -27,7 +28,7 @@ _lib = None
 
 D = 576
 DV = 512
-DTYPES = {"fp16": 0, "bf16": 1}
+DTYPES = {"fp16": 0, "bf16": 1, "e4m3": 2}
 
 
 def build(src=_SRC, out=_LIB, extra_flags=()):
@@ -62,6 +63,13 @@ def load(path=_LIB):
             ctypes.c_void_p, ctypes.c_double, ctypes.c_int, ctypes.c_int,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_mla_decode_rows_qs.restype = ctypes.c_int
+        lib.oracle_mla_decode_rows_qs.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_double, ctypes.c_int, ctypes.c_double, ctypes.c_double,
+            ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_widen.restype = ctypes.c_double
         lib.oracle_widen.argtypes = [ctypes.c_uint16, ctypes.c_int]
         if path == _LIB:
@@ -74,11 +82,15 @@ def _ptr(a):
 
 
 def decode_rows(q, kv, block_table, cache_seqlens, softmax_scale, dtype, rows,
-                threads=1, lib=None, with_abs=False, seqlen_q=1, is_causal=False):
+                threads=1, lib=None, with_abs=False, seqlen_q=1, is_causal=False,
+                q_scale=1.0, kv_scale=1.0):
     """Evaluate the definition for the (seq, row) pairs in `rows`.
 
-    q            : uint16 [b, seqlen_q * h, 576]   (stored bits; row = qi * h + head)
-    kv           : uint16 [num_pages, page_size, 576]
+    q            : uint16 [b, seqlen_q * h, 576]   (stored bits; row = qi * h + head),
+                   or uint8 e4m3 bytes when dtype is "e4m3"
+    kv           : uint16 [num_pages, page_size, 576] (uint8 for "e4m3")
+    q_scale, kv_scale: dequantisation scales (e4m3 only; the values the definition
+                   uses are q_scale * q and kv_scale * kv)
     block_table  : int32  [b, max_blocks]
     cache_seqlens: int32  [b]
     rows         : int array [n, 2] of (seq, row)
@@ -89,8 +101,11 @@ def decode_rows(q, kv, block_table, cache_seqlens, softmax_scale, dtype, rows,
     each output sums, which bounds the error of any rounding of them.
     """
     lib = lib or load()
-    q = np.ascontiguousarray(q, dtype=np.uint16)
-    kv = np.ascontiguousarray(kv, dtype=np.uint16)
+    fp8 = dtype == "e4m3"
+    q = np.ascontiguousarray(q, dtype=np.uint8 if fp8 else np.uint16)
+    kv = np.ascontiguousarray(kv, dtype=np.uint8 if fp8 else np.uint16)
+    if not fp8:
+        assert q_scale == 1.0 and kv_scale == 1.0, "scales apply to e4m3 inputs only"
     bt = np.ascontiguousarray(block_table, dtype=np.int32)
     sl = np.ascontiguousarray(cache_seqlens, dtype=np.int32)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
@@ -115,6 +130,12 @@ def decode_rows(q, kv, block_table, cache_seqlens, softmax_scale, dtype, rows,
         ls = lse[lo:hi]
         ab = _ptr(absw[lo:hi]) if with_abs else None
         scratch = np.empty(max_len, dtype=np.float64)
+        if fp8:
+            return lib.oracle_mla_decode_rows_qs(
+                b, int(seqlen_q), h, int(bool(is_causal)), _ptr(q), _ptr(kv), num_pages,
+                page_size, _ptr(bt), bt.shape[1], _ptr(sl), float(softmax_scale), code,
+                float(q_scale), float(kv_scale), hi - lo, _ptr(rb), _ptr(rh), _ptr(o), _ptr(ls),
+                _ptr(scratch), ab)
         if seqlen_q == 1 and not is_causal:
             return lib.oracle_mla_decode_rows(
                 b, h, _ptr(q), _ptr(kv), num_pages, page_size, _ptr(bt), bt.shape[1],
@@ -139,13 +160,14 @@ def decode_rows(q, kv, block_table, cache_seqlens, softmax_scale, dtype, rows,
 
 
 def decode(q, kv, block_table, cache_seqlens, softmax_scale, dtype, threads=1, seqlen_q=1,
-           is_causal=False):
+           is_causal=False, q_scale=1.0, kv_scale=1.0):
     """Every (seq, row) pair; returns out [b, rows, 512] and lse [b, rows] (float64),
     rows = seqlen_q * h (token-major)."""
     b, h = q.shape[0], q.shape[1]
     rows = np.stack(np.meshgrid(np.arange(b), np.arange(h), indexing="ij"), -1).reshape(-1, 2)
     out, lse = decode_rows(q, kv, block_table, cache_seqlens, softmax_scale, dtype, rows,
-                           threads=threads, seqlen_q=seqlen_q, is_causal=is_causal)
+                           threads=threads, seqlen_q=seqlen_q, is_causal=is_causal,
+                           q_scale=q_scale, kv_scale=kv_scale)
     return out.reshape(b, h, DV), lse.reshape(b, h)
 
 
@@ -175,5 +197,5 @@ def compact_pages(kv_pages_fn, block_table, cache_seqlens, seqs, page_size):
     for r, s in enumerate(seqs):
         n = (int(sl[s]) + page_size - 1) // page_size
         table[r, :n] = [remap[int(p)] for p in bt[s, :n]]
-    kv = kv_pages_fn(uniq) if len(uniq) else np.zeros((0, page_size, D), np.uint16)
+    kv = kv_pages_fn(uniq) if len(uniq) else np.zeros((0, page_size, D), np.uint16)  # (any dtype)
     return kv, table, sl[seqs].astype(np.int32)

@@ -28,6 +28,9 @@
  *                       block_table[b][t / page_size], row t % page_size;
  *                       tokens at or beyond cache_seqlens[b] do not exist.
  *
+ *   [TL §变体内核]  an experimental variant keeps the KV cache in FP8
+ *                       (example_mla_decode_kv_fp8.py); no format is given.
+ *
  * Readings where the pages are silent:
  *   - lse is the natural-log log-sum-exp of the scaled scores,
  *     lse = m + ln(sum_t exp(s_t - m)), m = max_t s_t  (the FlashAttention
@@ -36,6 +39,11 @@
  *   - inputs are the bf16 / fp16 bit patterns exactly as stored; the oracle
  *     widens them to double and rounds nothing afterwards (the kernels round
  *     P to the input dtype; the parity tolerance absorbs that).
+ *   - FP8 cache: q and every cached row are stored as e4m3 (1 sign bit, 4
+ *     exponent bits with bias 7, 3 fraction bits, no infinities, S.1111.111 is
+ *     NaN), each tensor with one fp32 dequantisation scale: the values the
+ *     definition uses are q = q_scale * q8, k = kv_scale * k8 and
+ *     v = kv_scale * v8 (v the first 512 columns of the dequantised row).
  */
 #include <math.h>
 #include <stdint.h>
@@ -69,12 +77,39 @@ static double bf16_bits_to_double(uint16_t x) {
   return (double)f;
 }
 
-/* dtype: 0 = fp16, 1 = bf16 */
+/* e4m3 -> double, from the format's definition: 1 sign bit, 4 exponent bits
+ * with bias 7, 3 fraction bits; exponent 0 is subnormal, S.1111.111 is NaN and
+ * there are no infinities. */
+static double e4m3_bits_to_double(uint8_t x) {
+  int sign = (x >> 7) & 1;
+  int e = (x >> 3) & 0xf;
+  int f = x & 7;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)f, -9); /* subnormal: f * 2^-3 * 2^-6 */
+  } else if (e == 15 && f == 7) {
+    v = NAN;
+  } else {
+    v = ldexp((double)(f | 8), e - 10); /* (8+f) * 2^(e-7-3) */
+  }
+  return sign ? -v : v;
+}
+
+/* dtype: 0 = fp16, 1 = bf16, 2 = e4m3 */
 static double widen(uint16_t x, int dtype) {
+  if (dtype == 2) return e4m3_bits_to_double((uint8_t)x);
   return dtype == 1 ? bf16_bits_to_double(x) : half_bits_to_double(x);
 }
 
-/* Exported for the exhaustive conversion pin. */
+/* Element i of a stored array: 16-bit patterns (fp16, bf16) or bytes (e4m3). */
+static double elem(const void *base, int64_t i, int dtype) {
+  if (dtype == 2) return e4m3_bits_to_double(((const uint8_t *)base)[i]);
+  return widen(((const uint16_t *)base)[i], dtype);
+}
+
+static int elem_size(int dtype) { return dtype == 2 ? 1 : 2; }
+
+/* Exported for the exhaustive conversion pins. */
 double oracle_widen(uint16_t x, int dtype) { return widen(x, dtype); }
 
 /*
@@ -88,10 +123,10 @@ double oracle_widen(uint16_t x, int dtype) { return widen(x, dtype); }
  *   scores      : scratch, at least seqlen doubles
  * Returns 0, or -1 if the block table points outside the cache.
  */
-static int one_row(const uint16_t *q_row, const uint16_t *kv, int64_t num_pages,
+static int one_row(const void *q_row, const void *kv, int64_t num_pages,
                    int page_size, const int32_t *table_row, int seqlen,
-                   double softmax_scale, int dtype, double *out_row, double *abs_row,
-                   double *lse_out, double *scores) {
+                   double softmax_scale, int dtype, double q_scale, double kv_scale,
+                   double *out_row, double *abs_row, double *lse_out, double *scores) {
   for (int d = 0; d < MLA_DV; ++d) out_row[d] = 0.0;
   if (abs_row)
     for (int d = 0; d < MLA_DV; ++d) abs_row[d] = 0.0;
@@ -99,14 +134,16 @@ static int one_row(const uint16_t *q_row, const uint16_t *kv, int64_t num_pages,
     *lse_out = -INFINITY;
     return 0;
   }
-  /* s_t = scale * sum_c q[c] * k_t[c]  over all 576 columns */
+  /* s_t = scale * sum_c q[c] * k_t[c]  over all 576 columns, with the
+   * dequantised values q = q_scale * q_stored and k = kv_scale * k_stored */
   double m = -INFINITY;
   for (int t = 0; t < seqlen; ++t) {
     int32_t page = table_row[t / page_size];
     if (page < 0 || page >= num_pages) return -1;
-    const uint16_t *k = kv + ((int64_t)page * page_size + t % page_size) * MLA_D;
+    const int64_t k = ((int64_t)page * page_size + t % page_size) * MLA_D;
     double dot = 0.0;
-    for (int c = 0; c < MLA_D; ++c) dot += widen(q_row[c], dtype) * widen(k[c], dtype);
+    for (int c = 0; c < MLA_D; ++c)
+      dot += q_scale * elem(q_row, c, dtype) * (kv_scale * elem(kv, k + c, dtype));
     scores[t] = softmax_scale * dot;
     if (scores[t] > m) m = scores[t];
   }
@@ -115,11 +152,11 @@ static int one_row(const uint16_t *q_row, const uint16_t *kv, int64_t num_pages,
   for (int t = 0; t < seqlen; ++t) z += exp(scores[t] - m);
   for (int t = 0; t < seqlen; ++t) {
     int32_t page = table_row[t / page_size];
-    const uint16_t *v = kv + ((int64_t)page * page_size + t % page_size) * MLA_D;
+    const int64_t v = ((int64_t)page * page_size + t % page_size) * MLA_D;
     double p = exp(scores[t] - m) / z;
-    for (int d = 0; d < MLA_DV; ++d) out_row[d] += p * widen(v[d], dtype);
+    for (int d = 0; d < MLA_DV; ++d) out_row[d] += p * (kv_scale * elem(kv, v + d, dtype));
     if (abs_row)
-      for (int d = 0; d < MLA_DV; ++d) abs_row[d] += p * fabs(widen(v[d], dtype));
+      for (int d = 0; d < MLA_DV; ++d) abs_row[d] += p * fabs(kv_scale * elem(kv, v + d, dtype));
   }
   *lse_out = m + log(z);
   return 0;
@@ -145,12 +182,13 @@ static int one_row(const uint16_t *q_row, const uint16_t *kv, int64_t num_pages,
  *   scratch      : at least max(cache_seqlens) doubles
  * Returns 0 on success, -1 on an out-of-range page or row index.
  */
-int oracle_mla_decode_rows_q(int b, int seqlen_q, int h, int is_causal, const uint16_t *q,
-                             const uint16_t *kv, int64_t num_pages, int page_size,
-                             const int32_t *block_table, int max_blocks,
-                             const int32_t *cache_seqlens, double softmax_scale, int dtype,
-                             int n_rows, const int32_t *row_b, const int32_t *row_r,
-                             double *out, double *lse, double *scratch, double *absw) {
+int oracle_mla_decode_rows_qs(int b, int seqlen_q, int h, int is_causal, const void *q,
+                              const void *kv, int64_t num_pages, int page_size,
+                              const int32_t *block_table, int max_blocks,
+                              const int32_t *cache_seqlens, double softmax_scale, int dtype,
+                              double q_scale, double kv_scale, int n_rows,
+                              const int32_t *row_b, const int32_t *row_r, double *out,
+                              double *lse, double *scratch, double *absw) {
   if (seqlen_q < 1) return -1;
   const int rows_per_seq = seqlen_q * h;
   for (int r = 0; r < n_rows; ++r) {
@@ -161,13 +199,25 @@ int oracle_mla_decode_rows_q(int b, int seqlen_q, int h, int is_causal, const ui
     int qi = ri / h; /* query token of this row */
     int visible = is_causal ? L - (seqlen_q - 1 - qi) : L;
     if (visible < 0) visible = 0;
-    int rc = one_row(q + ((int64_t)bi * rows_per_seq + ri) * MLA_D, kv, num_pages, page_size,
-                     block_table + (int64_t)bi * max_blocks, visible, softmax_scale, dtype,
-                     out + (int64_t)r * MLA_DV, absw ? absw + (int64_t)r * MLA_DV : 0, lse + r,
-                     scratch);
+    const char *q_row = (const char *)q + ((int64_t)bi * rows_per_seq + ri) * MLA_D * elem_size(dtype);
+    int rc = one_row(q_row, kv, num_pages, page_size, block_table + (int64_t)bi * max_blocks,
+                     visible, softmax_scale, dtype, q_scale, kv_scale, out + (int64_t)r * MLA_DV,
+                     absw ? absw + (int64_t)r * MLA_DV : 0, lse + r, scratch);
     if (rc) return rc;
   }
   return 0;
+}
+
+/* 16-bit inputs (no dequantisation scales). */
+int oracle_mla_decode_rows_q(int b, int seqlen_q, int h, int is_causal, const uint16_t *q,
+                             const uint16_t *kv, int64_t num_pages, int page_size,
+                             const int32_t *block_table, int max_blocks,
+                             const int32_t *cache_seqlens, double softmax_scale, int dtype,
+                             int n_rows, const int32_t *row_b, const int32_t *row_r,
+                             double *out, double *lse, double *scratch, double *absw) {
+  return oracle_mla_decode_rows_qs(b, seqlen_q, h, is_causal, q, kv, num_pages, page_size,
+                                   block_table, max_blocks, cache_seqlens, softmax_scale, dtype,
+                                   1.0, 1.0, n_rows, row_b, row_r, out, lse, scratch, absw);
 }
 
 /* One query token per sequence: q is [b][h][576] and the rows are (sequence, head). */

@@ -374,10 +374,82 @@ def pin_query_tokens(lib):
     return True
 
 
+# ---- e4m3 cache with dequantisation scales
+
+def bits8(x):
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def vals8(b):
+    return torch.from_numpy(np.asarray(b, dtype=np.uint8)).view(torch.float8_e4m3fn).to(
+        torch.float64).numpy()
+
+
+def paged8(logical, page_size, rng, num_extra_pages=2):
+    """paged() for e4m3 bytes: finite garbage everywhere not overwritten."""
+    b = len(logical)
+    nblk = [(x.shape[0] + page_size - 1) // page_size for x in logical]
+    num_pages = sum(nblk) + num_extra_pages
+    perm = rng.permutation(num_pages)
+    kv = (rng.integers(0, 256, size=(num_pages, page_size, D)) & 0x77).astype(np.uint8)
+    table = np.full((b, max(1, max(nblk))), -1, dtype=np.int32)
+    k = 0
+    for i, x in enumerate(logical):
+        for j in range(nblk[i]):
+            page = int(perm[k]); k += 1
+            table[i, j] = page
+            rows = x[j * page_size:(j + 1) * page_size]
+            kv[page, : rows.shape[0]] = rows
+    return kv, table
+
+
+def pin_fp8_brute_force(lib):
+    """e4m3 storage with scales against the naive softmax over the dequantised logical
+    sequence (torch's e4m3 widening, an independent path)."""
+    rng = np.random.default_rng(21)
+    q_scale, kv_scale, scale = 0.37, 1.9, 0.05
+    for page_size, lens in ((64, (37, 130)), (128, (1, 200))):
+        h = 2
+        logical = [bits8(rng.standard_normal((L, D)) * 3) for L in lens]
+        q = bits8(rng.standard_normal((len(lens), h, D)) * 3)
+        kv, table = paged8(logical, page_size, rng)
+        rows = np.stack(np.meshgrid(np.arange(len(lens)), np.arange(h), indexing="ij"),
+                        -1).reshape(-1, 2)
+        out, lse = oracle.decode_rows(q, kv, table, np.asarray(lens, np.int32), scale, "e4m3",
+                                      rows, lib=lib, q_scale=q_scale, kv_scale=kv_scale)
+        out, lse = out.reshape(len(lens), h, DV), lse.reshape(len(lens), h)
+        for i in range(len(lens)):
+            lv = kv_scale * vals8(logical[i])
+            for j in range(h):
+                ref_o, ref_l = brute(q_scale * vals8(q[i, j]), lv, scale)
+                if not np.allclose(out[i, j], ref_o, rtol=1e-11, atol=1e-12):
+                    return False
+                if abs(lse[i, j] - ref_l) > 1e-11 * max(1.0, abs(ref_l)):
+                    return False
+    return True
+
+
+def pin_fp8_len_one(lib):
+    """One cached token: out is exactly kv_scale times its value columns, lse its score."""
+    rng = np.random.default_rng(22)
+    row = bits8(rng.standard_normal((1, D)) * 4)
+    q = bits8(rng.standard_normal((1, 1, D)) * 4)
+    kv, table = paged8([row], 64, rng)
+    out, lse = oracle.decode_rows(q, kv, table, np.asarray([1], np.int32), 0.1, "e4m3",
+                                  np.array([[0, 0]], np.int32), lib=lib, q_scale=0.5,
+                                  kv_scale=3.0)
+    v = vals8(row[0])
+    if not np.array_equal(out[0], 3.0 * v[:DV]):
+        return False
+    s0 = 0.1 * math.fsum(0.5 * vals8(q[0, 0]) * (3.0 * v))
+    return abs(lse[0] - s0) <= 1e-12 * max(1, abs(s0))
+
+
 PINS = [pin_brute_force, pin_len_one, pin_identical_scores, pin_zero_query, pin_two_tokens,
         pin_dominant_token, pin_empty_sequence, pin_page_permutation, pin_token_permutation,
         pin_head_independence, pin_softmax_shift, pin_split_combine, pin_batch_rows, pin_abs_weights,
-        pin_query_tokens]
+        pin_query_tokens, pin_fp8_brute_force, pin_fp8_len_one]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -403,6 +475,15 @@ def test_widen_bf16_exhaustive():
     assert same.all()
 
 
+def test_widen_e4m3_exhaustive():
+    lib = oracle.load()
+    allbits = np.arange(256, dtype=np.uint8)
+    ref = vals8(allbits)
+    got = np.array([lib.oracle_widen(int(x), 2) for x in allbits])
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all()
+
+
 def test_bad_table_is_an_error():
     rng = np.random.default_rng(3)
     rows = bits(rng.standard_normal((10, D)), "bf16")
@@ -416,10 +497,10 @@ def test_bad_table_is_an_error():
 # mutants: each plausible slip in the oracle must be caught by some pin
 
 MUTANTS = {
-    "drop_rope_term": ("for (int c = 0; c < MLA_D; ++c) dot +=",
-                       "for (int c = 0; c < MLA_DV; ++c) dot +="),
-    "v_wrong_columns": ("out_row[d] += p * widen(v[d], dtype)",
-                        "out_row[d] += p * widen(v[d + 64], dtype)"),
+    "drop_rope_term": ("for (int c = 0; c < MLA_D; ++c)\n      dot +=",
+                       "for (int c = 0; c < MLA_DV; ++c)\n      dot +="),
+    "v_wrong_columns": ("out_row[d] += p * (kv_scale * elem(kv, v + d, dtype))",
+                        "out_row[d] += p * (kv_scale * elem(kv, v + d + 64, dtype))"),
     "page_index_mod": ("int32_t page = table_row[t / page_size];\n    if (page < 0",
                        "int32_t page = table_row[t % page_size];\n    if (page < 0"),
     "row_in_page_div": ("(int64_t)page * page_size + t % page_size) * MLA_D;\n    double dot",
@@ -434,12 +515,20 @@ MUTANTS = {
                          "q + ((int64_t)ri * b + bi) * MLA_D"),
     "first_token_skipped": ("for (int t = 0; t < seqlen; ++t) z +=",
                             "for (int t = 1; t < seqlen; ++t) z +="),
-    "abs_sign_kept": ("abs_row[d] += p * fabs(widen(v[d], dtype));", "abs_row[d] += p * widen(v[d], dtype);"),
+    "abs_sign_kept": ("abs_row[d] += p * fabs(kv_scale * elem(kv, v + d, dtype));",
+                      "abs_row[d] += p * (kv_scale * elem(kv, v + d, dtype));"),
     "causal_off_by_one": ("L - (seqlen_q - 1 - qi) : L", "L - (seqlen_q - qi) : L"),
     "causal_ignored": ("is_causal ? L - (seqlen_q - 1 - qi) : L", "L"),
     "query_token_reversed": ("int qi = ri / h;", "int qi = seqlen_q - 1 - ri / h;"),
     "query_rows_head_major": ("int qi = ri / h;", "int qi = ri % seqlen_q;"),
-    "abs_unweighted": ("abs_row[d] += p * fabs(widen(v[d], dtype));", "abs_row[d] += fabs(widen(v[d], dtype));"),
+    "e4m3_bias": ("v = ldexp((double)(f | 8), e - 10);", "v = ldexp((double)(f | 8), e - 9);"),
+    "e4m3_subnormal": ("v = ldexp((double)f, -9); /* subnormal", "v = ldexp((double)f, -10); /* subnormal"),
+    "e4m3_nan_pattern": ("} else if (e == 15 && f == 7) {", "} else if (0) {"),
+    "kv_scale_dropped_in_v": ("out_row[d] += p * (kv_scale * elem(kv, v + d, dtype));",
+                              "out_row[d] += p * elem(kv, v + d, dtype);"),
+    "q_scale_dropped": ("dot += q_scale * elem(q_row, c, dtype)", "dot += elem(q_row, c, dtype)"),
+    "abs_unweighted": ("abs_row[d] += p * fabs(kv_scale * elem(kv, v + d, dtype));",
+                       "abs_row[d] += fabs(kv_scale * elem(kv, v + d, dtype));"),
 }
 
 
@@ -470,6 +559,11 @@ def test_mutant_is_caught(name):
             got = np.array([lib.oracle_widen(int(x), 0) for x in allbits])
             if not (((got == ref) | (np.isnan(got) & np.isnan(ref))).all()):
                 caught.append("widen_fp16")
+        allbits8 = np.arange(256, dtype=np.uint8)  # the exhaustive e4m3 widening check
+        got8 = np.array([lib.oracle_widen(int(x), 2) for x in allbits8])
+        ref8 = vals8(allbits8)
+        if not (((got8 == ref8) | (np.isnan(got8) & np.isnan(ref8))).all()):
+            caught.append("widen_e4m3")
         assert caught, f"mutant {name} survived every pin"
     finally:
         shutil.rmtree(tmp, ignore_errors=True)
