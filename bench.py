@@ -214,6 +214,11 @@ class ClockSampler:
                 "source": src}
 
 
+def input_scales(x):
+    """The dequantisation scales of an e4m3 workload's inputs (none for 16-bit ones)."""
+    return {k: x[k] for k in ("q_scale", "kv_scale") if k in x}
+
+
 def max_over_ranks(x, world, device):
     """The largest of every rank's `x` (the job's time is its slowest rank's)."""
     if world <= 1:
@@ -261,7 +266,7 @@ def oracle_sample_time(w, target_seconds, seqs_max=64):
         t0 = time.perf_counter()
         oracle.decode(q, kv, x["block_table"].numpy(), x["cache_seqlens"].numpy(),
                       w.softmax_scale, w.dtype, threads=cores, seqlen_q=sub.seqlen_q,
-                      is_causal=sub.causal)
+                      is_causal=sub.causal, **input_scales(x))
         elapsed += time.perf_counter() - t0
         flops += sub.flops()
         nseq += 1
@@ -295,7 +300,7 @@ def run_reference(args):
         t0 = time.perf_counter()
         oracle.decode(q, kv, x["block_table"].numpy(), x["cache_seqlens"].numpy(),
                       w.softmax_scale, w.dtype, threads=cores, seqlen_q=sub.seqlen_q,
-                      is_causal=sub.causal)
+                      is_causal=sub.causal, **input_scales(x))
         return time.perf_counter() - t0, sub.flops()
 
     t_probe, _ = one(min(L0, 512), 1)
@@ -350,7 +355,8 @@ def run_ours(args):
     sets = [base]
     for _ in range(max(0, args.copies - 1)):
         sets.append({"q": base["q"].clone(), "kv_cache": base["kv_cache"].clone(),
-                     "block_table": base["block_table"], "cache_seqlens": base["cache_seqlens"]})
+                     "block_table": base["block_table"], "cache_seqlens": base["cache_seqlens"],
+                     **input_scales(base)})
     sets = [as_layout(s, args.layout) for s in sets]
     base = sets[0]
     num_sm = mla.mla_device_num_sm(local)
@@ -359,12 +365,14 @@ def run_ours(args):
     nsplit = torch.empty((w.batch + 1,), dtype=torch.int32, device=dev)
     ws = torch.empty((mla.mla_workspace_size(w.batch, w.rows, parts),), dtype=torch.uint8,
                      device=dev)
-    out = torch.empty((w.batch, w.seqlen_q, w.heads, 512), dtype=w.torch_dtype, device=dev)
+    out = torch.empty((w.batch, w.seqlen_q, w.heads, 512), dtype=mla.out_dtype(w.torch_dtype),
+                      device=dev)
     lse = torch.empty((w.batch, w.heads) if w.seqlen_q == 1 else (w.batch, w.seqlen_q, w.heads),
                       dtype=torch.float32, device=dev)
     calls = [mla.prepare_decode(s["q"], s["kv_cache"], s["block_table"], s["cache_seqlens"],
                                 w.softmax_scale, meta, nsplit, out, lse, ws, q_pe=s["q_pe"],
-                                k_pe=s["k_pe"], is_causal=w.causal) for s in sets]
+                                k_pe=s["k_pe"], is_causal=w.causal, **input_scales(s))
+             for s in sets]
     metas = [mla.prepare_metadata(s["cache_seqlens"], w.heads, num_sm, meta, nsplit,
                                   seqlen_q=w.seqlen_q) for s in sets]
 
@@ -416,14 +424,14 @@ def run_ours(args):
     split_ms = max_over_ranks(split_ms, world, dev)
 
     # ---- end to end through the public API with pinned host buffers
-    host = {k: v.cpu().pin_memory() for k, v in base.items() if v is not None}
+    host = {k: v.cpu().pin_memory() for k, v in base.items() if torch.is_tensor(v)}
     dbuf = {k: torch.empty_like(base[k]) for k in host}
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     e2e_call = mla.prepare_decode(dbuf["q"], dbuf["kv_cache"], dbuf["block_table"],
                                   dbuf["cache_seqlens"], w.softmax_scale, meta, nsplit, out, lse,
                                   ws, q_pe=dbuf.get("q_pe"), k_pe=dbuf.get("k_pe"),
-                                  is_causal=w.causal)
+                                  is_causal=w.causal, **input_scales(base))
     e2e_meta = mla.prepare_metadata(dbuf["cache_seqlens"], w.heads, num_sm, meta, nsplit,
                                     seqlen_q=w.seqlen_q)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
@@ -459,16 +467,20 @@ def run_ours(args):
     achieved = nbytes / (split_ms * 1e-3) / 1e9
     traffic = ncu_traffic(w.name)
     # the bound is whichever of HBM bytes and tensor flops takes longer at the measured
-    # peaks (fp16 runs at bf16's nominal tensor rate); the kernel is timed alone in a
-    # ~100 us launch, so the burst tensor peak applies
+    # peaks (fp16 runs at bf16's nominal tensor rate, e4m3 at twice it: 4.5 vs 2.25
+    # PFLOP/s nominal); the kernel is timed alone in a ~100 us launch, so the burst
+    # tensor peak applies
+    f8 = w.dtype == "e4m3"
+    tensor_peak = bf16_peak * (2.0 if f8 else 1.0)
     tflops_achieved = flops / (split_ms * 1e-3) / 1e12
     roofline = {"kernel": "split", "kernel_ms": split_ms, "kernel_launches_timed": len(ev),
                 "traffic": traffic,
-                "hbm_frac": achieved / hbm_peak, "tensor_frac": tflops_achieved / bf16_peak}
-    if flops / (bf16_peak * 1e12) > nbytes / (hbm_peak * 1e9):
-        roofline.update(bound="tensor", achieved=tflops_achieved, peak=bf16_peak, unit="TFLOP/s",
-                        frac=tflops_achieved / bf16_peak,
-                        peak_source=f"{peak_src} bf16_tflops (burst)")
+                "hbm_frac": achieved / hbm_peak, "tensor_frac": tflops_achieved / tensor_peak}
+    if flops / (tensor_peak * 1e12) > nbytes / (hbm_peak * 1e9):
+        roofline.update(bound="tensor", achieved=tflops_achieved, peak=tensor_peak, unit="TFLOP/s",
+                        frac=tflops_achieved / tensor_peak,
+                        peak_source=f"{peak_src} bf16_tflops (burst)"
+                                    + (" x 2 (nominal e4m3 / bf16 ratio)" if f8 else ""))
     else:
         roofline.update(bound="hbm", achieved=achieved, peak=hbm_peak, unit="GB/s",
                         frac=achieved / hbm_peak, peak_source=f"{peak_src} hbm_gbs")
@@ -485,7 +497,7 @@ def run_ours(args):
                    "seqlen": int(w.seqlens[0]), "page_block_size": w.page_size,
                    "block_table": "seeded random permutation", "softmax_scale": w.softmax_scale,
                    "l2": f"{len(sets)} rotating input sets, KV "
-                         f"{w.total_tokens * 576 * 2 / 1e6:.0f} MB each (> 129 MB L2)",
+                         f"{w.total_tokens * 576 * w.elem_bytes / 1e6:.0f} MB each (> 129 MB L2)",
                    "parallelism": f"replicas x{world}", "num_sm_parts": parts,
                    "layout": args.layout},
         "effective_hbm_gbs": world * nbytes / (ms * 1e-3) / 1e9,

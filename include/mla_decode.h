@@ -20,8 +20,9 @@
  *     stream).  Work is enqueued asynchronously; no entry point synchronises
  *     except mla_get_device_error.
  *   - Strides are in ELEMENTS.  Element types: q / kv_cache / out (and q_pe /
- *     k_pe) are fp16 or bf16 (the same for all); lse, the workspace are fp32;
- *     tables int32.
+ *     k_pe) are fp16 or bf16 (the same for all), or q / kv_cache are e4m3 and
+ *     out is bf16 (MLA_DTYPE_E4M3, below); lse, the workspace are fp32; tables
+ *     int32.
  *   - Argument errors are detected on the host, before any launch, and return
  *     a negative mla_status without touching the GPU.  Launch failures return
  *     MLA_ERR_CUDA.  Faults the kernels detect while running (a block-table
@@ -38,7 +39,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 3
+#define MLA_ABI_VERSION 4
 
 /* Shape contract [TL §先看核心难点]: 576 = 512 latent + 64 RoPE; v = 512. */
 #define MLA_HEAD_DIM 576
@@ -59,7 +60,8 @@ typedef enum {
   MLA_OK = 0,
   MLA_ERR_NULL = -1,            /* a required pointer is NULL */
   MLA_ERR_SHAPE = -2,           /* unsupported or inconsistent dimension */
-  MLA_ERR_DTYPE = -3,           /* dtype is not fp16 / bf16 */
+  MLA_ERR_DTYPE = -3,           /* dtype is not fp16 / bf16 / e4m3, or e4m3 with
+                                   separate q_pe / k_pe or a non-finite scale */
   MLA_ERR_ALIGN = -4,           /* pointer or stride violates 16-byte alignment */
   MLA_ERR_PAGE = -5,            /* page_block_size not a positive multiple of 64 */
   MLA_ERR_WORKSPACE = -6,       /* workspace missing or too small */
@@ -69,7 +71,19 @@ typedef enum {
   MLA_ERR_ARCH = -10            /* the current device is not sm_103 */
 } mla_status;
 
-enum { MLA_DTYPE_FP16 = 0, MLA_DTYPE_BF16 = 1 };
+/*
+ * MLA_DTYPE_E4M3: an FP8 KV cache [TL §变体内核 names an FP8-cache variant of
+ * the decode kernel and fixes no format; this is the library's reading].  q and
+ * kv_cache hold OCP e4m3 bytes (1 sign, 4 exponent bits with bias 7, 3 fraction
+ * bits, no infinities, S.1111.111 is NaN), each tensor with one fp32
+ * dequantisation scale: the decode runs on q_scale * q and kv_scale * kv, i.e.
+ * x_t = softmax_scale * q_scale * kv_scale * (q . kv[t]) and
+ * out = kv_scale * sum_t softmax_t(x) * kv[t][0:512].  out is bf16.  The
+ * softmax weights are rounded to e4m3 before the value product (they are at most
+ * 256 there, so none saturates); O is divided by the sum of the rounded weights.
+ * Only the fused layout: q_pe and k_pe must be NULL.  Strides count bytes.
+ */
+enum { MLA_DTYPE_FP16 = 0, MLA_DTYPE_BF16 = 1, MLA_DTYPE_E4M3 = 2 };
 
 /*
  * Detail code of MLA_ERR_DEVICE_TIMEOUT: the split kernel's wait that gave up
@@ -157,7 +171,8 @@ typedef enum {
  * token qi sees (all t < L_i, or t < L_i - (s - 1 - qi) with is_causal), computed with
  * exp2-based online softmax, split-KV partials and a combine pass
  * [TL §Split Kernel, §Combine Kernel].  Accumulation is fp32; the softmax
- * weights are rounded to the input dtype before the value product.
+ * weights are rounded to the input dtype before the value product (for e4m3,
+ * see MLA_DTYPE_E4M3 for the scales).
  */
 typedef struct mla_fwd_params {
   int32_t b;              /* sequences (>= 1) */
@@ -166,7 +181,7 @@ typedef struct mla_fwd_params {
   int32_t h_k;            /* KV heads: must be 1 */
   int32_t d;              /* must be MLA_HEAD_DIM */
   int32_t d_v;            /* must be MLA_HEAD_DIM_V */
-  int32_t dtype;          /* MLA_DTYPE_FP16 or MLA_DTYPE_BF16 */
+  int32_t dtype;          /* MLA_DTYPE_FP16, MLA_DTYPE_BF16 or MLA_DTYPE_E4M3 */
   float softmax_scale;    /* multiplies q.k before the softmax */
 
   const void *q;
@@ -203,6 +218,11 @@ typedef struct mla_fwd_params {
 
   /* seqlen_q > 1 only: nonzero = causal mask among the query tokens (above) */
   int32_t is_causal;
+
+  /* MLA_DTYPE_E4M3 only (ignored otherwise): dequantisation scales of q and
+   * kv_cache, finite and > 0 */
+  float q_scale;
+  float kv_scale;
 } mla_fwd_params;
 
 /* ABI version (MLA_ABI_VERSION) and sizeof(mla_fwd_params), for bindings. */
@@ -260,8 +280,8 @@ int mla_workspace_size(int b, int h, int num_sm_parts, size_t *bytes);
  * FM §内存访问优化, §Softmax 计算优化].  Enqueues the split kernel (a
  * persistent grid of 2-CTA clusters walking the metadata) and the combine
  * kernel on `stream`.  Alignment: q, kv_cache, out, workspace (and q_pe,
- * k_pe when given) 16-byte aligned; all their strides multiples of 8
- * elements.  Row strides must cover the row: kv_row_stride >= 576 (>= 512
+ * k_pe when given) 16-byte aligned; all their strides multiples of 16 bytes
+ * (8 elements; 16 for e4m3 q / kv_cache).  Row strides must cover the row: kv_row_stride >= 576 (>= 512
  * with k_pe), k_pe_row_stride >= 64, each page stride >= page_block_size
  * times its row stride.
  */

@@ -20,20 +20,26 @@ __all__ = [
     "mla_metadata_shape", "mla_get_metadata", "mla_workspace_size", "mla_decode_fwd",
     "mla_decode_fwd_timed", "prepare_decode", "DecodeCall", "prepare_metadata", "MetadataCall",
     "mla_get_device_error", "mla_test_forced_timeout", "library_path", "HEAD_DIM", "HEAD_DIM_V", "ROPE_DIM", "BLOCK_N",
-    "META_STRIDE", "SCHED_FIXED_COST", "SCHED_SEGMENT_COST", "MAX_NUM_SM",
+    "META_STRIDE", "SCHED_FIXED_COST", "SCHED_SEGMENT_COST", "MAX_NUM_SM", "out_dtype",
 ]
 
 HEAD_DIM = 576
 HEAD_DIM_V = 512
 ROPE_DIM = HEAD_DIM - HEAD_DIM_V
-ABI_VERSION = 3
+ABI_VERSION = 4
 BLOCK_N = 64
 META_STRIDE = 8
 SCHED_FIXED_COST = 5
 SCHED_SEGMENT_COST = 16
 MAX_NUM_SM = 2046
 STATIC_WORKSPACE_BYTES = 64 << 20
-_DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1}
+_DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1, torch.float8_e4m3fn: 2}
+
+
+def out_dtype(dtype):
+    """dtype of `out` for q / kv_cache of `dtype`: the same, bf16 for e4m3."""
+    return torch.bfloat16 if dtype == torch.float8_e4m3fn else dtype
+
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -63,6 +69,7 @@ class FwdParams(ctypes.Structure):
         ("q_pe", _vp), ("q_pe_batch_stride", _i64), ("q_pe_head_stride", _i64),
         ("k_pe", _vp), ("k_pe_page_stride", _i64), ("k_pe_row_stride", _i64),
         ("is_causal", _i32),
+        ("q_scale", ctypes.c_float), ("kv_scale", ctypes.c_float),
     ]
 
 
@@ -226,7 +233,8 @@ def mla_workspace_size(b, h, num_sm_parts):
 
 def mla_decode_fwd(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                    tile_scheduler_metadata, num_splits, out=None, lse=None, workspace=None,
-                   split_events=None, q_pe=None, k_pe=None, is_causal=False):
+                   split_events=None, q_pe=None, k_pe=None, is_causal=False, q_scale=1.0,
+                   kv_scale=1.0):
     """Paged split-KV MLA decode (see prepare_decode for the argument contract).
 
     split_events: optional (begin, end) torch.cuda.Event pair recorded around the
@@ -234,7 +242,8 @@ def mla_decode_fwd(q, kv_cache, block_table, cache_seqlens, softmax_scale,
     """
     call = prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                           tile_scheduler_metadata, num_splits, out, lse, workspace,
-                          q_pe=q_pe, k_pe=k_pe, is_causal=is_causal)
+                          q_pe=q_pe, k_pe=k_pe, is_causal=is_causal, q_scale=q_scale,
+                          kv_scale=kv_scale)
     call(split_events=split_events)
     return call.out, call.lse
 
@@ -266,13 +275,17 @@ class DecodeCall:
 
 def prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                    tile_scheduler_metadata, num_splits, out=None, lse=None, workspace=None,
-                   q_pe=None, k_pe=None, is_causal=False):
+                   q_pe=None, k_pe=None, is_causal=False, q_scale=1.0, kv_scale=1.0):
     """Paged split-KV MLA decode.
 
     q [b, 1, h, 576], kv_cache [num_pages, page_size, 1, 576] (fp16 or bf16, same
     dtype), block_table int32 [b, max_blocks], cache_seqlens int32 [b], metadata
     from mla_get_metadata.  Returns (out [b, 1, h, 512] in q's dtype, lse fp32 [b, h]
     natural-log).  Launches on the current stream of q's device.
+
+    FP8 cache: q and kv_cache both torch.float8_e4m3fn with dequantisation scales
+    q_scale and kv_scale (the decode runs on q_scale * q and kv_scale * kv); out is
+    bf16; the RoPE columns must be inside q and kv_cache (no q_pe / k_pe).
 
     Split layout: with q_pe [b, s, h, 64] given, q is [b, s, h, 512] (latent
     columns only); with k_pe [num_pages, page_size, 1, 64] given, kv_cache is
@@ -293,7 +306,10 @@ def prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
     if kv_cache.dim() != 4 or kv_cache.shape[2] != 1 or kv_cache.shape[3] != kv_cols:
         raise ValueError(f"kv_cache must be [num_pages, page_size, 1, {kv_cols}]")
     if q.dtype not in _DTYPE_CODE or kv_cache.dtype != q.dtype:
-        raise ValueError("q and kv_cache must share dtype fp16 or bf16")
+        raise ValueError("q and kv_cache must share dtype fp16, bf16 or float8_e4m3fn")
+    f8 = q.dtype == torch.float8_e4m3fn
+    if f8 and (q_pe is not None or k_pe is not None):
+        raise ValueError("an e4m3 cache takes the RoPE columns inside q and kv_cache")
     if q_pe is not None and (q_pe.dim() != 4 or tuple(q_pe.shape) != (q.shape[0], s_q,
                                                                        q.shape[2], ROPE_DIM)):
         raise ValueError("q_pe must be [b, s, h, 64]")
@@ -327,13 +343,14 @@ def prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
     parts = tile_scheduler_metadata.shape[0]
     dev = q.device
     lse_shape = (b, h) if s_q == 1 else (b, s_q, h)
+    odt = out_dtype(q.dtype)
     if out is None:
-        out = torch.empty((b, s_q, h, HEAD_DIM_V), dtype=q.dtype, device=dev)
+        out = torch.empty((b, s_q, h, HEAD_DIM_V), dtype=odt, device=dev)
     if lse is None:
         lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
-    if (out.shape != (b, s_q, h, HEAD_DIM_V) or out.dtype != q.dtype or out.stride(3) != 1
+    if (out.shape != (b, s_q, h, HEAD_DIM_V) or out.dtype != odt or out.stride(3) != 1
             or (s_q > 1 and out.stride(1) != h * out.stride(2))):
-        raise ValueError("out must be [b, s, h, 512] in q's dtype, contiguous columns, "
+        raise ValueError(f"out must be [b, s, h, 512] in {odt}, contiguous columns, "
                          "evenly strided rows")
     if (tuple(lse.shape) != lse_shape or lse.dtype != torch.float32 or lse.stride(-1) != 1
             or (s_q > 1 and lse.stride(1) != h)):
@@ -347,6 +364,7 @@ def prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
     p.is_causal = 1 if is_causal else 0
     p.dtype = _DTYPE_CODE[q.dtype]
     p.softmax_scale = float(softmax_scale)
+    p.q_scale, p.kv_scale = float(q_scale), float(kv_scale)
     p.q, p.q_batch_stride, p.q_head_stride = q.data_ptr(), q.stride(0), q.stride(2)
     p.kv_cache = kv_cache.data_ptr()
     p.kv_page_stride, p.kv_row_stride = kv_cache.stride(0), kv_cache.stride(1)
@@ -380,14 +398,14 @@ def mla_decode_fwd_timed(*args, split_events, **kw):
 
 def mla_decode_fwd_static(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                           tile_scheduler_metadata, num_splits, out=None, lse=None, q_pe=None,
-                          k_pe=None, is_causal=False):
+                          k_pe=None, is_causal=False, q_scale=1.0, kv_scale=1.0):
     """mla_decode_fwd with the library's built-in per-device scratch
     (STATIC_WORKSPACE_BYTES) in place of a workspace tensor: the C call allocates
     nothing.  Calls on one device must not overlap on the GPU.  Returns (out, lse)."""
     no_ws = torch.empty((0,), dtype=torch.uint8, device=q.device)
     call = prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                           tile_scheduler_metadata, num_splits, out, lse, no_ws, q_pe=q_pe,
-                          k_pe=k_pe, is_causal=is_causal)
+                          k_pe=k_pe, is_causal=is_causal, q_scale=q_scale, kv_scale=kv_scale)
     lib = _load()
     with torch.cuda.device(call.device):
         rc = lib.mla_decode_fwd_static(ctypes.byref(call.params), _stream(call.device))

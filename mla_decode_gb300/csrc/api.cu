@@ -79,7 +79,8 @@ const char *mla_status_string(int s) {
     case MLA_OK: return "ok";
     case MLA_ERR_NULL: return "a required pointer is NULL";
     case MLA_ERR_SHAPE: return "unsupported or inconsistent shape";
-    case MLA_ERR_DTYPE: return "dtype must be fp16 or bf16";
+    case MLA_ERR_DTYPE:
+      return "dtype must be fp16, bf16 or e4m3 (e4m3: fused layout, finite positive scales)";
     case MLA_ERR_ALIGN: return "pointer or stride is not 16-byte aligned";
     case MLA_ERR_PAGE: return "page_block_size must be a positive multiple of 64";
     case MLA_ERR_WORKSPACE: return "workspace missing or too small";
@@ -175,9 +176,14 @@ int resolve_args(const mla_fwd_params *p, FwdArgs &a) {
     return MLA_ERR_SHAPE;
   const int rows = p->seqlen_q * p->h;  // query rows per sequence, token-major
   if (rows > 1024) return MLA_ERR_SHAPE;
-  if (p->dtype != MLA_DTYPE_FP16 && p->dtype != MLA_DTYPE_BF16) return MLA_ERR_DTYPE;
-  if (p->page_block_size <= 0 || p->page_block_size % MLA_BLOCK_N != 0) return MLA_ERR_PAGE;
+  if (p->dtype != MLA_DTYPE_FP16 && p->dtype != MLA_DTYPE_BF16 && p->dtype != MLA_DTYPE_E4M3)
+    return MLA_ERR_DTYPE;
+  const bool f8 = p->dtype == MLA_DTYPE_E4M3;
   const bool sep_q = p->q_pe != nullptr, sep_k = p->k_pe != nullptr;
+  if (f8 && (sep_q || sep_k || !(isfinite(p->q_scale) && p->q_scale > 0.f) ||
+             !(isfinite(p->kv_scale) && p->kv_scale > 0.f)))
+    return MLA_ERR_DTYPE;
+  if (p->page_block_size <= 0 || p->page_block_size % MLA_BLOCK_N != 0) return MLA_ERR_PAGE;
   const int kv_cols = sep_k ? MLA_HEAD_DIM_V : MLA_HEAD_DIM;
   if (p->num_pages < 1 || p->max_blocks_per_seq < 1 || p->num_sm_parts < 1 ||
       p->q_head_stride < 1 || p->q_batch_stride < 1 || p->kv_row_stride < kv_cols ||
@@ -189,9 +195,11 @@ int resolve_args(const mla_fwd_params *p, FwdArgs &a) {
   if (sep_k && (p->k_pe_row_stride < MLA_HEAD_DIM - MLA_HEAD_DIM_V ||
                 p->k_pe_page_stride < (int64_t)p->page_block_size * p->k_pe_row_stride))
     return MLA_ERR_SHAPE;
+  // TMA strides are multiples of 16 bytes: 8 16-bit elements, 16 e4m3 bytes
+  const int64_t in16 = f8 ? 16 : 8;
   if (!aligned16(p->q) || !aligned16(p->kv_cache) || !aligned16(p->out) ||
-      !aligned16(p->workspace) || (p->q_batch_stride % 8) || (p->q_head_stride % 8) ||
-      (p->kv_page_stride % 8) || (p->kv_row_stride % 8) || (p->o_batch_stride % 8) ||
+      !aligned16(p->workspace) || (p->q_batch_stride % in16) || (p->q_head_stride % in16) ||
+      (p->kv_page_stride % in16) || (p->kv_row_stride % in16) || (p->o_batch_stride % 8) ||
       (p->o_head_stride % 8))
     return MLA_ERR_ALIGN;
   if (sep_q && (!aligned16(p->q_pe) || (p->q_pe_batch_stride % 8) || (p->q_pe_head_stride % 8)))
@@ -210,15 +218,17 @@ int resolve_args(const mla_fwd_params *p, FwdArgs &a) {
   a.heads = p->h;
   a.causal = p->seqlen_q > 1 && p->is_causal != 0;
   a.dtype = p->dtype;
-  a.scale_log2 = p->softmax_scale * 1.4426950408889634f;
+  a.scale_log2 = f8 ? (float)((double)p->softmax_scale * 1.4426950408889634 * p->q_scale * p->kv_scale)
+                   : p->softmax_scale * 1.4426950408889634f;
+  a.o_scale = f8 ? p->kv_scale : 1.f;
   a.q = p->q;
   a.q_batch_stride = p->q_batch_stride;
   a.q_head_stride = p->q_head_stride;
   a.kv = p->kv_cache;
   a.kv_page_stride = p->kv_page_stride;
   a.kv_row_stride = p->kv_row_stride;
-  // fused layout: the RoPE columns are 512 elements (1 KB) into each row
-  const int64_t rope_off = MLA_HEAD_DIM_V * 2;
+  // fused layout: the RoPE columns are 512 elements into each row
+  const int64_t rope_off = MLA_HEAD_DIM_V * (f8 ? 1 : 2);
   a.q_pe = sep_q ? p->q_pe : static_cast<const char *>(p->q) + rope_off;
   a.q_pe_batch_stride = sep_q ? p->q_pe_batch_stride : p->q_batch_stride;
   a.q_pe_head_stride = sep_q ? p->q_pe_head_stride : p->q_head_stride;

@@ -123,8 +123,9 @@ cudaError_t launch_combine(const FwdArgs &a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return a.dtype == MLA_DTYPE_BF16 ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, a)
-                                   : cudaLaunchKernelEx(&cfg, combine_kernel<__half>, a);
+  // e4m3 inputs give bf16 outputs
+  return a.dtype == MLA_DTYPE_FP16 ? cudaLaunchKernelEx(&cfg, combine_kernel<__half>, a)
+                                   : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, a);
 }
 
 }  // namespace mla

@@ -14,7 +14,9 @@ struct FwdArgs {
   int q_len;         // query tokens per sequence
   int heads;         // query heads per token (rows q_len * heads)
   int causal;        // token qi sees the cached tokens t < L - (q_len - 1 - qi)
-  float scale_log2;  // softmax_scale * log2(e): scores are kept in base-2 units
+  float scale_log2;  // softmax_scale * log2(e) (times q_scale * kv_scale for e4m3):
+                     // scores are kept in base-2 units
+  float o_scale;     // multiplies the normalised output: kv_scale for e4m3, else 1
   const void *q;
   int64_t q_batch_stride, q_head_stride;
   const void *kv;

@@ -7,10 +7,11 @@
 //   smem descriptor (64 bit): start address >> 4 in bits [0,14), leading-dimension
 //     byte offset >> 4 in [16,30), stride-dimension byte offset >> 4 in [32,46),
 //     the constant 1 in [46,48), base offset in [49,52), swizzle mode in [61,64)
-//     (2 = 128-byte swizzle).
-//   instruction descriptor (32 bit, kind::f16): D format in [4,6) (1 = f32),
-//     A format [7,10) and B format [10,13) (0 = f16, 1 = bf16), A / B major in
-//     bits 15 / 16 (0 = K-major, 1 = MN-major), N >> 3 in [17,23), M >> 4 in [24,29).
+//     (2 = 128-byte swizzle, 4 = 64-byte swizzle).
+//   instruction descriptor (32 bit): D format in [4,6) (1 = f32), A format
+//     [7,10) and B format [10,13) (kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4:
+//     0 = e4m3), A / B major in bits 15 / 16 (0 = K-major, 1 = MN-major),
+//     N >> 3 in [17,23), M >> 4 in [24,29).
 #pragma once
 
 #include <stdint.h>
@@ -233,6 +234,26 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// The same two forms for 8-bit operands (kind::f8f6f4: K = 32 per instruction).
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on `bar` (this CTA) once all previously issued MMAs of this thread complete.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile(
@@ -329,7 +350,21 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t addr) {
   return d;
 }
 
-// MN-major operand: each K row holds 64 contiguous MN elements (128 bytes,
+// K-major operand tile stored as rows of 64 bytes with the 64-byte swizzle,
+// 8-row atoms 512 bytes apart (what a TMA box 64 bytes wide with SWIZZLE_64B
+// produces).
+__device__ __forceinline__ uint64_t desc_kmajor_sw64(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)1 << 16;                  // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(512 >> 4) << 32;         // 8-row group stride
+  d |= (uint64_t)1 << 46;                  // descriptor version
+  d |= (uint64_t)4 << 61;                  // 64-byte swizzle
+  return d;
+}
+
+// MN-major operand: each K row holds 128 contiguous bytes of MN elements (64 16-bit
+// or 128 8-bit,
 // swizzled); 8-row K groups are `sbo` bytes apart and consecutive 64-element MN
 // atoms are `lbo` bytes apart.
 __device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -342,7 +377,8 @@ __device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t addr, uint32_t l
   return d;
 }
 
-// kind::f16 instruction descriptor: f32 accumulate, A/B both bf16 (or both f16).
+// Instruction descriptor: f32 accumulate, A and B of the same format (format bit
+// 1: bf16 under kind::f16; 0: f16 under kind::f16, e4m3 under kind::f8f6f4).
 __host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool bf16, bool a_mn_major,
                                                  bool b_mn_major) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |

@@ -49,6 +49,9 @@
 
 #include <atomic>
 #include <mutex>
+#include <type_traits>
+
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "sm100.cuh"
@@ -60,21 +63,15 @@ using namespace sm100;
 
 constexpr int kThreads = 352;            // 11 warps (see the role map in the kernel)
 constexpr int kSB = 2;                   // pages (64 tokens each) per superblock
-constexpr int kNK = 2;                   // K ring entries (score CTA): one page each
-constexpr int kNV = 4;                   // V half-page tiles in flight (value CTA)
 constexpr int kNPR = 4;                  // P tiles in the value CTA's ring
 constexpr int kStageTiles = 4;           // P staging tiles in the score CTA (a ring)
 constexpr int kSBufs = 3;                // S accumulators in the score CTA's TMEM, one page each
-// score CTA TMEM columns: Q as packed 16-bit pairs (latent 0..255, RoPE 256..287),
-// then the S page accumulators (64 columns each)
-constexpr uint32_t kTQpe = 256;
+// score CTA TMEM columns: Q (latent, then RoPE), then the S page accumulators
+// (64 columns each) from kTS0
 constexpr uint32_t kTS0 = 320;
 static_assert(kTS0 + 64 * kSBufs <= 512, "score TMEM budget");
 constexpr int kChunk = 8192;             // [64 rows][128 B] swizzled atom
-constexpr int kKPage = 9 * kChunk;       // K entry: one page's 576 columns as nine atoms (72 KB)
-constexpr int kQBox = 2 * kChunk;        // [128 rows][64 columns] of Q (16 KB)
-constexpr int kVSlot = 4 * kChunk;       // 256 value columns of one page
-constexpr int kPTile = 16384;            // [128 heads][64 tokens] 16-bit, swizzled
+constexpr int kQBox = 2 * kChunk;        // [128 rows][128 B] box of Q (16 KB)
 constexpr float kTau = 8.f;              // lazy rescale: the reference max moves only when a
                                          // block exceeds it by more than this (log2 units)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // every wait: 1 s
@@ -82,28 +79,16 @@ constexpr uint64_t kForcedWaitNs = 1000000ull;     // the forced-timeout test's 
 
 struct Header {  // score -> value CTA, one per superblock
   float alpha[128];  // O rescale factor per row
-  float l[128];      // last superblock: row sum of the 16-bit weights (divides O)
+  float l[128];      // last superblock: row sum of the rounded weights (divides O)
   uint32_t flags;    // bit 1: last superblock of the segment
   uint32_t pad[3];
 };
 static_assert(sizeof(Header) % 16 == 0, "bulk copies move multiples of 16 bytes");
 
-// shared-memory map (offsets from the 1024-aligned base)
-constexpr int kOffK = 0;                                      // score: K ring (whole pages)
-constexpr int kOffPStage = kOffK + kNK * kKPage;              // score: P staging tiles
-constexpr int kOffHdrStage = kOffPStage + kStageTiles * kPTile;    // score: 2 headers
-constexpr int kOffRed = kOffHdrStage + 2 * (int)sizeof(Header);    // score: [3][2][128] floats
-constexpr int kScoreEnd = kOffRed + 6 * 128 * 4;
-constexpr int kOffV = 0;                                      // value: V ring
-constexpr int kOffPRing = kOffV + kNV * kVSlot;               // value: P tiles
-constexpr int kOffHdr = kOffPRing + kNPR * kPTile;            // value: 2 headers
-constexpr int kOffEpi = (kOffHdr + 2 * (int)sizeof(Header) + 1023) & ~1023;  // value: 8 x 2 KB
-constexpr int kValueEnd = kOffEpi + 8 * 2048;                 // epilogue staging, one per warp
-static_assert(kValueEnd <= kScoreEnd, "the value CTA's staging fits in the score CTA's footprint");
-constexpr int kOffBars = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 127) & ~127;
+constexpr int kNKMax = 5, kNVMax = 8;    // deepest K / V rings (e4m3)
 
 struct Bars {
-  uint64_t k_full[kNK], k_empty[kNK];   // score
+  uint64_t k_full[kNKMax], k_empty[kNKMax];  // score
   uint64_t s_full[kSBufs], s_free[kSBufs];  // score, per S page buffer
   uint64_t q_free;                      // score: MMAs of a segment done with Q (MMA commit)
   uint64_t qs_full;                     // score: first segment's Q columns 0..255 in staging
@@ -111,7 +96,7 @@ struct Bars {
   uint64_t stage_free[kStageTiles];     // score: a staging tile's copy landed (value CTA)
   uint64_t slot_free[kNPR];             // score, value-CTA MMA commits (multicast)
   uint64_t hdr_free[2];                 // score, arrived by the value CTA (both groups)
-  uint64_t v_full[kNV], v_empty[kNV];   // value
+  uint64_t v_full[kNVMax], v_empty[kNVMax];  // value
   uint64_t p_full[kNPR];                // value, bulk copies from the score CTA
   uint64_t hdr_full[2];                 // value, bulk copies from the score CTA
   uint64_t o_ready[2][2], o_done[2][2]; // value, [O half][superblock parity]
@@ -119,8 +104,54 @@ struct Bars {
   uint32_t tmem_base;
   int abort;
 };
-constexpr int kSmemBytes = kOffBars + (int)sizeof(Bars) + 1024;  // + alignment slack
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+// Geometry per element width.  Both widths keep a page's scores in one M=128 x
+// N=64 accumulator and feed the tensor cores 32 bytes of each row per MMA (K = 16
+// 16-bit or K = 32 8-bit elements).
+//  16-bit (kind::f16): a K ring entry is one page's 576 columns as nine swizzled
+//    [64 rows x 64 columns] atoms (72 KB, 128-byte swizzle); Q takes TMEM columns
+//    0..255 (latent) and 256..287 (RoPE); P tiles are [128 heads x 64 tokens]
+//    16-bit with the 128-byte swizzle; a V tile is one O half of one page, four
+//    [64 x 64] atoms (32 KB).
+//  e4m3 (kind::f8f6f4): a K ring entry is nine [64 rows x 64 B] atoms with the
+//    64-byte swizzle (36 KB, one TMA request), so the ring holds five pages; Q
+//    takes TMEM columns 0..127 and 128..143; P tiles are [128 x 64] bytes with the
+//    64-byte swizzle (8 KB); a V tile is two [64 rows x 128 B] atoms (16 KB).
+template <bool kF8>
+struct Geo {
+  static constexpr int kKEntry = kF8 ? 9 * 4096 : 9 * kChunk;
+  static constexpr int kNK = kF8 ? 5 : 2;             // K ring entries, one page each
+  static constexpr int kPTile = kF8 ? 8192 : 16384;
+  static constexpr int kVSlot = kF8 ? 2 * kChunk : 4 * kChunk;
+  static constexpr int kNV = kF8 ? 8 : 4;             // V tiles in flight
+  static constexpr int kVAtoms = kF8 ? 2 : 4;         // [64 rows x 128 B] atoms per V tile
+  static constexpr int kQHalf = kF8 ? 2 : 4;          // Q boxes per 256 latent columns
+  static constexpr int kQBoxCols = kF8 ? 128 : 64;    // Q columns per box
+  static constexpr uint32_t kTQhalf = kF8 ? 64 : 128; // TMEM columns per 256 latent columns
+  static constexpr uint32_t kTQpe = 2 * kTQhalf;      // Q's RoPE columns in TMEM
+  static constexpr int kRopeCps = kF8 ? 2 : 4;        // 32-byte TMEM copies of a row's RoPE part
+  static constexpr int kKStep = kF8 ? 32 : 16;        // K (tokens) per P.V MMA
+  // shared-memory map (offsets from the 1024-aligned base)
+  static constexpr int kOffK = 0;                                      // score: K ring
+  static constexpr int kOffPStage = kOffK + kNK * kKEntry;             // score: P staging tiles
+  static constexpr int kOffHdrStage = kOffPStage + kStageTiles * kPTile;  // score: 2 headers
+  static constexpr int kOffRed = kOffHdrStage + 2 * (int)sizeof(Header);  // score: [3][2][128] floats
+  static constexpr int kScoreEnd = kOffRed + 6 * 128 * 4;
+  static constexpr int kOffV = 0;                                      // value: V ring
+  static constexpr int kOffPRing = kOffV + kNV * kVSlot;               // value: P tiles
+  static constexpr int kOffHdr = kOffPRing + kNPR * kPTile;            // value: 2 headers
+  static constexpr int kOffEpi = (kOffHdr + 2 * (int)sizeof(Header) + 1023) & ~1023;  // 8 x 2 KB
+  static constexpr int kValueEnd = kOffEpi + 8 * 2048;                 // epilogue staging, one per warp
+  static constexpr int kOffBars = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 127) & ~127;
+  static constexpr int kSmemBytes = kOffBars + (int)sizeof(Bars) + 1024;  // + alignment slack
+  static_assert(kNK <= kNKMax && kNV <= kNVMax, "ring barriers");
+  static_assert(kValueEnd <= kScoreEnd, "the value CTA's staging fits in the score CTA's footprint");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kOffPStage % 1024 == 0 && kKEntry % 1024 == 0 && kOffPRing % 1024 == 0 &&
+                kVSlot % 1024 == 0 && kPTile % 1024 == 0, "swizzle atoms");
+  static_assert(kQHalf * kQBox <= kKEntry && kQHalf * kQBox <= kStageTiles * kPTile,
+                "half of Q's latent columns fit a ring entry and the staging tiles");
+};
 
 // wait sites, reported as the error detail on a timeout (mla_wait_site)
 enum : int {
@@ -283,6 +314,49 @@ template <> struct Pack<__half> {
   static constexpr bool kBf16 = false;
 };
 
+// Per element type: the geometry, the type of `out`, and the MMA kind.  e4m3
+// inputs give bf16 outputs.
+template <typename T>
+constexpr bool kIsF8 = std::is_same<T, __nv_fp8_e4m3>::value;
+template <typename T>
+using GeoOf = Geo<kIsF8<T>>;
+template <typename T>
+using OutT = typename std::conditional<kIsF8<T>, __nv_bfloat16, T>::type;
+
+// The instruction descriptor's A / B format bits: 0 is f16 for kind::f16 and
+// e4m3 for kind::f8f6f4, 1 is bf16.
+template <typename T>
+constexpr bool kFmtBit = std::is_same<T, __nv_bfloat16>::value;
+
+template <typename T>
+__device__ __forceinline__ void mma_ts_t(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t acc) {
+  if constexpr (kIsF8<T>) mma_ts_f8(d, a, b, idesc, acc);
+  else mma_ts(d, a, b, idesc, acc);
+}
+template <typename T>
+__device__ __forceinline__ void mma_ss_t(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t acc) {
+  if constexpr (kIsF8<T>) mma_ss_f8(d, a, b, idesc, acc);
+  else mma_ss(d, a, b, idesc, acc);
+}
+
+// Four weights as e4m3 bytes, the first in the lowest byte (rounded to nearest
+// even; the weights are finite and at most 256, so nothing saturates).
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+// The sum of four packed e4m3 values, as floats (the conversions are exact).
+__device__ __forceinline__ float sum_e4m3x4(uint32_t u) {
+  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(u & 0xffffu), __NV_E4M3);
+  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(u >> 16), __NV_E4M3);
+  const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&lo));
+  const float2 y = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
+  return (x.x + x.y) + (y.x + y.y);
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -354,6 +428,10 @@ template <typename T>
 __device__ void score_producer(const FwdArgs &a, const CUtensorMap *kmap, const CUtensorMap *qmap,
                                const CUtensorMap *pemap, const CUtensorMap *qpemap,
                                uint8_t *smem, const Ctx &c, int part, int head0) {
+  using G = GeoOf<T>;
+  // the RoPE box of Q: the separate 64-column map (16-bit), or the 128-byte box at
+  // column 512 of the 576-byte rows, zero-filled past column 575 (e4m3)
+  constexpr int kRopeX = kIsF8<T> ? MLA_HEAD_DIM_V : 0;
   Bars *b = c.bars;
   uint32_t kc = 0;      // ring entries filled so far
   bool first_seg = true;  // the part's first (non-empty) segment
@@ -363,8 +441,8 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *kmap, const 
   bool hc = false, hn = false;
   // the next ring entry, once the MMAs of its previous use are done with it
   auto next_entry = [&](uint32_t &slot) -> bool {
-    slot = kc % kNK;
-    const uint32_t use = kc / kNK;
+    slot = kc % G::kNK;
+    const uint32_t use = kc / G::kNK;
     ++kc;
     return use == 0 || wait_bar<false>(c, &b->k_empty[slot], (use - 1) & 1, W_K_EMPTY);
   };
@@ -373,25 +451,27 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *kmap, const 
       // ring uses: first segment: RoPE box, latent 256..511 (latent 0..255 go to the
       // staging tiles); later segments: latent 0..255, latent 256..511, RoPE box
       if (first_seg && leader) {
-        mbar_arrive_expect_tx(&b->qs_full, 4 * kQBox);
+        mbar_arrive_expect_tx(&b->qs_full, G::kQHalf * kQBox);
 #pragma unroll
-        for (int bx = 0; bx < 4; ++bx)
-          tma_load_3d(smem + kOffPStage + bx * kQBox, qmap, &b->qs_full, 64 * bx, head0, j.seq);
+        for (int bx = 0; bx < G::kQHalf; ++bx)
+          tma_load_3d(smem + G::kOffPStage + bx * kQBox, qmap, &b->qs_full, G::kQBoxCols * bx, head0,
+                      j.seq);
       }
       for (int i = first_seg ? 1 : 0; i < 3; ++i) {
         const int what = first_seg ? (i == 1 ? 2 : 1) : i;  // 0, 1: latent halves; 2: RoPE
         uint32_t slot;
         if (!next_entry(slot)) return false;
         if (leader) {
-          uint8_t *dst = smem + kOffK + slot * kKPage;
+          uint8_t *dst = smem + G::kOffK + slot * G::kKEntry;
           if (what < 2) {
-            mbar_arrive_expect_tx(&b->k_full[slot], 4 * kQBox);
+            mbar_arrive_expect_tx(&b->k_full[slot], G::kQHalf * kQBox);
 #pragma unroll
-            for (int bx = 0; bx < 4; ++bx)
-              tma_load_3d(dst + bx * kQBox, qmap, &b->k_full[slot], 64 * (4 * what + bx), head0, j.seq);
+            for (int bx = 0; bx < G::kQHalf; ++bx)
+              tma_load_3d(dst + bx * kQBox, qmap, &b->k_full[slot],
+                          G::kQBoxCols * (G::kQHalf * what + bx), head0, j.seq);
           } else {
             mbar_arrive_expect_tx(&b->k_full[slot], kQBox);
-            tma_load_3d(dst, qpemap, &b->k_full[slot], 0, head0, j.seq);
+            tma_load_3d(dst, qpemap, &b->k_full[slot], kRopeX, head0, j.seq);
           }
         }
       }
@@ -404,10 +484,10 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *kmap, const 
       uint32_t slot;
       if (!next_entry(slot)) return false;
       if (leader) {
-        mbar_arrive_expect_tx(&b->k_full[slot], kKPage);
-        uint8_t *dst = smem + kOffK + slot * kKPage;
+        mbar_arrive_expect_tx(&b->k_full[slot], G::kKEntry);
+        uint8_t *dst = smem + G::kOffK + slot * G::kKEntry;
         tma_load_4d(dst, kmap, &b->k_full[slot], 0, j.pg.row0[p], 0, j.pg.page[p]);
-        if (!a.k_fused)
+        if (!kIsF8<T> && !a.k_fused)
           tma_load_3d(dst + 8 * kChunk, pemap, &b->k_full[slot], 0, j.pg.row0[p], j.pg.page[p]);
       }
     }
@@ -437,17 +517,18 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *kmap, const 
 // a lane that leaves on a failed wait cannot block the others.
 template <typename T>
 __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int part, uint32_t tmem) {
+  using G = GeoOf<T>;
   Bars *b = c.bars;
   const uint32_t tQ = tmem;
-  const uint32_t idesc = idesc_f16(128, 64, Pack<T>::kBf16, false, false);
-  static_assert(kOffK % 1024 == 0 && kKPage % 1024 == 0, "swizzle atoms");
-  const uint64_t kdesc = desc_kmajor_sw128(smem_u32(smem + kOffK));
+  const uint32_t idesc = idesc_f16(128, 64, kFmtBit<T>, false, false);
+  const uint64_t kdesc = kIsF8<T> ? desc_kmajor_sw64(smem_u32(smem + G::kOffK))
+                                  : desc_kmajor_sw128(smem_u32(smem + G::kOffK));
   const uint32_t kfull = smem_u32(&b->k_full[0]), kempty = smem_u32(&b->k_empty[0]);
   uint32_t slot = 0, phase = 0;  // ring position of the next entry and its k_full parity
   uint32_t pgc = 0, segn = 0;    // pages issued (S page buffer pgc % kSBufs), segments
   const bool leader = elect_one();
   auto advance = [&]() {
-    if (++slot == kNK) {
+    if (++slot == G::kNK) {
       slot = 0;
       phase ^= 1u;
     }
@@ -473,23 +554,25 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
       if (what == 3) {  // latent 0..255 in the staging tiles (first segment)
         if (!wait_bar<false>(c, &b->qs_full, 0, W_K_FULL)) return;
         tc_fence_after();
-        bd = desc_kmajor_sw128(smem_u32(smem + kOffPStage));
+        bd = desc_kmajor_sw128(smem_u32(smem + G::kOffPStage));
       } else {
         if (!wait_addr<false>(c, kfull + 8 * slot, phase, W_K_FULL)) return;
         tc_fence_after();
-        bd = kdesc + (uint64_t)(slot * (kKPage >> 4));
+        // Q boxes use the 128-byte swizzle in either width
+        bd = desc_kmajor_sw128(smem_u32(smem + G::kOffK + slot * G::kKEntry));
       }
       if (leader) {
         if (what != 2) {
-          const uint32_t t0 = tQ + (what == 1 ? 128 : 0);
+          const uint32_t t0 = tQ + (what == 1 ? G::kTQhalf : 0);
 #pragma unroll
-          for (int bx = 0; bx < 4; ++bx)
+          for (int bx = 0; bx < G::kQHalf; ++bx)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               tmem_cp_128x256b(t0 + 32 * bx + 8 * k, bd + (uint64_t)(bx * (kQBox >> 4) + 2 * k));
         } else {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) tmem_cp_128x256b(tQ + kTQpe + 8 * k, bd + (uint64_t)(2 * k));
+          for (int k = 0; k < G::kRopeCps; ++k)
+            tmem_cp_128x256b(tQ + G::kTQpe + 8 * k, bd + (uint64_t)(2 * k));
         }
         if (what != 3) mma_commit_addr(kempty + 8 * slot);
       }
@@ -505,17 +588,28 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
       const uint32_t tS = tmem + kTS0 + 64 * sbuf;
       if (!wait_addr<false>(c, kfull + 8 * slot, phase, W_K_FULL)) return;
       tc_fence_after();
-      const uint64_t bd = kdesc + (uint64_t)(slot * (kKPage >> 4));
+      const uint64_t bd = kdesc + (uint64_t)(slot * (G::kKEntry >> 4));
       if (leader) {
+        if constexpr (kIsF8<T>) {
+          // nine [64 x 64 B] atoms, 4 KB apart, two K = 32 steps each; Q's TMEM
+          // columns run on through the RoPE part (16 per atom)
 #pragma unroll
-        for (int blk = 0; blk < 8; ++blk)
+          for (int blk = 0; blk < 9; ++blk)
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+              mma_ts_t<T>(tS, tQ + 16 * blk + 8 * k, bd + (uint64_t)(blk * (4096 >> 4) + 2 * k), idesc,
+                          (blk | k) != 0);
+        } else {
+#pragma unroll
+          for (int blk = 0; blk < 8; ++blk)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ts_t<T>(tS, tQ + 32 * blk + 8 * k, bd + (uint64_t)(blk * (kChunk >> 4) + 2 * k), idesc,
+                          (blk | k) != 0);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ts(tS, tQ + 32 * blk + 8 * k, bd + (uint64_t)(blk * (kChunk >> 4) + 2 * k), idesc,
-                   (blk | k) != 0);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ts(tS, tQ + kTQpe + 8 * k, bd + (uint64_t)(8 * (kChunk >> 4) + 2 * k), idesc, 1);
+            mma_ts_t<T>(tS, tQ + G::kTQpe + 8 * k, bd + (uint64_t)(8 * (kChunk >> 4) + 2 * k), idesc, 1);
+        }
         mma_commit_addr(kempty + 8 * slot);
         mma_commit(&b->s_full[sbuf]);
       }
@@ -528,10 +622,12 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
 
 // Ships each superblock's staged P tiles and header into the value CTA once the
 // value CTA has freed the matching ring slots.
+template <typename T>
 __device__ void score_copier(const FwdArgs &a, uint8_t *smem, const Ctx &c, int part) {
+  using G = GeoOf<T>;
   Bars *b = c.bars;
-  const uint32_t peer_pring = map_to_rank(smem_u32(smem + kOffPRing), 1);
-  const uint32_t peer_hdr = map_to_rank(smem_u32(smem + kOffHdr), 1);
+  const uint32_t peer_pring = map_to_rank(smem_u32(smem + G::kOffPRing), 1);
+  const uint32_t peer_hdr = map_to_rank(smem_u32(smem + G::kOffHdr), 1);
   const uint32_t peer_pfull = map_to_rank(smem_u32(&b->p_full[0]), 1);
   const uint32_t peer_hfull = map_to_rank(smem_u32(&b->hdr_full[0]), 1);
   uint32_t pc = 0;  // P tiles shipped so far (staging tile pc % kStageTiles, ring slot pc % kNPR)
@@ -545,14 +641,14 @@ __device__ void score_copier(const FwdArgs &a, uint8_t *smem, const Ctx &c, int 
     // the header first: the value CTA can prepare O for this superblock while it
     // is still consuming the previous one's tiles
     if (leader)
-      bulk_copy_to_peer(peer_hdr + buf * sizeof(Header), smem + kOffHdrStage + buf * sizeof(Header),
+      bulk_copy_to_peer(peer_hdr + buf * sizeof(Header), smem + G::kOffHdrStage + buf * sizeof(Header),
                         sizeof(Header), peer_hfull + buf * 8);
     for (int t = 0; t < np; ++t, ++pc) {
       const uint32_t r = pc % kNPR, use = pc / kNPR;
       if (use > 0 && !wait_bar<true>(c, &b->slot_free[r], (use - 1) & 1, W_SLOT_FREE)) return;
       if (leader)
-        bulk_copy_to_peer(peer_pring + r * kPTile, smem + kOffPStage + (pc % kStageTiles) * kPTile,
-                          kPTile, peer_pfull + r * 8);
+        bulk_copy_to_peer(peer_pring + r * G::kPTile, smem + G::kOffPStage + (pc % kStageTiles) * G::kPTile,
+                          G::kPTile, peer_pfull + r * 8);
     }
     w.advance(a);
     ++sb;
@@ -562,6 +658,7 @@ __device__ void score_copier(const FwdArgs &a, uint8_t *smem, const Ctx &c, int 
 template <typename T>
 __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int part,
                               uint32_t tmem, int head0) {
+  using G = GeoOf<T>;
   Bars *b = c.bars;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sw = warp - 2;             // 0..7
@@ -574,7 +671,7 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
   // sees q_len - 1 - qi fewer cached tokens than the sequence holds
   const int hidden = (a.causal && head_ok) ? a.q_len - 1 - head / a.heads : 0;
   const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
-  float *red_max = reinterpret_cast<float *>(smem + kOffRed);  // [2][128]
+  float *red_max = reinterpret_cast<float *>(smem + G::kOffRed);  // [2][128]
   float *red_sum = red_max + 256;                               // [2][128] fp32 weights
   float *red_sumr = red_max + 512;                              // [2][128] 16-bit weights
   const float scale = a.scale_log2;
@@ -665,30 +762,53 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
 #pragma unroll
       for (int e = 0; e < 4; ++e) pr[e] = 0.f;
       const bool write = ok && half < np;
-      const uint32_t row = smem_u32(smem + kOffPStage + tb * kPTile) + r * 128;
       // a row that has seen no token yet (causal rows only) has m_ref = -inf: its
       // weights are exp2(-inf) = 0, not exp2(-inf + inf)
       const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
+      if constexpr (kIsF8<T>) {
+        // e4m3 tile: 64 bytes per row, 16-byte piece ch (tokens 16 ch ..) at
+        // ch ^ ((row >> 1) & 3) (the 64-byte swizzle).  The weights are at most
+        // 2^kTau = 256 < 448, the largest e4m3 value.
+        const uint32_t row = smem_u32(smem + G::kOffPStage + tb * G::kPTile) + r * 64;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        float p[8];
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t u[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = fast_exp2(fmaf(__uint_as_float(v[ch >> 2][(ch & 3) * 8 + e]), sc, nm));
-          ps[e] += p[e];
+          for (int q = 0; q < 4; ++q) {
+            float p[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              p[e] = fast_exp2(fmaf(__uint_as_float(v[ch >> 1][(ch & 1) * 16 + 4 * q + e]), sc, nm));
+              ps[(4 * q + e) & 7] += p[e];
+            }
+            u[q] = pack_e4m3x4(p[0], p[1], p[2], p[3]);
+            pr[q] += sum_e4m3x4(u[q]);
+          }
+          if (write) st_shared_v4(row + ((ch ^ ((r >> 1) & 3)) << 4), u[0], u[1], u[2], u[3]);
         }
-        uint32_t u[4];
+      } else {
+        const uint32_t row = smem_u32(smem + G::kOffPStage + tb * G::kPTile) + r * 128;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          u[e] = Pack<T>::two(p[2 * e], p[2 * e + 1]);
-          pr[e] += Pack<T>::sum(u[e]);
+        for (int ch = 0; ch < 8; ++ch) {
+          float p[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            p[e] = fast_exp2(fmaf(__uint_as_float(v[ch >> 2][(ch & 3) * 8 + e]), sc, nm));
+            ps[e] += p[e];
+          }
+          uint32_t u[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            u[e] = Pack<T>::two(p[2 * e], p[2 * e + 1]);
+            pr[e] += Pack<T>::sum(u[e]);
+          }
+          if (write) st_shared_v4(row + ((ch ^ (r & 7)) << 4), u[0], u[1], u[2], u[3]);
         }
-        if (write) st_shared_v4(row + ((ch ^ (r & 7)) << 4), u[0], u[1], u[2], u[3]);
       }
       red_sum[half * 128 + r] = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       red_sumr[half * 128 + r] = (pr[0] + pr[1]) + (pr[2] + pr[3]);
       const int hs = sb & 1;
-      Header *hdr = reinterpret_cast<Header *>(smem + kOffHdrStage + hs * sizeof(Header));
+      Header *hdr = reinterpret_cast<Header *>(smem + G::kOffHdrStage + hs * sizeof(Header));
       if (ok && half == 0 && sb >= 2)
         ok = wait_bar<true>(c, &b->hdr_free[hs], ((sb >> 1) - 1) & 1, W_HDR_FREE);
       if (bar_red_or(1, 256, !ok || c.aborted())) return;
@@ -726,6 +846,7 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
 template <typename T>
 __device__ void value_producer(const FwdArgs &a, const CUtensorMap *map4, uint8_t *smem,
                                const Ctx &c, int part) {
+  using G = GeoOf<T>;
   Bars *b = c.bars;
   uint32_t vc = 0;
   const bool leader = elect_one();
@@ -740,13 +861,13 @@ __device__ void value_producer(const FwdArgs &a, const CUtensorMap *map4, uint8_
 #pragma unroll
       for (int p = 0; p < kSB; ++p) {
         if (p >= j.np) break;
-        const uint32_t slot = vc % kNV, use = vc / kNV;
+        const uint32_t slot = vc % G::kNV, use = vc / G::kNV;
         ++vc;
         if (use > 0 && !wait_bar<false>(c, &b->v_empty[slot], (use - 1) & 1, W_V_EMPTY)) return false;
         if (leader) {
-          mbar_arrive_expect_tx(&b->v_full[slot], kVSlot);
-          tma_load_4d(smem + kOffV + slot * kVSlot, map4, &b->v_full[slot], 0, j.pg.row0[p], 4 * g,
-                      j.pg.page[p]);
+          mbar_arrive_expect_tx(&b->v_full[slot], G::kVSlot);
+          tma_load_4d(smem + G::kOffV + slot * G::kVSlot, map4, &b->v_full[slot], 0, j.pg.row0[p],
+                      G::kVAtoms * g, j.pg.page[p]);
         }
       }
     }
@@ -767,13 +888,13 @@ __device__ void value_producer(const FwdArgs &a, const CUtensorMap *map4, uint8_
   }
 }
 
-// Rows [r0, r1) of a V tile (four 64-column boxes) set to zero, for the MMA
-// that reads them (once per segment end, so kept out of line).
-__device__ __noinline__ void zero_rows(uint8_t *vs, int r0, int r1) {
+// Rows [r0, r1) of a V tile (`atoms` [64 rows x 128 B] boxes) set to zero, for
+// the MMA that reads them (once per segment end, so kept out of line).
+__device__ __noinline__ void zero_rows(uint8_t *vs, int atoms, int r0, int r1) {
 #pragma unroll 1
   for (int row = r0; row < r1; ++row)
 #pragma unroll 1
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < atoms; ++i)
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) st_shared_v4(smem_u32(vs + i * kChunk + row * 128 + ch * 16), 0, 0, 0, 0);
   fence_proxy_async_smem();
@@ -783,10 +904,15 @@ __device__ __noinline__ void zero_rows(uint8_t *vs, int r0, int r1) {
 // and the loop only advances counters and descriptors between MMAs.
 template <typename T>
 __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int part, uint32_t tmem) {
+  using G = GeoOf<T>;
   Bars *b = c.bars;
-  const uint32_t idesc = idesc_f16(128, 256, Pack<T>::kBf16, false, true);
-  const uint64_t pdesc = desc_kmajor_sw128(smem_u32(smem + kOffPRing));
-  const uint64_t vdesc = desc_mnmajor_sw128(smem_u32(smem + kOffV), 8192, 1024);
+  const uint32_t idesc = idesc_f16(128, 256, kFmtBit<T>, false, true);
+  // P: K-major, 32 bytes of each row per K step in either width; V: N-major,
+  // [64 rows x 128 B] atoms 8 KB apart, K step = G::kKStep rows of 128 B
+  const uint64_t pdesc = kIsF8<T> ? desc_kmajor_sw64(smem_u32(smem + G::kOffPRing))
+                                  : desc_kmajor_sw128(smem_u32(smem + G::kOffPRing));
+  const uint64_t vdesc = desc_mnmajor_sw128(smem_u32(smem + G::kOffV), 8192, 1024);
+  constexpr int kSteps = 64 / G::kKStep;
   const uint32_t vfull = smem_u32(&b->v_full[0]), vempty = smem_u32(&b->v_empty[0]);
   const uint32_t pfull = smem_u32(&b->p_full[0]), sfree = smem_u32(&b->slot_free[0]);
   uint32_t vslot = 0, vphase = 0;  // V ring position of the next tile and its v_full parity
@@ -811,23 +937,26 @@ __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
 #pragma unroll 1
         for (int p = 0; p < np; ++p) {
           const int valid = min(64, s.L - ((sb0 + p) << 6));
-          const int ksteps = (valid + 15) >> 4;
+          const int ksteps = (valid + G::kKStep - 1) / G::kKStep;
           if (g == 0 && !wait_addr<true>(c, pfull + 8 * r, rph, W_P_FULL)) return;
           if (!wait_addr<false>(c, vfull + 8 * vslot, vphase, W_V_FULL)) return;
-          if (leader && (valid & 15)) zero_rows(smem + kOffV + vslot * kVSlot, valid, ksteps * 16);
+          if (leader && (valid % G::kKStep))
+            zero_rows(smem + G::kOffV + vslot * G::kVSlot, G::kVAtoms, valid, ksteps * G::kKStep);
           tc_fence_after();
-          const uint64_t pd = pdesc + (uint64_t)(r * (kPTile >> 4));
-          const uint64_t vd = vdesc + (uint64_t)(vslot * (kVSlot >> 4));
+          const uint64_t pd = pdesc + (uint64_t)(r * (G::kPTile >> 4));
+          const uint64_t vd = vdesc + (uint64_t)(vslot * (G::kVSlot >> 4));
           const uint32_t acc0 = (first >> g) & 1u ? 0u : 1u;
           if (leader) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              if (k < ksteps) mma_ss(tmem + 256 * g, pd + 2 * k, vd + 128 * k, idesc, k == 0 ? acc0 : 1u);
+            for (int k = 0; k < kSteps; ++k)
+              if (k < ksteps)
+                mma_ss_t<T>(tmem + 256 * g, pd + 2 * k, vd + (uint64_t)((G::kKStep * 128 >> 4) * k), idesc,
+                            k == 0 ? acc0 : 1u);
             mma_commit_addr(vempty + 8 * vslot);
             if (g == 1) mma_commit_multicast_addr(sfree + 8 * r, 1);  // P tile fully used
           }
           first &= ~(1u << g);
-          if (++vslot == kNV) {
+          if (++vslot == G::kNV) {
             vslot = 0;
             vphase ^= 1u;
           }
@@ -849,7 +978,9 @@ __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
 
 // Arms each incoming P tile's barrier and tells the score CTA as soon as the copy
 // has landed, so it can reuse the staging tile.
+template <typename T>
 __device__ void value_receiver(const FwdArgs &a, const Ctx &c, int part) {
+  using G = GeoOf<T>;
   Bars *b = c.bars;
   uint32_t pc = 0;  // P tiles received so far
   const bool leader = elect_one();
@@ -858,7 +989,7 @@ __device__ void value_receiver(const FwdArgs &a, const Ctx &c, int part) {
     const int np = min(kSB, w.s.hi - w.sb0);
     for (int t = 0; t < np; ++t, ++pc) {
       const uint32_t r = pc % kNPR;
-      if (leader) mbar_arrive_expect_tx(&b->p_full[r], kPTile);
+      if (leader) mbar_arrive_expect_tx(&b->p_full[r], G::kPTile);
       if (!wait_bar<true>(c, &b->p_full[r], (pc / kNPR) & 1, W_P_FULL)) return;
       if (leader) mbar_arrive_cluster(&b->stage_free[pc % kStageTiles], 0);
     }
@@ -878,7 +1009,9 @@ __device__ void value_receiver(const FwdArgs &a, const Ctx &c, int part) {
 template <typename T>
 __device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int nsplit, int head,
                                        bool head_ok, int g, uint32_t tO, float lrow, uint32_t epi) {
-  const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+  using O = OutT<T>;
+  // o_scale: the value dequantisation scale (e4m3 caches), 1 otherwise
+  const float inv = lrow > 0.f ? a.o_scale / lrow : 0.f;
   const int lane = threadIdx.x & 31;
   const int row0 = head - lane;  // the warp's first row
   if (nsplit != 1) {
@@ -912,15 +1045,15 @@ __device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int
     tmem_ld32(tO + 64 * i + 32, w[1]);
     tmem_wait_ld();
     {
-      T *o = reinterpret_cast<T *>(a.out) + (int64_t)seq * a.o_batch_stride + 256 * g + 64 * i;
+      O *o = reinterpret_cast<O *>(a.out) + (int64_t)seq * a.o_batch_stride + 256 * g + 64 * i;
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float *f = reinterpret_cast<const float *>(&w[t][8 * j]);
-          st_shared_v4(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), Pack<T>::two(f[0] * inv, f[1] * inv),
-                       Pack<T>::two(f[2] * inv, f[3] * inv), Pack<T>::two(f[4] * inv, f[5] * inv),
-                       Pack<T>::two(f[6] * inv, f[7] * inv));
+          st_shared_v4(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), Pack<O>::two(f[0] * inv, f[1] * inv),
+                       Pack<O>::two(f[2] * inv, f[3] * inv), Pack<O>::two(f[4] * inv, f[5] * inv),
+                       Pack<O>::two(f[6] * inv, f[7] * inv));
         }
         __syncwarp();
 #pragma unroll
@@ -940,7 +1073,7 @@ __device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int
 template <typename T>
 __device__ __noinline__ void zero_out(const FwdArgs &a, int seq, int split, int nsplit, int head, int g) {
   if (nsplit == 1) {
-    uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(a.out) + (int64_t)seq * a.o_batch_stride +
+    uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<OutT<T> *>(a.out) + (int64_t)seq * a.o_batch_stride +
                                          (int64_t)head * a.o_head_stride + 256 * g);
     for (int i = 0; i < 32; ++i) o[i] = make_uint4(0, 0, 0, 0);
   } else {
@@ -952,6 +1085,7 @@ __device__ __noinline__ void zero_out(const FwdArgs &a, int seq, int split, int 
 template <typename T>
 __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, int part,
                                  uint32_t tmem, int head0) {
+  using G = GeoOf<T>;
   Bars *b = c.bars;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sw = warp - 2;
@@ -984,7 +1118,7 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
       const int hs = sb & 1;
       if (sw == 0 && lane == 0) mbar_arrive_expect_tx(&b->hdr_full[hs], sizeof(Header));
       bool ok = wait_bar<true>(c, &b->hdr_full[hs], (sb >> 1) & 1, W_HDR_FULL);
-      const Header *hdr = reinterpret_cast<const Header *>(smem + kOffHdr + hs * sizeof(Header));
+      const Header *hdr = reinterpret_cast<const Header *>(smem + G::kOffHdr + hs * sizeof(Header));
       const uint32_t flags = hdr->flags;
       const float alpha = hdr->alpha[r];
       const float lrow = hdr->l[r];
@@ -1021,7 +1155,7 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
         if (bar_red_or(bar_id, 128, !ok || c.aborted())) return;
         tc_fence_after();
         write_out<T>(a, s.seq, s.split, s.nsplit, head, head_ok, g, tO, lrow,
-                     smem_u32(smem + kOffEpi + (warp - 2) * 2048));
+                     smem_u32(smem + G::kOffEpi + (warp - 2) * 2048));
         tc_fence_before();
         mbar_arrive(&b->o_free);
       }
@@ -1037,17 +1171,18 @@ split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant
                 const __grid_constant__ CUtensorMap kpe_map,
                 const __grid_constant__ CUtensorMap qpe_map,
                 const __grid_constant__ CUtensorMap kv4_map, const FwdArgs a) {
+  using G = GeoOf<T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  Bars *b = reinterpret_cast<Bars *>(smem + kOffBars);
+  Bars *b = reinterpret_cast<Bars *>(smem + G::kOffBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t role = cluster_ctarank();  // 0: score CTA, 1: value CTA
   const int part = blockIdx.x >> 1;
   const int head0 = blockIdx.y * 128;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNK; ++i) {
+    for (int i = 0; i < G::kNK; ++i) {
       mbar_init(&b->k_full[i], 1);
       mbar_init(&b->k_empty[i], 1);
     }
@@ -1072,7 +1207,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant
       mbar_init(&b->slot_free[i], 1);
       mbar_init(&b->p_full[i], 1);
     }
-    for (int i = 0; i < kNV; ++i) {
+    for (int i = 0; i < G::kNV; ++i) {
       mbar_init(&b->v_full[i], 1);
       mbar_init(&b->v_empty[i], 1);
     }
@@ -1118,7 +1253,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant
     } else if (warp < 10) {
       score_softmax<T>(a, smem, c, part, tmem, head0);
     } else {
-      if (loads) score_copier(a, smem, c, part);
+      if (loads) score_copier<T>(a, smem, c, part);
     }
   } else {
     // warp 0: V producer, 1: MMA, 2-5 / 6-9: correction and epilogue of O half 0 / 1,
@@ -1130,7 +1265,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant
     } else if (warp < 10) {
       value_correction<T>(a, smem, c, part, tmem, head0);
     } else {
-      value_receiver(a, c, part);
+      value_receiver<T>(a, c, part);
     }
   }
 
@@ -1166,21 +1301,28 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// One 3-D tiled map over a [outer][mid][cols] 16-bit tensor (strides in elements),
-// 128-byte swizzle, zero fill past the extents.
+template <typename T>
+constexpr CUtensorMapDataType map_dtype() {
+  return kIsF8<T> ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                  : (std::is_same<T, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+}
+
+// One 3-D tiled map over a [outer][mid][cols] tensor of T (strides in elements),
+// boxes of box_cols x box_mid, 128-byte swizzle, zero fill past the extents.
 template <typename T>
 cudaError_t make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t mid, uint64_t outer,
-                     int64_t mid_stride, int64_t outer_stride, uint32_t box_mid) {
+                     int64_t mid_stride, int64_t outer_stride, uint32_t box_cols, uint32_t box_mid) {
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
+  constexpr uint64_t es = sizeof(T);
   cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)mid, (cuuint64_t)outer};
-  cuuint64_t strides[2] = {(cuuint64_t)mid_stride * 2, (cuuint64_t)outer_stride * 2};
-  cuuint32_t box[3] = {64, box_mid, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(m, Pack<T>::kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                   3, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  cuuint64_t strides[2] = {(cuuint64_t)mid_stride * es, (cuuint64_t)outer_stride * es};
+  cuuint32_t box[3] = {box_cols, box_mid, 1};
+  cuuint32_t el[3] = {1, 1, 1};
+  CUresult r = enc(m, map_dtype<T>(), 3, const_cast<void *>(base), dims, strides, box, el,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -1198,26 +1340,28 @@ cudaError_t smem_attr() {
   if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
   std::lock_guard<std::mutex> lk(mu);
   if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
-  e = cudaFuncSetAttribute(split_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  e = cudaFuncSetAttribute(split_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           GeoOf<T>::kSmemBytes);
   if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
   return e;
 }
 
-// A 4-D tiled map over the cache's rows as [pages][64-column blocks][page rows]
-// [64 columns] (block stride 128 B, so a box of several blocks lands as that many
-// swizzled [64 rows x 64 columns] atoms back to back).
+// A 4-D tiled map over the cache's rows as [pages][column blocks][page rows]
+// [block_cols columns] (block stride block_cols elements, so a box of several
+// blocks lands as that many swizzled [64 rows x block] atoms back to back).
 template <typename T>
-cudaError_t make_block_map(CUtensorMap *m, const void *base, uint64_t blocks, uint32_t box_blocks,
-                           const FwdArgs &a) {
+cudaError_t make_block_map(CUtensorMap *m, const void *base, uint32_t block_cols, uint64_t blocks,
+                           uint32_t box_blocks, CUtensorMapSwizzle swizzle, const FwdArgs &a) {
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  cuuint64_t dims[4] = {64, (cuuint64_t)a.page_size, blocks, (cuuint64_t)a.num_pages};
-  cuuint64_t strides[3] = {(cuuint64_t)a.kv_row_stride * 2, 128, (cuuint64_t)a.kv_page_stride * 2};
-  cuuint32_t box[4] = {64, 64, box_blocks, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = enc(m, Pack<T>::kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                   4, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  constexpr uint64_t es = sizeof(T);
+  cuuint64_t dims[4] = {block_cols, (cuuint64_t)a.page_size, blocks, (cuuint64_t)a.num_pages};
+  cuuint64_t strides[3] = {(cuuint64_t)a.kv_row_stride * es, block_cols * es,
+                           (cuuint64_t)a.kv_page_stride * es};
+  cuuint32_t box[4] = {block_cols, 64, box_blocks, 1};
+  cuuint32_t el[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, map_dtype<T>(), 4, const_cast<void *>(base), dims, strides, box, el,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -1225,27 +1369,45 @@ cudaError_t make_block_map(CUtensorMap *m, const void *base, uint64_t blocks, ui
 template <typename T>
 cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
   constexpr uint64_t kLatent = MLA_HEAD_DIM_V, kRope = MLA_HEAD_DIM - MLA_HEAD_DIM_V;
-  // K: one box per page over all nine 64-column blocks of a 576-column row, or,
-  // with K_pe separate, the eight latent blocks plus a [64 rows x 64] K_pe box.
-  // V: the latent blocks again, four per box (one O half of one page).
-  // Q and Q_pe as [b][h][cols], boxes of 128 heads x 64 columns (rows past h read
-  // as zeros).
   CUtensorMap kmap, qmap, pemap, qpemap, map4;
-  cudaError_t e = make_block_map<T>(&kmap, a.kv, a.k_fused ? 9 : 8, a.k_fused ? 9 : 8, a);
-  if (e == cudaSuccess) e = make_block_map<T>(&map4, a.kv, kLatent / 64, 4, a);
-  if (e == cudaSuccess)
-    e = make_map<T>(&pemap, a.k_pe, kRope, a.page_size, a.num_pages, a.k_pe_row_stride,
-                    a.k_pe_page_stride, 64);
-  if (e == cudaSuccess)
-    e = make_map<T>(&qmap, a.q, kLatent, a.h, a.b, a.q_head_stride, a.q_batch_stride, 128);
-  if (e == cudaSuccess)
-    e = make_map<T>(&qpemap, a.q_pe, kRope, a.h, a.b, a.q_pe_head_stride, a.q_pe_batch_stride, 128);
+  cudaError_t e;
+  if constexpr (kIsF8<T>) {
+    // e4m3, RoPE columns inside the rows (the host rejects separate tensors).
+    // K: one box per page of nine [64 rows x 64 B] blocks, 64-byte swizzle.  V: the
+    // first four 128-byte blocks, two per box (one O half of one page).  Q as
+    // [b][h][576 B], boxes of 128 heads x 128 B; the RoPE box starts at column 512
+    // and reads zeros past column 575.
+    e = make_block_map<T>(&kmap, a.kv, 64, 9, 9, CU_TENSOR_MAP_SWIZZLE_64B, a);
+    if (e == cudaSuccess) e = make_block_map<T>(&map4, a.kv, 128, 4, 2, CU_TENSOR_MAP_SWIZZLE_128B, a);
+    if (e == cudaSuccess)
+      e = make_map<T>(&qmap, a.q, MLA_HEAD_DIM, a.h, a.b, a.q_head_stride, a.q_batch_stride, 128, 128);
+    qpemap = qmap;
+    pemap = kmap;  // unused
+  } else {
+    // K: one box per page over all nine 64-column blocks of a 576-column row, or,
+    // with K_pe separate, the eight latent blocks plus a [64 rows x 64] K_pe box.
+    // V: the latent blocks again, four per box (one O half of one page).  Q and
+    // Q_pe as [b][h][cols], boxes of 128 heads x 64 columns (rows past h read as
+    // zeros).
+    e = make_block_map<T>(&kmap, a.kv, 64, a.k_fused ? 9 : 8, a.k_fused ? 9 : 8,
+                          CU_TENSOR_MAP_SWIZZLE_128B, a);
+    if (e == cudaSuccess)
+      e = make_block_map<T>(&map4, a.kv, 64, kLatent / 64, 4, CU_TENSOR_MAP_SWIZZLE_128B, a);
+    if (e == cudaSuccess)
+      e = make_map<T>(&pemap, a.k_pe, kRope, a.page_size, a.num_pages, a.k_pe_row_stride,
+                      a.k_pe_page_stride, 64, 64);
+    if (e == cudaSuccess)
+      e = make_map<T>(&qmap, a.q, kLatent, a.h, a.b, a.q_head_stride, a.q_batch_stride, 64, 128);
+    if (e == cudaSuccess)
+      e = make_map<T>(&qpemap, a.q_pe, kRope, a.h, a.b, a.q_pe_head_stride, a.q_pe_batch_stride, 64,
+                      128);
+  }
   if (e != cudaSuccess) return e;
   if ((e = smem_attr<T>()) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * a.num_parts, (a.h + 127) / 128, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = GeoOf<T>::kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1262,7 +1424,12 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_split_tc(const FwdArgs &a, cudaStream_t s) {
-  return a.dtype == MLA_DTYPE_BF16 ? launch_typed<__nv_bfloat16>(a, s) : launch_typed<__half>(a, s);
+  switch (a.dtype) {
+    case MLA_DTYPE_BF16: return launch_typed<__nv_bfloat16>(a, s);
+    case MLA_DTYPE_FP16: return launch_typed<__half>(a, s);
+    case MLA_DTYPE_E4M3: return launch_typed<__nv_fp8_e4m3>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t split_tc_num_sm(int device, int *num_sm) {
@@ -1276,7 +1443,7 @@ cudaError_t split_tc_num_sm(int device, int *num_sm) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * 256, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = GeoOf<__nv_bfloat16>::kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;

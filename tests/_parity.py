@@ -21,6 +21,20 @@ addition, wherever the output format can hold the values to the bar (every
 |gpu - ref| must meet max 2e-2 and mean 2e-3 too.  The log records the plain
 error, the weighted one and the error beyond the output format's rounding.
 
+e4m3 cache (bf16 out).  The weights are rounded to e4m3 before P.V (3 fraction
+bits: a relative error |d_t| <= 2^-4 for weights in e4m3's normal range) and O
+is divided by the sum of the rounded weights, so the kernel's output is
+sum_t w~_t v_t with w~_t = w_t (1 + d_t) / (1 + d_bar), d_bar = sum_t w_t d_t.
+Hence |w~_t - w_t| <= w_t * 2 * 2^-4 / (1 - 2^-4) and
+|gpu - ref| <= 0.1334 * w.  The bar adds the bf16 rounding of out (2^-9 |out|,
+|out| <= w) and fp32 accumulation (1e-4 w): max(e) <= E4M3_OUT_MAX = 0.136.  For
+the mean, with independent zero-mean rounding errors of rms at most
+2^-4 / sqrt(3), E|gpu - ref| <= 2 * 2^-4 / sqrt(3) * w, so mean(e) <= 0.072.
+The lse bar is the 16-bit one (the scores are exact products summed in fp32, and
+the lse uses the unrounded weights).  Where every weight is a power of two that
+e4m3 holds exactly, the rounding is exact and check_exact_weights holds the
+output to half a bf16 ulp plus 1e-4 * max(1, w).
+
 Whole workloads are compared in chunks of sequences, so that the host copy of
 the pages a chunk reads stays within a fixed budget.
 """
@@ -36,9 +50,17 @@ import workloads
 OUT_MAX_ABS = 2e-2
 OUT_MEAN_ABS = 2e-3
 LSE_MAX_ABS = 1e-3
+E4M3_OUT_MAX = 0.136
+E4M3_OUT_MEAN = 0.072
+EXACT_REL = 1e-4
 
 ORACLE_THREADS = max(1, min(32, os.cpu_count() or 1))
 HOST_KV_BUDGET = 1 << 30  # bytes of cache pages copied to the host per chunk
+
+
+def scales(inputs):
+    """The e4m3 dequantisation scales of a workload's inputs (1, 1 for 16-bit ones)."""
+    return dict(q_scale=inputs.get("q_scale", 1.0), kv_scale=inputs.get("kv_scale", 1.0))
 
 
 def run_gpu(inputs, heads, scale, num_sm=None, is_causal=False):
@@ -48,7 +70,7 @@ def run_gpu(inputs, heads, scale, num_sm=None, is_causal=False):
                                             seqlen_q=s_q)
     out, lse = mla.mla_decode_fwd(inputs["q"], inputs["kv_cache"], inputs["block_table"],
                                   inputs["cache_seqlens"], scale, meta, num_splits,
-                                  is_causal=is_causal)
+                                  is_causal=is_causal, **scales(inputs))
     code, detail = mla.mla_get_device_error()
     assert code == 0, f"device error {code} ({mla.mla_status_string(code)}), detail {detail}"
     return out, lse, meta, num_splits
@@ -77,7 +99,7 @@ def oracle_rows(w, inputs, seqs=None):
                     -1).reshape(-1, 2)
     out, lse, absw = oracle.decode_rows(q_c, kv_c, table_c, sl_c, w.softmax_scale, w.dtype, rows,
                                         threads=ORACLE_THREADS, with_abs=True,
-                                        seqlen_q=w.seqlen_q, is_causal=w.causal)
+                                        seqlen_q=w.seqlen_q, is_causal=w.causal, **scales(inputs))
     return (out.reshape(len(seqs), w.rows, -1), lse.reshape(len(seqs), w.rows),
             absw.reshape(len(seqs), w.rows, -1))
 
@@ -85,7 +107,7 @@ def oracle_rows(w, inputs, seqs=None):
 def seq_chunks(w, seqs, budget=HOST_KV_BUDGET):
     """Consecutive groups of `seqs` whose pages take at most `budget` bytes on the host
     (a sequence larger than the budget forms a group of its own)."""
-    page_bytes = w.page_size * workloads.D * 2
+    page_bytes = w.page_size * workloads.D * w.elem_bytes
     chunk, used = [], 0
     for s in seqs:
         b = max(1, w.blocks_per_seq[s]) * page_bytes
@@ -116,10 +138,12 @@ def representable_bar(dtype):
 
 class ErrorStats:
     """Running max and mean of the out error over every element compared (in units of
-    max(1, w); plain; beyond the output format's rounding), and the lse error."""
+    max(1, w); plain; beyond the output format's rounding), and the lse error.
+    dtype: the input dtype ("bf16", "fp16", "e4m3"); the output's is bf16 for e4m3."""
 
     def __init__(self, dtype):
-        self.dtype = dtype
+        self.in_dtype = dtype
+        self.dtype = "bf16" if dtype == "e4m3" else dtype
         self.w_max = 0.0        # |gpu - ref| / max(1, w)
         self.w_sum = 0.0
         self.raw_max = 0.0      # |gpu - ref|
@@ -167,19 +191,24 @@ class ErrorStats:
                f"{d['out_mean_weighted']:.3e}; beyond the {self.dtype} rounding: max "
                f"{d['out_max_beyond_format']:.3e}; |ref| up to {self.ref_max:.3g}); "
                f"lse {self.lse_max:.3e}; {self.rows} rows")
+        assert self.lse_max <= LSE_MAX_ABS, msg
+        if self.in_dtype == "e4m3":
+            assert d["out_max_weighted"] <= E4M3_OUT_MAX, msg
+            assert d["out_mean_weighted"] <= E4M3_OUT_MEAN, msg
+            return d
         assert d["out_max_weighted"] <= OUT_MAX_ABS, msg
         assert d["out_mean_weighted"] <= OUT_MEAN_ABS, msg
-        assert self.lse_max <= LSE_MAX_ABS, msg
         if self.ref_max < representable_bar(self.dtype):
             assert d["out_max_abs"] <= OUT_MAX_ABS, msg
             assert d["out_mean_abs"] <= OUT_MEAN_ABS, msg
         return d
 
 
-def compare(out_gpu, lse_gpu, out_ref, lse_ref, abs_ref, what=""):
+def compare(out_gpu, lse_gpu, out_ref, lse_ref, abs_ref, what="", in_dtype=None):
     """out_gpu [n, rows, 512] (bf16 or fp16), lse_gpu [n, rows]; refs float64 numpy
-    (abs_ref: the oracle's weighted-absolute scale of each output)."""
-    st = ErrorStats("bf16" if out_gpu.dtype == torch.bfloat16 else "fp16")
+    (abs_ref: the oracle's weighted-absolute scale of each output).  in_dtype: the
+    inputs' dtype when it is not the output's (e4m3)."""
+    st = ErrorStats(in_dtype or ("bf16" if out_gpu.dtype == torch.bfloat16 else "fp16"))
     st.add(out_gpu, lse_gpu, out_ref, lse_ref, abs_ref, what)
     return st.check(what)
 
@@ -220,3 +249,18 @@ def check_workload(w, seqs=None, num_sm=None, poison_tail=False, inputs=None):
     out, lse, meta, ns = run_gpu(inputs, w.heads, w.softmax_scale, num_sm, is_causal=w.causal)
     stats = compare_chunked(w, inputs, [("out", out, lse)], seqs)["out"]
     return stats, out, lse, meta, ns, inputs
+
+
+def check_exact_weights(out_gpu, lse_gpu, out_ref, lse_ref, abs_ref, what=""):
+    """e4m3 inputs whose softmax weights are all powers of two in e4m3's range, so
+    that rounding them is exact: |gpu - ref| <= half a bf16 ulp of the larger of
+    the two plus EXACT_REL * max(1, w) (fp32 accumulation), and the lse bar."""
+    og = out_gpu.float().cpu().numpy().astype(np.float64)
+    lg = lse_gpu.float().cpu().numpy().astype(np.float64)
+    raw = np.abs(og - out_ref)
+    bar = half_ulp(np.maximum(np.abs(og), np.abs(out_ref)), "bf16") + EXACT_REL * np.maximum(1.0, abs_ref)
+    worst = float((raw - bar).max(initial=-1.0))
+    lse_err = float(np.abs(lg - lse_ref).max(initial=0.0))
+    assert worst <= 0, f"{what}: exceeds the exact-weight bar by {worst:.3e} (max |err| {raw.max():.3e})"
+    assert lse_err <= LSE_MAX_ABS, f"{what}: lse {lse_err:.3e}"
+    return {"out_max_abs": float(raw.max(initial=0.0)), "lse_max_abs": lse_err}

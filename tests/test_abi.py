@@ -45,7 +45,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_params_struct_matches(lib):
     import mla_decode_gb300 as m
     assert lib.mla_fwd_params_size() == ctypes.sizeof(m.FwdParams)
-    assert lib.mla_abi_version() == m.ABI_VERSION == 3
+    assert lib.mla_abi_version() == m.ABI_VERSION == 4
 
 
 def test_status_strings(lib):
@@ -146,6 +146,31 @@ def test_split_layout_rejects(lib, fields, code):
 def test_query_tokens_rejects(lib, fields, code):
     """seqlen_q > 1: rows = seqlen_q * h size lse and the workspace; at most 1024 rows."""
     p = good_params()
+    for k, v in fields.items():
+        setattr(p, k, v)
+    assert lib.mla_decode_fwd(ctypes.byref(p), None) == code
+
+
+def e4m3_params():
+    p = good_params()
+    p.dtype, p.q_scale, p.kv_scale = 2, 0.5, 2.0
+    return p
+
+
+@pytest.mark.parametrize("fields,code", [
+    ({}, -6),                                                  # valid up to the (small) workspace
+    ({"q_scale": 0.0}, -3), ({"kv_scale": -1.0}, -3),
+    ({"q_scale": float("nan")}, -3), ({"kv_scale": float("inf")}, -3),
+    ({**SEP_K}, -3), ({**SEP_Q}, -3),                          # fused layout only
+    ({"q_head_stride": 584}, -4),                              # 8 bytes: not a multiple of 16
+    ({"kv_row_stride": 584, "kv_page_stride": 64 * 584}, -4),
+    ({"kv_page_stride": 64 * 576 + 8}, -4),
+    ({"o_head_stride": 516}, -4),                              # bf16 out: 8 elements
+])
+def test_e4m3_validation(lib, fields, code):
+    """e4m3: finite positive scales, the fused layout, strides of 16 bytes."""
+    p = e4m3_params()
+    p.workspace_bytes = 100
     for k, v in fields.items():
         setattr(p, k, v)
     assert lib.mla_decode_fwd(ctypes.byref(p), None) == code

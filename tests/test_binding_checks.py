@@ -30,7 +30,7 @@ def call(mla, t, **kw):
 @pytest.mark.parametrize("kw,t_kw,match", [
     ({}, dict(q_cols=512), r"q must be \[b, s, h, 576\]"),
     ({}, dict(kv_cols=512), r"kv_cache must be"),
-    ({}, dict(dtype=torch.float32), r"fp16 or bf16"),
+    ({}, dict(dtype=torch.float32), r"fp16, bf16 or float8_e4m3fn"),
     ({"q_pe": torch.zeros(2, 1, 16, 64, dtype=torch.bfloat16)}, {}, r"q must be \[b, s, h, 512\]"),
     ({"k_pe": torch.zeros(4, 64, 1, 64, dtype=torch.bfloat16)}, {}, r"kv_cache must be .*512"),
 ])
@@ -57,6 +57,21 @@ def test_query_token_shape_of_q_pe(mla):
     t = tensors(s=2, q_cols=512)
     with pytest.raises(ValueError, match=r"q_pe must be \[b, s, h, 64\]"):
         call(mla, t, q_pe=torch.zeros(2, 1, 16, 64, dtype=torch.bfloat16))
+
+
+def test_e4m3_checks(mla):
+    t = tensors(dtype=torch.float8_e4m3fn)
+    # the e4m3 cache keeps its RoPE columns inside the rows
+    with pytest.raises(ValueError, match=r"RoPE columns inside"):
+        call(mla, tensors(q_cols=512, dtype=torch.float8_e4m3fn),
+             q_pe=torch.zeros(2, 1, 16, 64, dtype=torch.float8_e4m3fn))
+    # q and the cache share the dtype
+    t["kv_cache"] = torch.zeros(4, 64, 1, 576, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match=r"must share dtype"):
+        call(mla, t)
+    # e4m3 gives bf16 outputs
+    assert mla.out_dtype(torch.float8_e4m3fn) == torch.bfloat16
+    assert mla.out_dtype(torch.float16) == torch.float16
 
 
 def test_host_tensors_are_refused(mla):

@@ -2,7 +2,8 @@
 
 This module only draws inputs: it holds none of the method's arithmetic.  Both
 the CUDA path and the CPU oracle consume exactly the tensors built here (the
-oracle gets host copies of the same stored 16-bit values).
+oracle gets host copies of the same stored values: 16-bit patterns, or e4m3
+bytes and their two scales).
 
 Shapes follow the pages' decode workloads: one query token per sequence,
 h query heads, one latent KV head, rows of 576 = 512 latent + 64 RoPE, a cache
@@ -18,6 +19,11 @@ Value recipe (all seeded):
   * table entries past a sequence's last block are -1 (never read);
   * cache_seqlens are given or drawn from a numpy PCG64 stream (platform
     independent).
+  * e4m3 workloads (an FP8 cache with one dequantisation scale per tensor): q and
+    the cache are drawn the same way in fp32, then quantised per tensor with
+    scale = amax / 448 (448 is e4m3's largest finite value) as
+    stored = e4m3(x / scale), rounded to nearest even; the draws are made twice
+    from the same generator state (amax first, then the quantisation).
 """
 from dataclasses import dataclass, replace
 
@@ -35,7 +41,7 @@ class Workload:
     batch: int
     heads: int
     seqlens: tuple          # per-sequence cache length
-    dtype: str              # "bf16" | "fp16"
+    dtype: str              # "bf16" | "fp16" | "e4m3"
     page_size: int = 64
     softmax_scale: float = 192 ** -0.5
     seed: int = 0
@@ -57,7 +63,18 @@ class Workload:
 
     @property
     def torch_dtype(self):
-        return torch.bfloat16 if self.dtype == "bf16" else torch.float16
+        return {"bf16": torch.bfloat16, "fp16": torch.float16,
+                "e4m3": torch.float8_e4m3fn}[self.dtype]
+
+    @property
+    def elem_bytes(self):
+        """Bytes per stored q / cache element."""
+        return 1 if self.dtype == "e4m3" else 2
+
+    @property
+    def out_dtype(self):
+        """Format of the output: the input's, bf16 for an e4m3 cache."""
+        return "bf16" if self.dtype == "e4m3" else self.dtype
 
     @property
     def blocks_per_seq(self):
@@ -82,9 +99,9 @@ class Workload:
         return float(self.heads) * pairs * 2 * (D + DV)
 
     def bytes(self):
-        """Algorithmic bytes: KV rows (token granular) + Q + O."""
-        esz = 2
-        return float(self.total_tokens * D * esz + self.batch * self.rows * (D + DV) * esz)
+        """Algorithmic bytes: KV rows (token granular) + Q + O (O is 16-bit)."""
+        esz = self.elem_bytes
+        return float(self.total_tokens * D * esz + self.batch * self.rows * (D * esz + DV * 2))
 
 
 def _varlen_lengths(batch, lo, hi, seed):
@@ -119,6 +136,10 @@ def configs():
         # paged shape with two causal query tokens, 256 query rows per sequence
         "mtp": Workload("mtp", 64, 128, (4096,) * 64, "bf16", page_size=64,
                         softmax_scale=192 ** -0.5, seed=7, seqlen_q=2, causal=True),
+        # the paged shape with an FP8 cache: q and the cache in e4m3 with one
+        # dequantisation scale per tensor, bf16 out
+        "paged_fp8": Workload("paged_fp8", 64, 128, (4096,) * 64, "e4m3", page_size=64,
+                              softmax_scale=192 ** -0.5, seed=21),
         # the TileLang guide's own command lines (section 如何运行、验证与基准测试):
         # example_mla_decode.py defaults (contiguous cache, fp16 as in its comparison);
         # its example_mla_decode_paged.py line is the "split" workload above
@@ -146,16 +167,55 @@ def custom(batch, heads, seqlens, dtype="bf16", page_size=64, softmax_scale=192 
                     softmax_scale, seed, shuffle, **kw)
 
 
-def _randn_into(out, gen, scale_rows=None):
-    """Fill `out` (any float dtype, contiguous) with N(0,1) drawn in fp32 chunks."""
+E4M3_MAX = 448.0
+
+
+def _fp32_rows(n_rows, gen, device, hot_frac=0.0, hot_mult=1.0):
+    """The fp32 draws of `n_rows` rows of 576, chunk by chunk (the same sequence of
+    generator calls as the 16-bit paths make)."""
+    if hot_frac > 0:
+        rows_per_chunk = max(1, _CHUNK // D)
+        pos = 0
+        while pos < n_rows:
+            m = min(rows_per_chunk, n_rows - pos)
+            x = torch.randn((m, D), generator=gen, device=device, dtype=torch.float32)
+            hot = torch.rand((m, 1), generator=gen, device=device) < hot_frac
+            yield torch.where(hot, x * hot_mult, x).view(-1)
+            pos += m
+    else:
+        n = n_rows * D
+        pos = 0
+        while pos < n:
+            m = min(_CHUNK, n - pos)
+            yield torch.randn(m, generator=gen, device=device, dtype=torch.float32)
+            pos += m
+
+
+def _round_into(out, gen, **draw):
+    """Fill the 16-bit tensor `out` (rows of 576) with the draws rounded to its dtype."""
     flat = out.view(-1)
-    n = flat.numel()
     pos = 0
-    while pos < n:
-        m = min(_CHUNK, n - pos)
-        x = torch.randn(m, generator=gen, device=out.device, dtype=torch.float32)
-        flat[pos:pos + m] = x.to(out.dtype)
-        pos += m
+    for x in _fp32_rows(out.numel() // D, gen, out.device, **draw):
+        flat[pos:pos + x.numel()] = x.to(out.dtype)
+        pos += x.numel()
+
+
+def _quantize_e4m3(out, gen, **draw):
+    """Fill the e4m3 tensor `out` (rows of 576) with per-tensor quantised draws;
+    returns the dequantisation scale (amax / 448, as an fp32 value)."""
+    state = gen.get_state()
+    n_rows = out.numel() // D
+    amax = 0.0
+    for x in _fp32_rows(n_rows, gen, out.device, **draw):
+        amax = max(amax, float(x.abs().max()))
+    scale = float(np.float32(amax / E4M3_MAX)) if amax > 0 else 1.0
+    gen.set_state(state)
+    flat = out.view(-1)
+    pos = 0
+    for x in _fp32_rows(n_rows, gen, out.device, **draw):
+        flat[pos:pos + x.numel()] = (x / scale).clamp_(-E4M3_MAX, E4M3_MAX).to(out.dtype)
+        pos += x.numel()
+    return scale
 
 
 def make_inputs(w: Workload, device="cpu", poison_tail=False):
@@ -168,6 +228,7 @@ def make_inputs(w: Workload, device="cpu", poison_tail=False):
       cache_seqlens int32 [b]
     poison_tail fills cache rows past each sequence's length (inside its last
     page) with NaN, to prove they are never read into the result.
+    e4m3 workloads add "q_scale" and "kv_scale" (floats).
     """
     device = torch.device(device)
     gen = torch.Generator(device=device)
@@ -176,24 +237,15 @@ def make_inputs(w: Workload, device="cpu", poison_tail=False):
     b, h, P = w.batch, w.heads, w.page_size
 
     q = torch.empty((b, w.seqlen_q, h, D), dtype=dt, device=device)
-    _randn_into(q, gen)
-
     kv = torch.empty((w.num_pages, P, 1, D), dtype=dt, device=device)
-    if w.hot_row_frac > 0:
-        # draw fp32 rows, scale the chosen ones, then round (chunked by pages)
-        rows_per_chunk = max(1, _CHUNK // D)
-        flat = kv.view(-1, D)
-        nrows = flat.shape[0]
-        pos = 0
-        while pos < nrows:
-            m = min(rows_per_chunk, nrows - pos)
-            x = torch.randn((m, D), generator=gen, device=device, dtype=torch.float32)
-            hot = torch.rand((m, 1), generator=gen, device=device) < w.hot_row_frac
-            x = torch.where(hot, x * w.hot_row_mult, x)
-            flat[pos:pos + m] = x.to(dt)
-            pos += m
+    hot = dict(hot_frac=w.hot_row_frac, hot_mult=w.hot_row_mult)
+    scales = {}
+    if w.dtype == "e4m3":
+        scales["q_scale"] = _quantize_e4m3(q, gen)
+        scales["kv_scale"] = _quantize_e4m3(kv, gen, **hot)
     else:
-        _randn_into(kv, gen)
+        _round_into(q, gen)
+        _round_into(kv, gen, **hot)
 
     # block table: seeded permutation of physical pages, or identity
     nb = w.blocks_per_seq
@@ -221,6 +273,7 @@ def make_inputs(w: Workload, device="cpu", poison_tail=False):
         "kv_cache": kv,
         "block_table": table.to(device),
         "cache_seqlens": seqlens.to(device),
+        **scales,
     }
 
 
@@ -240,5 +293,8 @@ def sample_seqs(w: Workload, n, seed=1234):
 
 
 def to_bits(t):
-    """Stored 16-bit patterns of a bf16/fp16 tensor as a numpy uint16 array (host)."""
+    """Stored bit patterns as a host numpy array: uint16 for bf16 / fp16, uint8 for
+    e4m3."""
+    if t.dtype == torch.float8_e4m3fn:
+        return t.detach().contiguous().view(torch.uint8).cpu().numpy()
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
