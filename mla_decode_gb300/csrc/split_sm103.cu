@@ -1,5 +1,7 @@
 // Split kernel for sm_103a: tcgen05 tensor cores, TMEM accumulators, TMA loads,
-// a 2-CTA cluster per scheduler part.
+// a 2-CTA cluster per scheduler part.  One template serves bf16 / fp16 inputs
+// (kind::f16 MMAs) and an e4m3 cache with per-tensor scales (kind::f8f6f4, bf16
+// out; the geometry differences are in Geo below).
 //
 // What it computes (per sequence segment and 128-row tile of query rows: heads,
 // or seqlen_q x heads token-major) is the TileLang
@@ -348,13 +350,23 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
   return lo | (hi << 16);
 }
-// The sum of four packed e4m3 values, as floats (the conversions are exact).
-__device__ __forceinline__ float sum_e4m3x4(uint32_t u) {
-  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(u & 0xffffu), __NV_E4M3);
-  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(u >> 16), __NV_E4M3);
-  const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&lo));
-  const float2 y = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
-  return (x.x + x.y) + (y.x + y.y);
+// The largest (kMax) or smallest of 64 raw scores held as fp32 bit patterns,
+// with three-input max / min: 32 dependent-free pairs folded into 4 chains.
+template <bool kMax>
+__device__ __forceinline__ float extreme3(const uint32_t (&v)[2][32]) {
+  float m[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) m[c] = kMax ? -INFINITY : INFINITY;
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      float &acc = m[(e >> 1) & 3];
+      const float a = __uint_as_float(v[i][e]), b = __uint_as_float(v[i][e + 1]);
+      if (kMax) asm("max.f32 %0, %0, %1, %2;" : "+f"(acc) : "f"(a), "f"(b));
+      else asm("min.f32 %0, %0, %1, %2;" : "+f"(acc) : "f"(a), "f"(b));
+    }
+  return kMax ? fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])) : fminf(fminf(m[0], m[1]), fminf(m[2], m[3]));
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -692,7 +704,8 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
     // l: row sum of the fp32 weights (the LSE); lr: of the weights rounded to the
     // input dtype, which is what P . V summed (O / lr is then exactly a weighted
     // mean of the value rows: a row dominated by one token gives that token's value
-    // rather than value * (1 + the rounding error of its weight))
+    // rather than value * (1 + the rounding error of its weight)).  e4m3: O is
+    // divided by l (lr = l), the TileLang kernel's normalisation.
     float m_ref = -INFINITY, l = 0.f, lr = 0.f;
     const int nsb = (s.hi - s.lo + kSB - 1) / kSB;
     for (int j = 0; j < nsb; ++j, ++sb) {
@@ -735,15 +748,22 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       }
       // eight independent partial maxima (and sums below): 64-long dependent
       // chains would leave the warp waiting on instruction latency
-      float mp[8];
+      float mloc;
+      if constexpr (kIsF8<T>) {
+        // the extreme of the raw scores, scaled once (the scale may be negative):
+        // three-input max / min, two new scores per instruction
+        mloc = sc >= 0.f ? sc * extreme3<true>(v) : sc * extreme3<false>(v);
+      } else {
+        float mp[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
+        for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(v[i][e]) * sc);
-      const float mloc = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+          for (int e = 0; e < 32; ++e) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(v[i][e]) * sc);
+        mloc = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                     fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      }
       red_max[half * 128 + r] = mloc;
       if (bar_red_or(1, 256, !ok || c.aborted())) return;  // all softmax threads leave together
       const float m_blk = fmaxf(red_max[r], red_max[128 + r]);
@@ -768,23 +788,34 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       if constexpr (kIsF8<T>) {
         // e4m3 tile: 64 bytes per row, 16-byte piece ch (tokens 16 ch ..) at
         // ch ^ ((row >> 1) & 3) (the 64-byte swizzle).  The weights are at most
-        // 2^kTau = 256 < 448, the largest e4m3 value.
+        // 2^kTau = 256 < 448, the largest e4m3 value.  Pairs of scores go through
+        // the packed fp32x2 FMA / add; O is divided by the sum of the fp32 weights
+        // (as the TileLang split kernel sums acc_s before its cast), so the
+        // rounded weights are not summed.
         const uint32_t row = smem_u32(smem + G::kOffPStage + tb * G::kPTile) + r * 64;
+        const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(nm, nm);
+        float2 s2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s2[e] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t u[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            float p[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              p[e] = fast_exp2(fmaf(__uint_as_float(v[ch >> 1][(ch & 1) * 16 + 4 * q + e]), sc, nm));
-              ps[(4 * q + e) & 7] += p[e];
-            }
-            u[q] = pack_e4m3x4(p[0], p[1], p[2], p[3]);
-            pr[q] += sum_e4m3x4(u[q]);
+            const uint32_t *x = &v[ch >> 1][(ch & 1) * 16 + 4 * q];
+            float2 a = __ffma2_rn(make_float2(__uint_as_float(x[0]), __uint_as_float(x[1])), sc2, nm2);
+            float2 b = __ffma2_rn(make_float2(__uint_as_float(x[2]), __uint_as_float(x[3])), sc2, nm2);
+            a = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+            b = make_float2(fast_exp2(b.x), fast_exp2(b.y));
+            s2[q] = __fadd2_rn(s2[q], __fadd2_rn(a, b));
+            u[q] = pack_e4m3x4(a.x, a.y, b.x, b.y);
           }
           if (write) st_shared_v4(row + ((ch ^ ((r >> 1) & 3)) << 4), u[0], u[1], u[2], u[3]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          ps[2 * e] = s2[e].x;
+          ps[2 * e + 1] = s2[e].y;
         }
       } else {
         const uint32_t row = smem_u32(smem + G::kOffPStage + tb * G::kPTile) + r * 128;
@@ -806,14 +837,15 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
         }
       }
       red_sum[half * 128 + r] = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      red_sumr[half * 128 + r] = (pr[0] + pr[1]) + (pr[2] + pr[3]);
+      if constexpr (!kIsF8<T>) red_sumr[half * 128 + r] = (pr[0] + pr[1]) + (pr[2] + pr[3]);
       const int hs = sb & 1;
       Header *hdr = reinterpret_cast<Header *>(smem + G::kOffHdrStage + hs * sizeof(Header));
       if (ok && half == 0 && sb >= 2)
         ok = wait_bar<true>(c, &b->hdr_free[hs], ((sb >> 1) - 1) & 1, W_HDR_FREE);
       if (bar_red_or(1, 256, !ok || c.aborted())) return;
       l = l * alpha + (red_sum[r] + red_sum[128 + r]);
-      lr = lr * alpha + (red_sumr[r] + red_sumr[128 + r]);
+      if constexpr (kIsF8<T>) lr = l;
+      else lr = lr * alpha + (red_sumr[r] + red_sumr[128 + r]);
       if (half == 0) {
         // the first superblock of a segment overwrites O: nothing to rescale
         hdr->alpha[r] = j == 0 ? 1.f : alpha;
