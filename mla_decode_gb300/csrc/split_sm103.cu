@@ -65,8 +65,7 @@ using namespace sm100;
 
 constexpr int kThreads = 352;            // 11 warps (see the role map in the kernel)
 constexpr int kSB = 2;                   // pages (64 tokens each) per superblock
-constexpr int kNPR = 4;                  // P tiles in the value CTA's ring
-constexpr int kStageTiles = 4;           // P staging tiles in the score CTA (a ring)
+constexpr int kNStage = 2;               // superblock staging slots in the score CTA
 constexpr int kSBufs = 3;                // S accumulators in the score CTA's TMEM, one page each
 // score CTA TMEM columns: Q (latent, then RoPE), then the S page accumulators
 // (64 columns each) from kTS0
@@ -87,20 +86,18 @@ struct Header {  // score -> value CTA, one per superblock
 };
 static_assert(sizeof(Header) % 16 == 0, "bulk copies move multiples of 16 bytes");
 
-constexpr int kNKMax = 5, kNVMax = 8;    // deepest K / V rings (e4m3)
+constexpr int kNKMax = 5, kNVMax = 8, kNPSBMax = 4;  // deepest K / V / P rings (e4m3)
 
 struct Bars {
   uint64_t k_full[kNKMax], k_empty[kNKMax];  // score
   uint64_t s_full[kSBufs], s_free[kSBufs];  // score, per S page buffer
   uint64_t q_free;                      // score: MMAs of a segment done with Q (MMA commit)
   uint64_t qs_full;                     // score: first segment's Q columns 0..255 in staging
-  uint64_t stage_ready[2];              // score: a superblock's P tiles + header staged
-  uint64_t stage_free[kStageTiles];     // score: a staging tile's copy landed (value CTA)
-  uint64_t slot_free[kNPR];             // score, value-CTA MMA commits (multicast)
-  uint64_t hdr_free[2];                 // score, arrived by the value CTA (both groups)
+  uint64_t stage_ready[kNStage];        // score: a superblock's P tiles + header staged
+  uint64_t stage_free[kNStage];         // score: a staging slot's copy landed (value CTA)
+  uint64_t slot_free[kNPSBMax];         // score, value-CTA MMA commits (multicast)
   uint64_t v_full[kNVMax], v_empty[kNVMax];  // value
-  uint64_t p_full[kNPR];                // value, bulk copies from the score CTA
-  uint64_t hdr_full[2];                 // value, bulk copies from the score CTA
+  uint64_t p_full[kNPSBMax];            // value, bulk copies from the score CTA
   uint64_t o_ready[2][2], o_done[2][2]; // value, [O half][superblock parity]
   uint64_t o_free;                      // value
   uint32_t tmem_base;
@@ -129,30 +126,32 @@ struct Geo {
   static constexpr int kVAtoms = kF8 ? 2 : 4;         // [64 rows x 128 B] atoms per V tile
   static constexpr int kQHalf = kF8 ? 2 : 4;          // Q boxes per 256 latent columns
   static constexpr int kQBoxCols = kF8 ? 128 : 64;    // Q columns per box
+  // A superblock's P as it travels to the value CTA: [P tile of page 0 | P tile of
+  // page 1 | header], one bulk copy (a DSMEM copy costs ~0.25 us plus its bytes)
+  static constexpr int kSBBytes = 2 * kPTile + (int)sizeof(Header);
+  static constexpr int kSBSlot = (kSBBytes + 1023) & ~1023;
+  static constexpr int kNPSB = kF8 ? 4 : 2;           // superblock slots in the value CTA
   static constexpr uint32_t kTQhalf = kF8 ? 64 : 128; // TMEM columns per 256 latent columns
   static constexpr uint32_t kTQpe = 2 * kTQhalf;      // Q's RoPE columns in TMEM
   static constexpr int kRopeCps = kF8 ? 2 : 4;        // 32-byte TMEM copies of a row's RoPE part
   static constexpr int kKStep = kF8 ? 32 : 16;        // K (tokens) per P.V MMA
   // shared-memory map (offsets from the 1024-aligned base)
   static constexpr int kOffK = 0;                                      // score: K ring
-  static constexpr int kOffPStage = kOffK + kNK * kKEntry;             // score: P staging tiles
-  static constexpr int kOffHdrStage = kOffPStage + kStageTiles * kPTile;  // score: 2 headers
-  static constexpr int kOffRed = kOffHdrStage + 2 * (int)sizeof(Header);  // score: [3][2][128] floats
+  static constexpr int kOffPStage = kOffK + kNK * kKEntry;             // score: superblock staging
+  static constexpr int kOffRed = kOffPStage + kNStage * kSBSlot;       // score: [3][2][128] floats
   static constexpr int kScoreEnd = kOffRed + 6 * 128 * 4;
   static constexpr int kOffV = 0;                                      // value: V ring
-  static constexpr int kOffPRing = kOffV + kNV * kVSlot;               // value: P tiles
-  static constexpr int kOffHdr = kOffPRing + kNPR * kPTile;            // value: 2 headers
-  static constexpr int kOffEpi = (kOffHdr + 2 * (int)sizeof(Header) + 1023) & ~1023;  // 8 x 2 KB
+  static constexpr int kOffPRing = kOffV + kNV * kVSlot;               // value: superblock slots
+  static constexpr int kOffEpi = kOffPRing + kNPSB * kSBSlot;          // value: 8 x 2 KB
   static constexpr int kValueEnd = kOffEpi + 8 * 2048;                 // epilogue staging, one per warp
   static constexpr int kOffBars = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 127) & ~127;
   static constexpr int kSmemBytes = kOffBars + (int)sizeof(Bars) + 1024;  // + alignment slack
-  static_assert(kNK <= kNKMax && kNV <= kNVMax, "ring barriers");
-  static_assert(kValueEnd <= kScoreEnd, "the value CTA's staging fits in the score CTA's footprint");
+  static_assert(kNK <= kNKMax && kNV <= kNVMax && kNPSB <= kNPSBMax, "ring barriers");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kOffPStage % 1024 == 0 && kKEntry % 1024 == 0 && kOffPRing % 1024 == 0 &&
                 kVSlot % 1024 == 0 && kPTile % 1024 == 0, "swizzle atoms");
-  static_assert(kQHalf * kQBox <= kKEntry && kQHalf * kQBox <= kStageTiles * kPTile,
-                "half of Q's latent columns fit a ring entry and the staging tiles");
+  static_assert(kQHalf * kQBox <= kKEntry && kQHalf * kQBox <= kNStage * kSBSlot,
+                "half of Q's latent columns fit a ring entry and the staging slots");
 };
 
 // wait sites, reported as the error detail on a timeout (mla_wait_site)
@@ -242,20 +241,6 @@ struct SegWalk {
   }
 };
 
-
-// Per-tile barrier bookkeeping in registers (arrays indexed by a run-time tile
-// number would live in local memory): bit t of `par` is the parity of the number
-// of completed uses of tile t, bit t of `used` says whether it was used at all.
-struct TileUse {
-  uint32_t par = 0, used = 0;
-  __device__ __forceinline__ uint32_t parity(int t) const { return (par >> t) & 1u; }
-  __device__ __forceinline__ bool was_used(int t) const { return (used >> t) & 1u; }
-  __device__ __forceinline__ void advance(int first, int n) {
-    const uint32_t m = ((1u << n) - 1u) << first;
-    par ^= m;
-    used |= m;
-  }
-};
 
 // Physical pages and first rows of the (up to kSB) pages of a superblock.  The
 // block-table loads are issued early (issue) and only consumed later (finish):
@@ -632,36 +617,24 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
   }
 }
 
-// Ships each superblock's staged P tiles and header into the value CTA once the
-// value CTA has freed the matching ring slots.
+// Ships each superblock's staged P tiles and header into the value CTA, as one
+// bulk copy, once the value CTA has freed the matching superblock slot.
 template <typename T>
 __device__ void score_copier(const FwdArgs &a, uint8_t *smem, const Ctx &c, int part) {
   using G = GeoOf<T>;
   Bars *b = c.bars;
   const uint32_t peer_pring = map_to_rank(smem_u32(smem + G::kOffPRing), 1);
-  const uint32_t peer_hdr = map_to_rank(smem_u32(smem + G::kOffHdr), 1);
   const uint32_t peer_pfull = map_to_rank(smem_u32(&b->p_full[0]), 1);
-  const uint32_t peer_hfull = map_to_rank(smem_u32(&b->hdr_full[0]), 1);
-  uint32_t pc = 0;  // P tiles shipped so far (staging tile pc % kStageTiles, ring slot pc % kNPR)
   uint32_t sb = 0;
   const bool leader = elect_one();
   SbWalk w(a, part);
   while (w.more) {
-    const int np = min(kSB, w.s.hi - w.sb0);
-    const uint32_t buf = sb & 1;
-    if (!wait_bar<false>(c, &b->stage_ready[buf], (sb >> 1) & 1, W_STAGE_READY)) return;
-    // the header first: the value CTA can prepare O for this superblock while it
-    // is still consuming the previous one's tiles
+    const uint32_t st = sb % kNStage, slot = sb % G::kNPSB, use = sb / G::kNPSB;
+    if (!wait_bar<false>(c, &b->stage_ready[st], (sb / kNStage) & 1, W_STAGE_READY)) return;
+    if (use > 0 && !wait_bar<true>(c, &b->slot_free[slot], (use - 1) & 1, W_SLOT_FREE)) return;
     if (leader)
-      bulk_copy_to_peer(peer_hdr + buf * sizeof(Header), smem + G::kOffHdrStage + buf * sizeof(Header),
-                        sizeof(Header), peer_hfull + buf * 8);
-    for (int t = 0; t < np; ++t, ++pc) {
-      const uint32_t r = pc % kNPR, use = pc / kNPR;
-      if (use > 0 && !wait_bar<true>(c, &b->slot_free[r], (use - 1) & 1, W_SLOT_FREE)) return;
-      if (leader)
-        bulk_copy_to_peer(peer_pring + r * G::kPTile, smem + G::kOffPStage + (pc % kStageTiles) * G::kPTile,
-                          G::kPTile, peer_pfull + r * 8);
-    }
+      bulk_copy_to_peer(peer_pring + slot * G::kSBSlot, smem + G::kOffPStage + st * G::kSBSlot, G::kSBBytes,
+                        peer_pfull + slot * 8);
     w.advance(a);
     ++sb;
   }
@@ -689,8 +662,6 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
   const float scale = a.scale_log2;
   uint32_t sb = 0;
   uint32_t pgs = 0;  // pages read so far: page p of a superblock is in S buffer (pgs + p) % kSBufs
-  uint32_t pt = 0;   // P tiles written so far: page p of a superblock uses staging tile (pt + p) % 4
-  TileUse tu;        // per staging tile
   SegWalk walk(a, part);
   Seg s;
   while (walk.next(a, s)) {
@@ -712,7 +683,9 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       const int sb0 = s.lo + j * kSB;
       const int np = min(kSB, s.hi - sb0);
       const bool last = j == nsb - 1;
-      const uint32_t buf = sb & 1;  // header / staging-stage parity
+      // staging slot of this superblock: [P tile of page 0 | page 1 | header]
+      const uint32_t buf = sb % kNStage;
+      uint8_t *stage = smem + G::kOffPStage + buf * G::kSBSlot;
       bool ok = true;
       uint32_t v[2][32];
       if (half < np) {  // my page's scores (a half without a page sees only -inf)
@@ -772,10 +745,9 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
         alpha = fast_exp2(m_ref - m_blk);
         m_ref = m_blk;
       }
-      // my staging tile must have left for the value CTA
-      const int tb = (int)((pt + half) % kStageTiles);
-      if (ok && half < np && tu.was_used(tb))
-        ok = wait_bar<true>(c, &b->stage_free[tb], tu.parity(tb) ^ 1u, W_STAGE_FREE);
+      // the staging slot's previous superblock must have left for the value CTA
+      if (ok && sb >= kNStage)
+        ok = wait_bar<true>(c, &b->stage_free[buf], (sb / kNStage - 1) & 1, W_STAGE_FREE);
       float ps[8], pr[4];
 #pragma unroll
       for (int e = 0; e < 8; ++e) ps[e] = 0.f;
@@ -792,7 +764,7 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
         // the packed fp32x2 FMA / add; O is divided by the sum of the fp32 weights
         // (as the TileLang split kernel sums acc_s before its cast), so the
         // rounded weights are not summed.
-        const uint32_t row = smem_u32(smem + G::kOffPStage + tb * G::kPTile) + r * 64;
+        const uint32_t row = smem_u32(stage + half * G::kPTile) + r * 64;
         const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(nm, nm);
         float2 s2[4];
 #pragma unroll
@@ -818,7 +790,7 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
           ps[2 * e + 1] = s2[e].y;
         }
       } else {
-        const uint32_t row = smem_u32(smem + G::kOffPStage + tb * G::kPTile) + r * 128;
+        const uint32_t row = smem_u32(stage + half * G::kPTile) + r * 128;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           float p[8];
@@ -838,10 +810,7 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       }
       red_sum[half * 128 + r] = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       if constexpr (!kIsF8<T>) red_sumr[half * 128 + r] = (pr[0] + pr[1]) + (pr[2] + pr[3]);
-      const int hs = sb & 1;
-      Header *hdr = reinterpret_cast<Header *>(smem + G::kOffHdrStage + hs * sizeof(Header));
-      if (ok && half == 0 && sb >= 2)
-        ok = wait_bar<true>(c, &b->hdr_free[hs], ((sb >> 1) - 1) & 1, W_HDR_FREE);
+      Header *hdr = reinterpret_cast<Header *>(stage + 2 * G::kPTile);
       if (bar_red_or(1, 256, !ok || c.aborted())) return;
       l = l * alpha + (red_sum[r] + red_sum[128 + r]);
       if constexpr (kIsF8<T>) lr = l;
@@ -861,10 +830,6 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       if (sw == 0 && lane == 0) hdr->flags = last ? 2u : 0u;
       fence_proxy_async_smem();
       mbar_arrive(&b->stage_ready[buf]);  // the copier ships the tiles and the header
-#pragma unroll
-      for (int t = 0; t < kSB; ++t)
-        if (t < np) tu.advance((int)((pt + t) % kStageTiles), 1);
-      pt += np;
     }
   }
 }
@@ -948,7 +913,6 @@ __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
   const uint32_t vfull = smem_u32(&b->v_full[0]), vempty = smem_u32(&b->v_empty[0]);
   const uint32_t pfull = smem_u32(&b->p_full[0]), sfree = smem_u32(&b->slot_free[0]);
   uint32_t vslot = 0, vphase = 0;  // V ring position of the next tile and its v_full parity
-  uint32_t pslot = 0, pphase = 0;  // P ring position of this superblock's first tile
   uint32_t sb = 0, segn = 0;
   const bool leader = elect_one();
   SegWalk walk(a, part);
@@ -962,20 +926,20 @@ __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
       const int sb0 = s.lo + j * kSB;
       const int np = min(kSB, s.hi - sb0);
 #pragma unroll 1
+      const uint32_t r = sb % G::kNPSB;  // this superblock's P slot
       for (int g = 0; g < 2; ++g) {
         if (!wait_bar<false>(c, &b->o_ready[g][sb & 1], (sb >> 1) & 1, W_O_READY)) return;
         tc_fence_after();
-        uint32_t r = pslot, rph = pphase;
 #pragma unroll 1
         for (int p = 0; p < np; ++p) {
           const int valid = min(64, s.L - ((sb0 + p) << 6));
           const int ksteps = (valid + G::kKStep - 1) / G::kKStep;
-          if (g == 0 && !wait_addr<true>(c, pfull + 8 * r, rph, W_P_FULL)) return;
+          if (g == 0 && p == 0 && !wait_addr<true>(c, pfull + 8 * r, (sb / G::kNPSB) & 1, W_P_FULL)) return;
           if (!wait_addr<false>(c, vfull + 8 * vslot, vphase, W_V_FULL)) return;
           if (leader && (valid % G::kKStep))
             zero_rows(smem + G::kOffV + vslot * G::kVSlot, G::kVAtoms, valid, ksteps * G::kKStep);
           tc_fence_after();
-          const uint64_t pd = pdesc + (uint64_t)(r * (G::kPTile >> 4));
+          const uint64_t pd = pdesc + (uint64_t)((r * G::kSBSlot + p * G::kPTile) >> 4);
           const uint64_t vd = vdesc + (uint64_t)(vslot * (G::kVSlot >> 4));
           const uint32_t acc0 = (first >> g) & 1u ? 0u : 1u;
           if (leader) {
@@ -985,47 +949,37 @@ __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
                 mma_ss_t<T>(tmem + 256 * g, pd + 2 * k, vd + (uint64_t)((G::kKStep * 128 >> 4) * k), idesc,
                             k == 0 ? acc0 : 1u);
             mma_commit_addr(vempty + 8 * vslot);
-            if (g == 1) mma_commit_multicast_addr(sfree + 8 * r, 1);  // P tile fully used
+            if (g == 1 && p == np - 1) mma_commit_multicast_addr(sfree + 8 * r, 1);  // P slot fully used
           }
           first &= ~(1u << g);
           if (++vslot == G::kNV) {
             vslot = 0;
             vphase ^= 1u;
           }
-          if (++r == kNPR) {
-            r = 0;
-            rph ^= 1u;
-          }
         }
         if (leader) mma_commit(&b->o_done[g][sb & 1]);
-        if (g == 1) {
-          pslot = r;
-          pphase = rph;
-        }
       }
     }
     ++segn;
   }
 }
 
-// Arms each incoming P tile's barrier and tells the score CTA as soon as the copy
-// has landed, so it can reuse the staging tile.
+// Arms each incoming superblock's barrier and tells the score CTA as soon as the
+// copy has landed, so it can reuse the staging slot.
 template <typename T>
 __device__ void value_receiver(const FwdArgs &a, const Ctx &c, int part) {
   using G = GeoOf<T>;
   Bars *b = c.bars;
-  uint32_t pc = 0;  // P tiles received so far
+  uint32_t sb = 0;
   const bool leader = elect_one();
   SbWalk w(a, part);
   while (w.more) {
-    const int np = min(kSB, w.s.hi - w.sb0);
-    for (int t = 0; t < np; ++t, ++pc) {
-      const uint32_t r = pc % kNPR;
-      if (leader) mbar_arrive_expect_tx(&b->p_full[r], G::kPTile);
-      if (!wait_bar<true>(c, &b->p_full[r], (pc / kNPR) & 1, W_P_FULL)) return;
-      if (leader) mbar_arrive_cluster(&b->stage_free[pc % kStageTiles], 0);
-    }
+    const uint32_t slot = sb % G::kNPSB;
+    if (leader) mbar_arrive_expect_tx(&b->p_full[slot], G::kSBBytes);
+    if (!wait_bar<true>(c, &b->p_full[slot], (sb / G::kNPSB) & 1, W_P_FULL)) return;
+    if (leader) mbar_arrive_cluster(&b->stage_free[sb % kNStage], 0);
     w.advance(a);
+    ++sb;
   }
 }
 
@@ -1147,15 +1101,15 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
     }
     const int nsb = (s.hi - s.lo + kSB - 1) / kSB;
     for (int j = 0; j < nsb; ++j, ++sb) {
-      const int hs = sb & 1;
-      if (sw == 0 && lane == 0) mbar_arrive_expect_tx(&b->hdr_full[hs], sizeof(Header));
-      bool ok = wait_bar<true>(c, &b->hdr_full[hs], (sb >> 1) & 1, W_HDR_FULL);
-      const Header *hdr = reinterpret_cast<const Header *>(smem + G::kOffHdr + hs * sizeof(Header));
+      // the header travels in the superblock's P slot, behind its two tiles
+      const uint32_t slot = sb % G::kNPSB;
+      bool ok = wait_bar<true>(c, &b->p_full[slot], (sb / G::kNPSB) & 1, W_HDR_FULL);
+      const Header *hdr =
+          reinterpret_cast<const Header *>(smem + G::kOffPRing + slot * G::kSBSlot + 2 * G::kPTile);
       const uint32_t flags = hdr->flags;
       const float alpha = hdr->alpha[r];
       const float lrow = hdr->l[r];
       if (bar_red_or(bar_id, 128, !ok || c.aborted())) return;
-      if ((sw & 3) == 0 && lane == 0) mbar_arrive_cluster(&b->hdr_free[hs], 0);
       // O_done(sb - 2) keeps the o_ready barriers from running two phases ahead;
       // a warp whose heads moved their reference max rescales once the previous
       // superblock's MMAs into this half are complete
@@ -1219,9 +1173,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant
       mbar_init(&b->k_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-
-      mbar_init(&b->hdr_free[i], 2);
-      mbar_init(&b->hdr_full[i], 1);
       for (int k = 0; k < 2; ++k) {
         mbar_init(&b->o_ready[i][k], 128);
         mbar_init(&b->o_done[i][k], 1);
@@ -1233,9 +1184,11 @@ split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant
       mbar_init(&b->s_full[i], 1);
       mbar_init(&b->s_free[i], 128);  // the four warps of the half that reads the page
     }
-    for (int i = 0; i < 2; ++i) mbar_init(&b->stage_ready[i], 256);
-    for (int i = 0; i < kStageTiles; ++i) mbar_init(&b->stage_free[i], 1);
-    for (int i = 0; i < kNPR; ++i) {
+    for (int i = 0; i < kNStage; ++i) {
+      mbar_init(&b->stage_ready[i], 256);
+      mbar_init(&b->stage_free[i], 1);
+    }
+    for (int i = 0; i < G::kNPSB; ++i) {
       mbar_init(&b->slot_free[i], 1);
       mbar_init(&b->p_full[i], 1);
     }
