@@ -1023,35 +1023,32 @@ __device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int
     return;
   }
   // one split: 16-bit rows of `out`, every lane takes part (the tile is shared by
-  // the warp)
-#pragma unroll 1
-  for (int i = 0; i < 4; ++i) {
-    uint32_t w[2][32];
-    tmem_ld32(tO + 64 * i, w[0]);
-    tmem_ld32(tO + 64 * i + 32, w[1]);
-    tmem_wait_ld();
-    {
-      O *o = reinterpret_cast<O *>(a.out) + (int64_t)seq * a.o_batch_stride + 256 * g + 64 * i;
+  // the warp).  32 columns at a time; the next 32 columns' TMEM load is in flight
+  // while the current ones go out.
+  O *o = reinterpret_cast<O *>(a.out) + (int64_t)seq * a.o_batch_stride + 256 * g;
+  uint32_t w[2][32];
+  tmem_ld32(tO, w[0]);
+  tmem_wait_ld_regs(w[0]);
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
+  for (int q = 0; q < 8; ++q) {
+    if (q < 7) tmem_ld32(tO + 32 * (q + 1), w[(q + 1) & 1]);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float *f = reinterpret_cast<const float *>(&w[t][8 * j]);
-          st_shared_v4(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), Pack<O>::two(f[0] * inv, f[1] * inv),
-                       Pack<O>::two(f[2] * inv, f[3] * inv), Pack<O>::two(f[4] * inv, f[5] * inv),
-                       Pack<O>::two(f[6] * inv, f[7] * inv));
-        }
-        __syncwarp();
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int row = 8 * r + (lane >> 2), j = lane & 3;
-          const uint4 v = ld_shared_v4(epi + row * 64 + ((j ^ ((row >> 1) & 3)) << 4));
-          if (row0 + row < a.h)
-            *reinterpret_cast<uint4 *>(o + (int64_t)(row0 + row) * a.o_head_stride + 32 * t + 8 * j) = v;
-        }
-        __syncwarp();
-      }
+    for (int j = 0; j < 4; ++j) {
+      const float *f = reinterpret_cast<const float *>(&w[q & 1][8 * j]);
+      st_shared_v4(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), Pack<O>::two(f[0] * inv, f[1] * inv),
+                   Pack<O>::two(f[2] * inv, f[3] * inv), Pack<O>::two(f[4] * inv, f[5] * inv),
+                   Pack<O>::two(f[6] * inv, f[7] * inv));
     }
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int row = 8 * r + (lane >> 2), j = lane & 3;
+      const uint4 v = ld_shared_v4(epi + row * 64 + ((j ^ ((row >> 1) & 3)) << 4));
+      if (row0 + row < a.h)
+        *reinterpret_cast<uint4 *>(o + (int64_t)(row0 + row) * a.o_head_stride + 32 * q + 8 * j) = v;
+    }
+    __syncwarp();
+    if (q < 7) tmem_wait_ld_regs(w[(q + 1) & 1]);
   }
 }
 
