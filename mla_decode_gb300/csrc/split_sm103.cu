@@ -63,9 +63,9 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 352;            // 11 warps (see the role map in the kernel)
+constexpr int kThreads = 384;            // 12 warps (see the role map in the kernel)
 constexpr int kSB = 2;                   // pages (64 tokens each) per superblock
-constexpr int kNStage = 2;               // superblock staging slots in the score CTA
+constexpr int kNStageMax = 4;            // superblock staging slots in the score CTA (at most)
 constexpr int kSBufs = 3;                // S accumulators in the score CTA's TMEM, one page each
 // score CTA TMEM columns: Q (latent, then RoPE), then the S page accumulators
 // (64 columns each) from kTS0
@@ -93,8 +93,8 @@ struct Bars {
   uint64_t s_full[kSBufs], s_free[kSBufs];  // score, per S page buffer
   uint64_t q_free;                      // score: MMAs of a segment done with Q (MMA commit)
   uint64_t qs_full;                     // score: first segment's Q columns 0..255 in staging
-  uint64_t stage_ready[kNStage];        // score: a superblock's P tiles + header staged
-  uint64_t stage_free[kNStage];         // score: a staging slot's copy landed (value CTA)
+  uint64_t stage_ready[kNStageMax];     // score: a superblock's P tiles + header staged
+  uint64_t stage_free[kNStageMax];      // score: a staging slot's copy landed (value CTA)
   uint64_t slot_free[kNPSBMax];         // score, value-CTA MMA commits (multicast)
   uint64_t v_full[kNVMax], v_empty[kNVMax];  // value
   uint64_t p_full[kNPSBMax];            // value, bulk copies from the score CTA
@@ -119,7 +119,8 @@ struct Bars {
 template <bool kF8>
 struct Geo {
   static constexpr int kKEntry = kF8 ? 9 * 4096 : 9 * kChunk;
-  static constexpr int kNK = kF8 ? 5 : 2;             // K ring entries, one page each
+  static constexpr int kNK = kF8 ? 4 : 2;             // K ring entries, one page each
+  static constexpr int kNStage = kF8 ? 4 : 2;         // superblock staging slots (score CTA)
   static constexpr int kPTile = kF8 ? 8192 : 16384;
   static constexpr int kVSlot = kF8 ? 2 * kChunk : 4 * kChunk;
   static constexpr int kNV = kF8 ? 8 : 4;             // V tiles in flight
@@ -146,7 +147,8 @@ struct Geo {
   static constexpr int kValueEnd = kOffEpi + 8 * 2048;                 // epilogue staging, one per warp
   static constexpr int kOffBars = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 127) & ~127;
   static constexpr int kSmemBytes = kOffBars + (int)sizeof(Bars) + 1024;  // + alignment slack
-  static_assert(kNK <= kNKMax && kNV <= kNVMax && kNPSB <= kNPSBMax, "ring barriers");
+  static_assert(kNK <= kNKMax && kNV <= kNVMax && kNPSB <= kNPSBMax && kNStage <= kNStageMax,
+                "ring barriers");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kOffPStage % 1024 == 0 && kKEntry % 1024 == 0 && kOffPRing % 1024 == 0 &&
                 kVSlot % 1024 == 0 && kPTile % 1024 == 0, "swizzle atoms");
@@ -629,8 +631,8 @@ __device__ void score_copier(const FwdArgs &a, uint8_t *smem, const Ctx &c, int 
   const bool leader = elect_one();
   SbWalk w(a, part);
   while (w.more) {
-    const uint32_t st = sb % kNStage, slot = sb % G::kNPSB, use = sb / G::kNPSB;
-    if (!wait_bar<false>(c, &b->stage_ready[st], (sb / kNStage) & 1, W_STAGE_READY)) return;
+    const uint32_t st = sb % G::kNStage, slot = sb % G::kNPSB, use = sb / G::kNPSB;
+    if (!wait_bar<false>(c, &b->stage_ready[st], (sb / G::kNStage) & 1, W_STAGE_READY)) return;
     if (use > 0 && !wait_bar<true>(c, &b->slot_free[slot], (use - 1) & 1, W_SLOT_FREE)) return;
     if (leader)
       bulk_copy_to_peer(peer_pring + slot * G::kSBSlot, smem + G::kOffPStage + st * G::kSBSlot, G::kSBBytes,
@@ -684,7 +686,7 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       const int np = min(kSB, s.hi - sb0);
       const bool last = j == nsb - 1;
       // staging slot of this superblock: [P tile of page 0 | page 1 | header]
-      const uint32_t buf = sb % kNStage;
+      const uint32_t buf = sb % G::kNStage;
       uint8_t *stage = smem + G::kOffPStage + buf * G::kSBSlot;
       bool ok = true;
       uint32_t v[2][32];
@@ -746,8 +748,8 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
         m_ref = m_blk;
       }
       // the staging slot's previous superblock must have left for the value CTA
-      if (ok && sb >= kNStage)
-        ok = wait_bar<true>(c, &b->stage_free[buf], (sb / kNStage - 1) & 1, W_STAGE_FREE);
+      if (ok && sb >= G::kNStage)
+        ok = wait_bar<true>(c, &b->stage_free[buf], (sb / G::kNStage - 1) & 1, W_STAGE_FREE);
       float ps[8], pr[4];
 #pragma unroll
       for (int e = 0; e < 8; ++e) ps[e] = 0.f;
@@ -897,10 +899,13 @@ __device__ __noinline__ void zero_rows(uint8_t *vs, int atoms, int r0, int r1) {
   fence_proxy_async_smem();
 }
 
-// As in the score CTA: the whole warp runs the loop, one elected lane issues,
-// and the loop only advances counters and descriptors between MMAs.
+// One warp per O half g (warps 1 and 11): the two halves' MMAs are issued in
+// parallel, since a step's waits, issues and commits take ~500 SM clocks of one
+// warp's time, longer than the tensor core needs for its two MMAs.  As in the score
+// CTA, the whole warp runs the loop and one elected lane issues.
 template <typename T>
-__device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int part, uint32_t tmem) {
+__device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int part, uint32_t tmem,
+                          int g) {
   using G = GeoOf<T>;
   Bars *b = c.bars;
   const uint32_t idesc = idesc_f16(128, 256, kFmtBit<T>, false, true);
@@ -912,7 +917,8 @@ __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
   constexpr int kSteps = 64 / G::kKStep;
   const uint32_t vfull = smem_u32(&b->v_full[0]), vempty = smem_u32(&b->v_empty[0]);
   const uint32_t pfull = smem_u32(&b->p_full[0]), sfree = smem_u32(&b->slot_free[0]);
-  uint32_t vslot = 0, vphase = 0;  // V ring position of the next tile and its v_full parity
+  const uint32_t tO = tmem + 256 * g;
+  uint32_t vc = 0;  // V tiles (both halves) of the superblocks before the current one
   uint32_t sb = 0, segn = 0;
   const bool leader = elect_one();
   SegWalk walk(a, part);
@@ -920,45 +926,40 @@ __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
   while (walk.next(a, s)) {
     if (s.hi <= s.lo) continue;
     if (segn > 0 && !wait_bar<false>(c, &b->o_free, (segn - 1) & 1, W_O_FREE)) return;  // epilogue read O
-    uint32_t first = 3u;  // bit g: the next MMA into O half g starts the accumulation
+    uint32_t acc = 0u;  // the segment's first MMA into this half starts the accumulation
     const int nsb = (s.hi - s.lo + kSB - 1) / kSB;
     for (int j = 0; j < nsb; ++j, ++sb) {
       const int sb0 = s.lo + j * kSB;
       const int np = min(kSB, s.hi - sb0);
-#pragma unroll 1
       const uint32_t r = sb % G::kNPSB;  // this superblock's P slot
-      for (int g = 0; g < 2; ++g) {
-        if (!wait_bar<false>(c, &b->o_ready[g][sb & 1], (sb >> 1) & 1, W_O_READY)) return;
-        tc_fence_after();
+      if (!wait_bar<false>(c, &b->o_ready[g][sb & 1], (sb >> 1) & 1, W_O_READY)) return;
+      if (!wait_addr<true>(c, pfull + 8 * r, (sb / G::kNPSB) & 1, W_P_FULL)) return;
+      tc_fence_after();
 #pragma unroll 1
-        for (int p = 0; p < np; ++p) {
-          const int valid = min(64, s.L - ((sb0 + p) << 6));
-          const int ksteps = (valid + G::kKStep - 1) / G::kKStep;
-          if (g == 0 && p == 0 && !wait_addr<true>(c, pfull + 8 * r, (sb / G::kNPSB) & 1, W_P_FULL)) return;
-          if (!wait_addr<false>(c, vfull + 8 * vslot, vphase, W_V_FULL)) return;
-          if (leader && (valid % G::kKStep))
-            zero_rows(smem + G::kOffV + vslot * G::kVSlot, G::kVAtoms, valid, ksteps * G::kKStep);
-          tc_fence_after();
-          const uint64_t pd = pdesc + (uint64_t)((r * G::kSBSlot + p * G::kPTile) >> 4);
-          const uint64_t vd = vdesc + (uint64_t)(vslot * (G::kVSlot >> 4));
-          const uint32_t acc0 = (first >> g) & 1u ? 0u : 1u;
-          if (leader) {
+      for (int p = 0; p < np; ++p) {
+        // the V stream holds a superblock's tiles as half 0's pages, then half 1's
+        const uint32_t t = vc + g * np + p, vslot = t % G::kNV;
+        const int valid = min(64, s.L - ((sb0 + p) << 6));
+        const int ksteps = (valid + G::kKStep - 1) / G::kKStep;
+        if (!wait_addr<false>(c, vfull + 8 * vslot, (t / G::kNV) & 1, W_V_FULL)) return;
+        if (leader && (valid % G::kKStep))
+          zero_rows(smem + G::kOffV + vslot * G::kVSlot, G::kVAtoms, valid, ksteps * G::kKStep);
+        tc_fence_after();
+        const uint64_t pd = pdesc + (uint64_t)((r * G::kSBSlot + p * G::kPTile) >> 4);
+        const uint64_t vd = vdesc + (uint64_t)(vslot * (G::kVSlot >> 4));
+        if (leader) {
 #pragma unroll
-            for (int k = 0; k < kSteps; ++k)
-              if (k < ksteps)
-                mma_ss_t<T>(tmem + 256 * g, pd + 2 * k, vd + (uint64_t)((G::kKStep * 128 >> 4) * k), idesc,
-                            k == 0 ? acc0 : 1u);
-            mma_commit_addr(vempty + 8 * vslot);
-            if (g == 1 && p == np - 1) mma_commit_multicast_addr(sfree + 8 * r, 1);  // P slot fully used
-          }
-          first &= ~(1u << g);
-          if (++vslot == G::kNV) {
-            vslot = 0;
-            vphase ^= 1u;
-          }
+          for (int k = 0; k < kSteps; ++k)
+            if (k < ksteps)
+              mma_ss_t<T>(tO, pd + 2 * k, vd + (uint64_t)((G::kKStep * 128 >> 4) * k), idesc, k == 0 ? acc : 1u);
+          mma_commit_addr(vempty + 8 * vslot);
+          // the P slot is free once both halves' MMAs on it are done (two arrivals)
+          if (p == np - 1) mma_commit_multicast_addr(sfree + 8 * r, 1);
         }
-        if (leader) mma_commit(&b->o_done[g][sb & 1]);
+        acc = 1u;
       }
+      if (leader) mma_commit(&b->o_done[g][sb & 1]);
+      vc += 2 * np;
     }
     ++segn;
   }
@@ -977,7 +978,7 @@ __device__ void value_receiver(const FwdArgs &a, const Ctx &c, int part) {
     const uint32_t slot = sb % G::kNPSB;
     if (leader) mbar_arrive_expect_tx(&b->p_full[slot], G::kSBBytes);
     if (!wait_bar<true>(c, &b->p_full[slot], (sb / G::kNPSB) & 1, W_P_FULL)) return;
-    if (leader) mbar_arrive_cluster(&b->stage_free[sb % kNStage], 0);
+    if (leader) mbar_arrive_cluster(&b->stage_free[sb % G::kNStage], 0);
     w.advance(a);
     ++sb;
   }
@@ -1181,12 +1182,12 @@ split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant
       mbar_init(&b->s_full[i], 1);
       mbar_init(&b->s_free[i], 128);  // the four warps of the half that reads the page
     }
-    for (int i = 0; i < kNStage; ++i) {
+    for (int i = 0; i < G::kNStage; ++i) {
       mbar_init(&b->stage_ready[i], 256);
       mbar_init(&b->stage_free[i], 1);
     }
     for (int i = 0; i < G::kNPSB; ++i) {
-      mbar_init(&b->slot_free[i], 1);
+      mbar_init(&b->slot_free[i], 2);    // the last MMA commit of each O half
       mbar_init(&b->p_full[i], 1);
     }
     for (int i = 0; i < G::kNV; ++i) {
@@ -1225,25 +1226,25 @@ split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant
   // up after 1 ms; every other role sees the abort and unwinds
   const bool loads = !a.forced_timeout;
   if (role == 0) {
-    // warp 0: K producer, 1: MMA, 2-9: softmax, 10: P/header copier.  Each role has
-    // a whole warp (a diverged spin loop would starve the other lanes' path, and
-    // warp-uniform issue loops let one elected lane issue at full rate).
+    // warp 0: K producer, 1: MMA, 2-9: softmax, 10: P/header copier, 11: idle.  Each
+    // role has a whole warp (a diverged spin loop would starve the other lanes' path,
+    // and warp-uniform issue loops let one elected lane issue at full rate).
     if (warp == 0) {
       if (loads) score_producer<T>(a, &k_map, &q_map, &kpe_map, &qpe_map, smem, c, part, head0);
     } else if (warp == 1) {
       score_mma<T>(a, smem, loads ? c : Ctx{b, a.err, kForcedWaitNs}, part, tmem);
     } else if (warp < 10) {
       score_softmax<T>(a, smem, c, part, tmem, head0);
-    } else {
+    } else if (warp == 10) {
       if (loads) score_copier<T>(a, smem, c, part);
     }
   } else {
-    // warp 0: V producer, 1: MMA, 2-5 / 6-9: correction and epilogue of O half 0 / 1,
-    // 10: P-tile receiver
+    // warp 0: V producer, 1 / 11: MMAs into O half 0 / 1, 2-5 / 6-9: correction and
+    // epilogue of O half 0 / 1, 10: superblock receiver
     if (warp == 0) {
       if (loads) value_producer<T>(a, &kv4_map, smem, c, part);
-    } else if (warp == 1) {
-      value_mma<T>(a, smem, c, part, tmem);
+    } else if (warp == 1 || warp == 11) {
+      value_mma<T>(a, smem, c, part, tmem, warp == 1 ? 0 : 1);
     } else if (warp < 10) {
       value_correction<T>(a, smem, c, part, tmem, head0);
     } else {
