@@ -356,6 +356,14 @@ __device__ __forceinline__ float extreme3(const uint32_t (&v)[2][32]) {
   return kMax ? fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])) : fminf(fminf(m[0], m[1]), fminf(m[2], m[3]));
 }
 
+// A 32-byte global store (one L2 sector); `p` must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                             uint32_t e, uint32_t f, uint32_t g, uint32_t h) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+               "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
+               : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -1023,34 +1031,38 @@ __device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int
     }
     return;
   }
-  // one split: 16-bit rows of `out`, every lane takes part (the tile is shared by
-  // the warp).  32 columns at a time; the next 32 columns' TMEM load is in flight
-  // while the current ones go out.
-  O *o = reinterpret_cast<O *>(a.out) + (int64_t)seq * a.o_batch_stride + 256 * g;
+  // one split: each thread writes its own row's 16-bit values, 32 columns (64 B) at a
+  // time as two 32-byte stores (whole L2 sectors; 16-byte stores when `out`'s rows
+  // are not 32-byte aligned), while the next 32 columns' TMEM load is in flight.
+  O *o = reinterpret_cast<O *>(a.out) + (int64_t)seq * a.o_batch_stride + (int64_t)head * a.o_head_stride +
+         256 * g;
+  const bool v8 = ((reinterpret_cast<uintptr_t>(a.out) | (uintptr_t)(a.o_batch_stride * 2) |
+                    (uintptr_t)(a.o_head_stride * 2)) & 31) == 0;
   uint32_t w[2][32];
   tmem_ld32(tO, w[0]);
   tmem_wait_ld_regs(w[0]);
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     if (q < 7) tmem_ld32(tO + 32 * (q + 1), w[(q + 1) & 1]);
+    uint32_t hv[16];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float *f = reinterpret_cast<const float *>(&w[q & 1][8 * j]);
-      st_shared_v4(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), Pack<O>::two(f[0] * inv, f[1] * inv),
-                   Pack<O>::two(f[2] * inv, f[3] * inv), Pack<O>::two(f[4] * inv, f[5] * inv),
-                   Pack<O>::two(f[6] * inv, f[7] * inv));
-    }
-    __syncwarp();
+    for (int e = 0; e < 16; ++e)
+      hv[e] = Pack<O>::two(__uint_as_float(w[q & 1][2 * e]) * inv, __uint_as_float(w[q & 1][2 * e + 1]) * inv);
+    if (head_ok) {
+      O *dst = o + 32 * q;
+      if (v8) {
+        st_global_v8(dst, hv[0], hv[1], hv[2], hv[3], hv[4], hv[5], hv[6], hv[7]);
+        st_global_v8(dst + 16, hv[8], hv[9], hv[10], hv[11], hv[12], hv[13], hv[14], hv[15]);
+      } else {
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int row = 8 * r + (lane >> 2), j = lane & 3;
-      const uint4 v = ld_shared_v4(epi + row * 64 + ((j ^ ((row >> 1) & 3)) << 4));
-      if (row0 + row < a.h)
-        *reinterpret_cast<uint4 *>(o + (int64_t)(row0 + row) * a.o_head_stride + 32 * q + 8 * j) = v;
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<uint4 *>(dst + 8 * k) = make_uint4(hv[4 * k], hv[4 * k + 1], hv[4 * k + 2], hv[4 * k + 3]);
+      }
     }
-    __syncwarp();
     if (q < 7) tmem_wait_ld_regs(w[(q + 1) & 1]);
   }
+  (void)epi;
+  (void)lane;
 }
 
 // The zero output row half of an empty sequence (its lse is -inf).
