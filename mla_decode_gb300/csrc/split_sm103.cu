@@ -139,8 +139,8 @@ struct Geo {
   // shared-memory map (offsets from the 1024-aligned base)
   static constexpr int kOffK = 0;                                      // score: K ring
   static constexpr int kOffPStage = kOffK + kNK * kKEntry;             // score: superblock staging
-  static constexpr int kOffRed = kOffPStage + kNStage * kSBSlot;       // score: [3][2][128] floats
-  static constexpr int kScoreEnd = kOffRed + 6 * 128 * 4;
+  static constexpr int kOffRed = kOffPStage + kNStage * kSBSlot;       // score: [4][2][128] floats
+  static constexpr int kScoreEnd = kOffRed + 8 * 128 * 4;
   static constexpr int kOffV = 0;                                      // value: V ring
   static constexpr int kOffPRing = kOffV + kNV * kVSlot;               // value: superblock slots
   static constexpr int kOffEpi = kOffPRing + kNPSB * kSBSlot;          // value: 8 x 2 KB
@@ -666,9 +666,10 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
   // sees q_len - 1 - qi fewer cached tokens than the sequence holds
   const int hidden = (a.causal && head_ok) ? a.q_len - 1 - head / a.heads : 0;
   const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
-  float *red_max = reinterpret_cast<float *>(smem + G::kOffRed);  // [2][128]
-  float *red_sum = red_max + 256;                               // [2][128] fp32 weights
-  float *red_sumr = red_max + 512;                              // [2][128] 16-bit weights
+  // [superblock parity][half][128]: a half can be one superblock ahead of the other
+  float *red_max = reinterpret_cast<float *>(smem + G::kOffRed);
+  float *red_sum = red_max + 512;                               // [half][128] fp32 weights
+  float *red_sumr = red_max + 768;                              // [half][128] 16-bit weights
   const float scale = a.scale_log2;
   uint32_t sb = 0;
   uint32_t pgs = 0;  // pages read so far: page p of a superblock is in S buffer (pgs + p) % kSBufs
@@ -687,6 +688,9 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
     // mean of the value rows: a row dominated by one token gives that token's value
     // rather than value * (1 + the rounding error of its weight)).  e4m3: O is
     // divided by l (lr = l), the TileLang kernel's normalisation.
+    // Each half keeps the sums of its own pages (rescaled by the common alpha); the
+    // two halves' sums meet once, at the segment's last superblock, so a superblock
+    // costs one named barrier (the row-max exchange).
     float m_ref = -INFINITY, l = 0.f, lr = 0.f;
     const int nsb = (s.hi - s.lo + kSB - 1) / kSB;
     for (int j = 0; j < nsb; ++j, ++sb) {
@@ -747,9 +751,10 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
         mloc = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                      fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       }
-      red_max[half * 128 + r] = mloc;
+      float *rmax = red_max + (sb & 1) * 256;
+      rmax[half * 128 + r] = mloc;
       if (bar_red_or(1, 256, !ok || c.aborted())) return;  // all softmax threads leave together
-      const float m_blk = fmaxf(red_max[r], red_max[128 + r]);
+      const float m_blk = fmaxf(rmax[r], rmax[128 + r]);
       float alpha = 1.f;
       if (m_blk > m_ref + kTau) {  // also the first block (m_ref = -inf)
         alpha = fast_exp2(m_ref - m_blk);
@@ -818,13 +823,17 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
           if (write) st_shared_v4(row + ((ch ^ (r & 7)) << 4), u[0], u[1], u[2], u[3]);
         }
       }
-      red_sum[half * 128 + r] = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      if constexpr (!kIsF8<T>) red_sumr[half * 128 + r] = (pr[0] + pr[1]) + (pr[2] + pr[3]);
-      Header *hdr = reinterpret_cast<Header *>(stage + 2 * G::kPTile);
-      if (bar_red_or(1, 256, !ok || c.aborted())) return;
-      l = l * alpha + (red_sum[r] + red_sum[128 + r]);
+      l = l * alpha + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
       if constexpr (kIsF8<T>) lr = l;
-      else lr = lr * alpha + (red_sumr[r] + red_sumr[128 + r]);
+      else lr = lr * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+      Header *hdr = reinterpret_cast<Header *>(stage + 2 * G::kPTile);
+      if (last) {  // the row's totals: both halves' sums
+        red_sum[half * 128 + r] = l;
+        red_sumr[half * 128 + r] = lr;
+        if (bar_red_or(1, 256, !ok || c.aborted())) return;
+        l = red_sum[r] + red_sum[128 + r];
+        lr = red_sumr[r] + red_sumr[128 + r];
+      }
       if (half == 0) {
         // the first superblock of a segment overwrites O: nothing to rescale
         hdr->alpha[r] = j == 0 ? 1.f : alpha;
