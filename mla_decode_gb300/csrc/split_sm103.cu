@@ -641,7 +641,7 @@ __device__ void score_copier(const FwdArgs &a, uint8_t *smem, const Ctx &c, int 
   while (w.more) {
     const uint32_t st = sb % G::kNStage, slot = sb % G::kNPSB, use = sb / G::kNPSB;
     if (!wait_bar<false>(c, &b->stage_ready[st], (sb / G::kNStage) & 1, W_STAGE_READY)) return;
-    if (use > 0 && !wait_bar<true>(c, &b->slot_free[slot], (use - 1) & 1, W_SLOT_FREE)) return;
+    if (use > 0 && !wait_bar<false>(c, &b->slot_free[slot], (use - 1) & 1, W_SLOT_FREE)) return;
     if (leader)
       bulk_copy_to_peer(peer_pring + slot * G::kSBSlot, smem + G::kOffPStage + st * G::kSBSlot, G::kSBBytes,
                         peer_pfull + slot * 8);
@@ -762,7 +762,7 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       }
       // the staging slot's previous superblock must have left for the value CTA
       if (ok && sb >= G::kNStage)
-        ok = wait_bar<true>(c, &b->stage_free[buf], (sb / G::kNStage - 1) & 1, W_STAGE_FREE);
+        ok = wait_bar<false>(c, &b->stage_free[buf], (sb / G::kNStage - 1) & 1, W_STAGE_FREE);
       float ps[8], pr[4];
 #pragma unroll
       for (int e = 0; e < 8; ++e) ps[e] = 0.f;
@@ -950,7 +950,7 @@ __device__ void value_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
       const int np = min(kSB, s.hi - sb0);
       const uint32_t r = sb % G::kNPSB;  // this superblock's P slot
       if (!wait_bar<false>(c, &b->o_ready[g][sb & 1], (sb >> 1) & 1, W_O_READY)) return;
-      if (!wait_addr<true>(c, pfull + 8 * r, (sb / G::kNPSB) & 1, W_P_FULL)) return;
+      if (!wait_addr<false>(c, pfull + 8 * r, (sb / G::kNPSB) & 1, W_P_FULL)) return;
       tc_fence_after();
 #pragma unroll 1
       for (int p = 0; p < np; ++p) {
@@ -994,8 +994,8 @@ __device__ void value_receiver(const FwdArgs &a, const Ctx &c, int part) {
   while (w.more) {
     const uint32_t slot = sb % G::kNPSB;
     if (leader) mbar_arrive_expect_tx(&b->p_full[slot], G::kSBBytes);
-    if (!wait_bar<true>(c, &b->p_full[slot], (sb / G::kNPSB) & 1, W_P_FULL)) return;
-    if (leader) mbar_arrive_cluster(&b->stage_free[sb % G::kNStage], 0);
+    if (!wait_bar<false>(c, &b->p_full[slot], (sb / G::kNPSB) & 1, W_P_FULL)) return;
+    if (leader) mbar_arrive_cluster_relaxed(&b->stage_free[sb % G::kNStage], 0);
     w.advance(a);
     ++sb;
   }
@@ -1122,7 +1122,7 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
     for (int j = 0; j < nsb; ++j, ++sb) {
       // the header travels in the superblock's P slot, behind its two tiles
       const uint32_t slot = sb % G::kNPSB;
-      bool ok = wait_bar<true>(c, &b->p_full[slot], (sb / G::kNPSB) & 1, W_HDR_FULL);
+      bool ok = wait_bar<false>(c, &b->p_full[slot], (sb / G::kNPSB) & 1, W_HDR_FULL);
       const Header *hdr =
           reinterpret_cast<const Header *>(smem + G::kOffPRing + slot * G::kSBSlot + 2 * G::kPTile);
       const uint32_t flags = hdr->flags;
