@@ -89,7 +89,7 @@ static_assert(sizeof(Header) % 16 == 0, "bulk copies move multiples of 16 bytes"
 constexpr int kNKMax = 5, kNVMax = 8, kNPSBMax = 4;  // deepest K / V / P rings (e4m3)
 
 struct Bars {
-  uint64_t k_full[kNKMax], k_empty[kNKMax];  // score
+  uint64_t k_full[2 * kNKMax], k_empty[2 * kNKMax];  // score, [entry][part]
   uint64_t s_full[kSBufs], s_free[kSBufs];  // score, per S page buffer
   uint64_t q_free;                      // score: MMAs of a segment done with Q (MMA commit)
   uint64_t qs_full;                     // score: first segment's Q columns 0..255 in staging
@@ -120,6 +120,11 @@ template <bool kF8>
 struct Geo {
   static constexpr int kKEntry = kF8 ? 9 * 4096 : 9 * kChunk;
   static constexpr int kNK = kF8 ? 4 : 2;             // K ring entries, one page each
+  // 16-bit: an entry fills and drains as two parts with barriers of their own,
+  // atoms 0..3 (A) and atoms 4..8 (B): the next page's A half loads while this
+  // page's B half is still in use, and a page's MMAs start once A is in
+  static constexpr int kKParts = kF8 ? 1 : 2;
+  static constexpr int kKAtomsA = 4;
   static constexpr int kNStage = kF8 ? 4 : 2;         // superblock staging slots (score CTA)
   static constexpr int kPTile = kF8 ? 8192 : 16384;
   static constexpr int kVSlot = kF8 ? 2 * kChunk : 4 * kChunk;
@@ -433,7 +438,7 @@ __device__ __forceinline__ void issue_job(const FwdArgs &a, SbWalk &w, SbJob &j)
 // all of Q is in flight at once and the first K page follows the small RoPE box.
 template <typename T>
 __device__ void score_producer(const FwdArgs &a, const CUtensorMap *kmap, const CUtensorMap *qmap,
-                               const CUtensorMap *pemap, const CUtensorMap *qpemap,
+                               const CUtensorMap *pemap, const CUtensorMap *qpemap, const CUtensorMap *map4,
                                uint8_t *smem, const Ctx &c, int part, int head0) {
   using G = GeoOf<T>;
   // the RoPE box of Q: the separate 64-column map (16-bit), or the 128-byte box at
@@ -446,12 +451,16 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *kmap, const 
   SbWalk w(a, part);
   SbJob cur{}, nxt{};
   bool hc = false, hn = false;
-  // the next ring entry, once the MMAs of its previous use are done with it
-  auto next_entry = [&](uint32_t &slot) -> bool {
+  // the next ring entry; part h of it is free once the MMAs of its previous use
+  // are done with that part
+  uint32_t kuse = 0;
+  auto next_entry = [&](uint32_t &slot) {
     slot = kc % G::kNK;
-    const uint32_t use = kc / G::kNK;
+    kuse = kc / G::kNK;
     ++kc;
-    return use == 0 || wait_bar<false>(c, &b->k_empty[slot], (use - 1) & 1, W_K_EMPTY);
+  };
+  auto part_free = [&](uint32_t slot, int h) -> bool {
+    return kuse == 0 || wait_bar<false>(c, &b->k_empty[2 * slot + h], (kuse - 1) & 1, W_K_EMPTY);
   };
   auto run = [&](SbJob &j) -> bool {
     if (j.first) {
@@ -467,19 +476,24 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *kmap, const 
       for (int i = first_seg ? 1 : 0; i < 3; ++i) {
         const int what = first_seg ? (i == 1 ? 2 : 1) : i;  // 0, 1: latent halves; 2: RoPE
         uint32_t slot;
-        if (!next_entry(slot)) return false;
+        next_entry(slot);
+        // Q takes the whole entry: part A's barrier carries the bytes, part B's
+        // completes by a plain arrival
+        for (int h = 0; h < G::kKParts; ++h)
+          if (!part_free(slot, h)) return false;
         if (leader) {
           uint8_t *dst = smem + G::kOffK + slot * G::kKEntry;
+          uint64_t *full = &b->k_full[2 * slot];
           if (what < 2) {
-            mbar_arrive_expect_tx(&b->k_full[slot], G::kQHalf * kQBox);
+            mbar_arrive_expect_tx(full, G::kQHalf * kQBox);
 #pragma unroll
             for (int bx = 0; bx < G::kQHalf; ++bx)
-              tma_load_3d(dst + bx * kQBox, qmap, &b->k_full[slot],
-                          G::kQBoxCols * (G::kQHalf * what + bx), head0, j.seq);
+              tma_load_3d(dst + bx * kQBox, qmap, full, G::kQBoxCols * (G::kQHalf * what + bx), head0, j.seq);
           } else {
-            mbar_arrive_expect_tx(&b->k_full[slot], kQBox);
-            tma_load_3d(dst, qpemap, &b->k_full[slot], kRopeX, head0, j.seq);
+            mbar_arrive_expect_tx(full, kQBox);
+            tma_load_3d(dst, qpemap, full, kRopeX, head0, j.seq);
           }
+          if (G::kKParts == 2) mbar_arrive(&b->k_full[2 * slot + 1]);
         }
       }
       first_seg = false;
@@ -489,13 +503,35 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *kmap, const 
     for (int p = 0; p < kSB; ++p) {
       if (p >= j.np) break;
       uint32_t slot;
-      if (!next_entry(slot)) return false;
-      if (leader) {
-        mbar_arrive_expect_tx(&b->k_full[slot], G::kKEntry);
-        uint8_t *dst = smem + G::kOffK + slot * G::kKEntry;
-        tma_load_4d(dst, kmap, &b->k_full[slot], 0, j.pg.row0[p], 0, j.pg.page[p]);
-        if (!kIsF8<T> && !a.k_fused)
-          tma_load_3d(dst + 8 * kChunk, pemap, &b->k_full[slot], 0, j.pg.row0[p], j.pg.page[p]);
+      next_entry(slot);
+      uint8_t *dst = smem + G::kOffK + slot * G::kKEntry;
+      if constexpr (kIsF8<T>) {
+        if (!part_free(slot, 0)) return false;
+        if (leader) {
+          mbar_arrive_expect_tx(&b->k_full[2 * slot], G::kKEntry);
+          tma_load_4d(dst, kmap, &b->k_full[2 * slot], 0, j.pg.row0[p], 0, j.pg.page[p]);
+        }
+      } else {
+        // part A: latent atoms 0..3 (the four-block map); part B: atoms 4..8, as
+        // five blocks of the 576-column rows or as latent atoms 4..7 plus the
+        // K_pe box
+        if (!part_free(slot, 0)) return false;
+        if (leader) {
+          mbar_arrive_expect_tx(&b->k_full[2 * slot], G::kKAtomsA * kChunk);
+          tma_load_4d(dst, map4, &b->k_full[2 * slot], 0, j.pg.row0[p], 0, j.pg.page[p]);
+        }
+        if (!part_free(slot, 1)) return false;
+        if (leader) {
+          uint64_t *full = &b->k_full[2 * slot + 1];
+          uint8_t *dstb = dst + G::kKAtomsA * kChunk;
+          mbar_arrive_expect_tx(full, (9 - G::kKAtomsA) * kChunk);
+          if (a.k_fused) {
+            tma_load_4d(dstb, kmap, full, 0, j.pg.row0[p], G::kKAtomsA, j.pg.page[p]);
+          } else {
+            tma_load_4d(dstb, map4, full, 0, j.pg.row0[p], G::kKAtomsA, j.pg.page[p]);
+            tma_load_3d(dst + 8 * kChunk, pemap, full, 0, j.pg.row0[p], j.pg.page[p]);
+          }
+        }
       }
     }
     return true;
@@ -563,7 +599,7 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
         tc_fence_after();
         bd = desc_kmajor_sw128(smem_u32(smem + G::kOffPStage));
       } else {
-        if (!wait_addr<false>(c, kfull + 8 * slot, phase, W_K_FULL)) return;
+        if (!wait_addr<false>(c, kfull + 16 * slot, phase, W_K_FULL)) return;
         tc_fence_after();
         // Q boxes use the 128-byte swizzle in either width
         bd = desc_kmajor_sw128(smem_u32(smem + G::kOffK + slot * G::kKEntry));
@@ -581,7 +617,10 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
           for (int k = 0; k < G::kRopeCps; ++k)
             tmem_cp_128x256b(tQ + G::kTQpe + 8 * k, bd + (uint64_t)(2 * k));
         }
-        if (what != 3) mma_commit_addr(kempty + 8 * slot);
+        if (what != 3) {
+          mma_commit_addr(kempty + 16 * slot);
+          if (G::kKParts == 2) mma_commit_addr(kempty + 16 * slot + 8);
+        }
       }
       if (what != 3) advance();
     }
@@ -593,11 +632,11 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
         tc_fence_after();
       }
       const uint32_t tS = tmem + kTS0 + 64 * sbuf;
-      if (!wait_addr<false>(c, kfull + 8 * slot, phase, W_K_FULL)) return;
+      if (!wait_addr<false>(c, kfull + 16 * slot, phase, W_K_FULL)) return;
       tc_fence_after();
       const uint64_t bd = kdesc + (uint64_t)(slot * (G::kKEntry >> 4));
-      if (leader) {
-        if constexpr (kIsF8<T>) {
+      if constexpr (kIsF8<T>) {
+        if (leader) {
           // nine [64 x 64 B] atoms, 4 KB apart, two K = 32 steps each; Q's TMEM
           // columns run on through the RoPE part (16 per atom)
 #pragma unroll
@@ -606,20 +645,32 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
             for (int k = 0; k < 2; ++k)
               mma_ts_t<T>(tS, tQ + 16 * blk + 8 * k, bd + (uint64_t)(blk * (4096 >> 4) + 2 * k), idesc,
                           (blk | k) != 0);
-        } else {
+          mma_commit_addr(kempty + 16 * slot);
+        }
+      } else {
+        // part A (atoms 0..3), its release, then part B (atoms 4..8; the ninth is
+        // the RoPE part, whose Q columns follow the latent ones)
+        if (leader) {
 #pragma unroll
-          for (int blk = 0; blk < 8; ++blk)
+          for (int blk = 0; blk < G::kKAtomsA; ++blk)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               mma_ts_t<T>(tS, tQ + 32 * blk + 8 * k, bd + (uint64_t)(blk * (kChunk >> 4) + 2 * k), idesc,
                           (blk | k) != 0);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts_t<T>(tS, tQ + G::kTQpe + 8 * k, bd + (uint64_t)(8 * (kChunk >> 4) + 2 * k), idesc, 1);
+          mma_commit_addr(kempty + 16 * slot);
         }
-        mma_commit_addr(kempty + 8 * slot);
-        mma_commit(&b->s_full[sbuf]);
+        if (!wait_addr<false>(c, kfull + 16 * slot + 8, phase, W_K_FULL)) return;
+        tc_fence_after();
+        if (leader) {
+#pragma unroll
+          for (int blk = G::kKAtomsA; blk < 9; ++blk)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ts_t<T>(tS, tQ + 32 * blk + 8 * k, bd + (uint64_t)(blk * (kChunk >> 4) + 2 * k), idesc, 1);
+          mma_commit_addr(kempty + 16 * slot + 8);
+        }
       }
+      if (leader) mma_commit(&b->s_full[sbuf]);
       advance();
     }
     if (leader) mma_commit(&b->q_free);
@@ -1188,8 +1239,10 @@ split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < G::kNK; ++i) {
-      mbar_init(&b->k_full[i], 1);
-      mbar_init(&b->k_empty[i], 1);
+      for (int h = 0; h < G::kKParts; ++h) {
+        mbar_init(&b->k_full[2 * i + h], 1);
+        mbar_init(&b->k_empty[2 * i + h], 1);
+      }
     }
     for (int i = 0; i < 2; ++i) {
       for (int k = 0; k < 2; ++k) {
@@ -1251,7 +1304,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant
     // role has a whole warp (a diverged spin loop would starve the other lanes' path,
     // and warp-uniform issue loops let one elected lane issue at full rate).
     if (warp == 0) {
-      if (loads) score_producer<T>(a, &k_map, &q_map, &kpe_map, &qpe_map, smem, c, part, head0);
+      if (loads) score_producer<T>(a, &k_map, &q_map, &kpe_map, &qpe_map, &kv4_map, smem, c, part, head0);
     } else if (warp == 1) {
       score_mma<T>(a, smem, loads ? c : Ctx{b, a.err, kForcedWaitNs}, part, tmem);
     } else if (warp < 10) {
@@ -1388,12 +1441,13 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
     qpemap = qmap;
     pemap = kmap;  // unused
   } else {
-    // K: one box per page over all nine 64-column blocks of a 576-column row, or,
-    // with K_pe separate, the eight latent blocks plus a [64 rows x 64] K_pe box.
-    // V: the latent blocks again, four per box (one O half of one page).  Q and
+    // K: a page in two parts, latent blocks 0..3 (the V map's box) and blocks 4..8
+    // of the 576-column rows (five blocks), or, with K_pe separate, latent blocks
+    // 4..7 plus a [64 rows x 64] K_pe box.  V: the latent blocks, four per box (one
+    // O half of one page).  Q and
     // Q_pe as [b][h][cols], boxes of 128 heads x 64 columns (rows past h read as
     // zeros).
-    e = make_block_map<T>(&kmap, a.kv, 64, a.k_fused ? 9 : 8, a.k_fused ? 9 : 8,
+    e = make_block_map<T>(&kmap, a.kv, 64, a.k_fused ? 9 : 8, a.k_fused ? 9 - GeoOf<T>::kKAtomsA : 8,
                           CU_TENSOR_MAP_SWIZZLE_128B, a);
     if (e == cudaSuccess)
       e = make_block_map<T>(&map4, a.kv, 64, kLatent / 64, 4, CU_TENSOR_MAP_SWIZZLE_128B, a);
