@@ -54,6 +54,9 @@ def parse_args():
     ap.add_argument("--layout", choices=["fused", "split"], default="fused",
                     help="fused: 576-column q / kv_cache rows; split: Q / Q_pe and KV / K_pe "
                          "as separate tensors")
+    ap.add_argument("--combine", choices=["fused", "kernel"], default="kernel",
+                    help="fused: the split kernel combines the sequences it split (grid "
+                         "barrier); kernel: a separate combine kernel after it")
     return ap.parse_args()
 
 
@@ -81,7 +84,8 @@ def measured_peaks():
 def kernel_source_hash():
     """Hash of the split kernel's sources (the kernel the roofline line reports)."""
     csrc = os.path.join(ROOT, "mla_decode_gb300", "csrc")
-    files = [os.path.join(csrc, f) for f in ("common.cuh", "internal.h", "sm100.cuh", "split_sm103.cu")]
+    files = [os.path.join(csrc, f) for f in ("combine.cuh", "common.cuh", "internal.h", "sm100.cuh",
+                                             "split_sm103.cu")]
     h = hashlib.sha256()
     for f in files:
         h.update(os.path.basename(f).encode())
@@ -371,7 +375,8 @@ def run_ours(args):
                       dtype=torch.float32, device=dev)
     calls = [mla.prepare_decode(s["q"], s["kv_cache"], s["block_table"], s["cache_seqlens"],
                                 w.softmax_scale, meta, nsplit, out, lse, ws, q_pe=s["q_pe"],
-                                k_pe=s["k_pe"], is_causal=w.causal, **input_scales(s))
+                                k_pe=s["k_pe"], is_causal=w.causal, **input_scales(s),
+                                fused_combine=args.combine == "fused")
              for s in sets]
     metas = [mla.prepare_metadata(s["cache_seqlens"], w.heads, num_sm, meta, nsplit,
                                   seqlen_q=w.seqlen_q) for s in sets]
@@ -431,7 +436,8 @@ def run_ours(args):
     e2e_call = mla.prepare_decode(dbuf["q"], dbuf["kv_cache"], dbuf["block_table"],
                                   dbuf["cache_seqlens"], w.softmax_scale, meta, nsplit, out, lse,
                                   ws, q_pe=dbuf.get("q_pe"), k_pe=dbuf.get("k_pe"),
-                                  is_causal=w.causal, **input_scales(base))
+                                  is_causal=w.causal, **input_scales(base),
+                                  fused_combine=args.combine == "fused")
     e2e_meta = mla.prepare_metadata(dbuf["cache_seqlens"], w.heads, num_sm, meta, nsplit,
                                     seqlen_q=w.seqlen_q)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
@@ -499,13 +505,14 @@ def run_ours(args):
                    "l2": f"{len(sets)} rotating input sets, KV "
                          f"{w.total_tokens * 576 * w.elem_bytes / 1e6:.0f} MB each (> 129 MB L2)",
                    "parallelism": f"replicas x{world}", "num_sm_parts": parts,
-                   "layout": args.layout},
+                   "layout": args.layout, "combine": args.combine},
         "effective_hbm_gbs": world * nbytes / (ms * 1e-3) / 1e9,
         "roofline": roofline,
         "e2e": {"value": job_tflops(world, flops, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": 3 * K,
+        # metadata, split and (unless fused) combine kernels per step
+        "gpu_launches": (2 if args.combine == "fused" else 3) * K,
         "clocks": clk,
         "kernel_source_hash": kernel_source_hash(),
     }

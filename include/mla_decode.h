@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 4
+#define MLA_ABI_VERSION 5
 
 /* Shape contract [TL §先看核心难点]: 576 = 512 latent + 64 RoPE; v = 512. */
 #define MLA_HEAD_DIM 576
@@ -106,7 +106,8 @@ typedef enum {
   MLA_WAIT_V_FULL = 13,      /* value: V data has arrived */
   MLA_WAIT_HDR_FULL = 14,    /* value: a rescale header has arrived */
   MLA_WAIT_O_DONE = 15,      /* value: the P.V MMAs of a superblock are done */
-  MLA_WAIT_STAGE_READY = 16  /* score: copier waits for staged P tiles */
+  MLA_WAIT_STAGE_READY = 16, /* score: copier waits for staged P tiles */
+  MLA_WAIT_GRID = 17         /* any CTA: the grid-wide barrier before the fused combine */
 } mla_wait_site;
 
 /*
@@ -223,6 +224,18 @@ typedef struct mla_fwd_params {
    * kv_cache, finite and > 0 */
   float q_scale;
   float kv_scale;
+
+  /* Nonzero: the split kernel combines the sequences it split itself [TL
+   * §变体内核, the persistent variant, which synchronises its split and combine
+   * phases grid-wide]: once every CTA of its grid has finished its parts and
+   * passed a grid-wide barrier, all of them run the combine, and no combine
+   * kernel is launched.  Zero: the combine kernel runs after the split kernel.
+   * Same results, bit for bit.  The barrier's two counters live in the
+   * workspace (mla_workspace_size) and need no initial value: each call tags
+   * them with its own number, and the last CTA to leave the barrier resets
+   * them for a replay of the same call (a captured CUDA graph).  After a call
+   * that reported MLA_ERR_DEVICE_TIMEOUT, re-capture such a graph. */
+  int32_t fused_combine;
 } mla_fwd_params;
 
 /* ABI version (MLA_ABI_VERSION) and sizeof(mla_fwd_params), for bindings. */
@@ -272,14 +285,15 @@ int mla_get_metadata(const int32_t *cache_seqlens, int b, int h, int num_sm,
                      void *stream);
 
 /* Workspace bytes for mla_decode_fwd: fp32 partial outputs and LSEs for up to
- * b + num_sm_parts splits of h query rows (heads, or seqlen_q * heads). */
+ * b + num_sm_parts splits of h query rows (heads, or seqlen_q * heads), then
+ * 256 bytes for the fused combine's grid barrier. */
 int mla_workspace_size(int b, int h, int num_sm_parts, size_t *bytes);
 
 /*
  * Paged split-KV MLA decode [TL §Split Kernel, §Combine Kernel, §变体内核;
  * FM §内存访问优化, §Softmax 计算优化].  Enqueues the split kernel (a
- * persistent grid of 2-CTA clusters walking the metadata) and the combine
- * kernel on `stream`.  Alignment: q, kv_cache, out, workspace (and q_pe,
+ * persistent grid of 2-CTA clusters walking the metadata) and, unless
+ * params->fused_combine is set, the combine kernel on `stream`.  Alignment: q, kv_cache, out, workspace (and q_pe,
  * k_pe when given) 16-byte aligned; all their strides multiples of 16 bytes
  * (8 elements; 16 for e4m3 q / kv_cache).  Row strides must cover the row: kv_row_stride >= 576 (>= 512
  * with k_pe), k_pe_row_stride >= 64, each page stride >= page_block_size

@@ -26,7 +26,7 @@ __all__ = [
 HEAD_DIM = 576
 HEAD_DIM_V = 512
 ROPE_DIM = HEAD_DIM - HEAD_DIM_V
-ABI_VERSION = 4
+ABI_VERSION = 5
 BLOCK_N = 64
 META_STRIDE = 8
 SCHED_FIXED_COST = 5
@@ -70,6 +70,7 @@ class FwdParams(ctypes.Structure):
         ("k_pe", _vp), ("k_pe_page_stride", _i64), ("k_pe_row_stride", _i64),
         ("is_causal", _i32),
         ("q_scale", ctypes.c_float), ("kv_scale", ctypes.c_float),
+        ("fused_combine", ctypes.c_int32),
     ]
 
 
@@ -234,7 +235,7 @@ def mla_workspace_size(b, h, num_sm_parts):
 def mla_decode_fwd(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                    tile_scheduler_metadata, num_splits, out=None, lse=None, workspace=None,
                    split_events=None, q_pe=None, k_pe=None, is_causal=False, q_scale=1.0,
-                   kv_scale=1.0):
+                   kv_scale=1.0, fused_combine=False):
     """Paged split-KV MLA decode (see prepare_decode for the argument contract).
 
     split_events: optional (begin, end) torch.cuda.Event pair recorded around the
@@ -243,7 +244,7 @@ def mla_decode_fwd(q, kv_cache, block_table, cache_seqlens, softmax_scale,
     call = prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                           tile_scheduler_metadata, num_splits, out, lse, workspace,
                           q_pe=q_pe, k_pe=k_pe, is_causal=is_causal, q_scale=q_scale,
-                          kv_scale=kv_scale)
+                          kv_scale=kv_scale, fused_combine=fused_combine)
     call(split_events=split_events)
     return call.out, call.lse
 
@@ -275,7 +276,8 @@ class DecodeCall:
 
 def prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                    tile_scheduler_metadata, num_splits, out=None, lse=None, workspace=None,
-                   q_pe=None, k_pe=None, is_causal=False, q_scale=1.0, kv_scale=1.0):
+                   q_pe=None, k_pe=None, is_causal=False, q_scale=1.0, kv_scale=1.0,
+                   fused_combine=False):
     """Paged split-KV MLA decode.
 
     q [b, 1, h, 576], kv_cache [num_pages, page_size, 1, 576] (fp16 or bf16, same
@@ -295,6 +297,11 @@ def prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
     head stride), out [b, s, h, 512], lse [b, s, h]; the cache already holds the s
     new tokens, and with is_causal token qi sees the cached tokens
     t < L - (s - 1 - qi).  The metadata must be made with seqlen_q = s.
+
+    fused_combine: the split kernel combines the sequences it split (after a
+    grid-wide barrier) instead of a separate combine kernel; same bits either way.
+    It saves the combine kernel's launch when nothing is split; when many
+    sequences are split the separate kernel (the default) is faster.
     """
     q_cols = HEAD_DIM_V if q_pe is not None else HEAD_DIM
     kv_cols = HEAD_DIM_V if k_pe is not None else HEAD_DIM
@@ -365,6 +372,7 @@ def prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
     p.dtype = _DTYPE_CODE[q.dtype]
     p.softmax_scale = float(softmax_scale)
     p.q_scale, p.kv_scale = float(q_scale), float(kv_scale)
+    p.fused_combine = 1 if fused_combine else 0
     p.q, p.q_batch_stride, p.q_head_stride = q.data_ptr(), q.stride(0), q.stride(2)
     p.kv_cache = kv_cache.data_ptr()
     p.kv_page_stride, p.kv_row_stride = kv_cache.stride(0), kv_cache.stride(1)
@@ -398,14 +406,15 @@ def mla_decode_fwd_timed(*args, split_events, **kw):
 
 def mla_decode_fwd_static(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                           tile_scheduler_metadata, num_splits, out=None, lse=None, q_pe=None,
-                          k_pe=None, is_causal=False, q_scale=1.0, kv_scale=1.0):
+                          k_pe=None, is_causal=False, q_scale=1.0, kv_scale=1.0, fused_combine=False):
     """mla_decode_fwd with the library's built-in per-device scratch
     (STATIC_WORKSPACE_BYTES) in place of a workspace tensor: the C call allocates
     nothing.  Calls on one device must not overlap on the GPU.  Returns (out, lse)."""
     no_ws = torch.empty((0,), dtype=torch.uint8, device=q.device)
     call = prepare_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale,
                           tile_scheduler_metadata, num_splits, out, lse, no_ws, q_pe=q_pe,
-                          k_pe=k_pe, is_causal=is_causal, q_scale=q_scale, kv_scale=kv_scale)
+                          k_pe=k_pe, is_causal=is_causal, q_scale=q_scale, kv_scale=kv_scale,
+                          fused_combine=fused_combine)
     lib = _load()
     with torch.cuda.device(call.device):
         rc = lib.mla_decode_fwd_static(ctypes.byref(call.params), _stream(call.device))

@@ -2,6 +2,7 @@
 // scheduler shape and the launch sequence (metadata -> split -> combine).
 #include <cuda_runtime.h>
 #include <math.h>
+#include <atomic>
 #include <mutex>
 #include <stdint.h>
 
@@ -57,11 +58,22 @@ void *static_workspace() {
 
 int max_splits_for(int b, int num_parts) { return b + num_parts; }
 
+// [oaccum][lseaccum, padded to 256 B][grid barrier: 256 B]
 size_t workspace_bytes_for(int b, int h, int num_parts) {
   size_t splits = (size_t)max_splits_for(b, num_parts);
   size_t o = splits * (size_t)h * MLA_HEAD_DIM_V * sizeof(float);
   size_t l = splits * (size_t)h * sizeof(float);
-  return o + ((l + 255) & ~(size_t)255);
+  return o + ((l + 255) & ~(size_t)255) + 256;
+}
+
+// A tag per call for the fused combine's barrier counters, never 0.
+static uint32_t next_token() {
+  static std::atomic<uint32_t> counter{0};
+  uint32_t t;
+  do {
+    t = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  } while (t == 0);
+  return t;
 }
 
 }  // namespace mla
@@ -256,6 +268,14 @@ int resolve_args(const mla_fwd_params *p, FwdArgs &a) {
                                          (size_t)a.max_splits * rows * MLA_HEAD_DIM_V * sizeof(float));
   a.err = err;
   a.forced_timeout = 0;
+  a.fused_combine = p->fused_combine != 0;
+  a.token = next_token();
+  {
+    const size_t o = (size_t)a.max_splits * rows * MLA_HEAD_DIM_V * sizeof(float);
+    const size_t l = (size_t)a.max_splits * rows * sizeof(float);
+    a.grid_bar = reinterpret_cast<unsigned long long *>(static_cast<char *>(p->workspace) + o +
+                                                        ((l + 255) & ~(size_t)255));
+  }
   return MLA_OK;
 }
 
@@ -274,7 +294,7 @@ int mla_decode_fwd_timed(const mla_fwd_params *p, void *stream, void *split_begi
   if (launch_split_tc(a, s) != cudaSuccess) return MLA_ERR_CUDA;
   if (split_end && cudaEventRecord(static_cast<cudaEvent_t>(split_end), s) != cudaSuccess)
     return MLA_ERR_CUDA;
-  if (launch_combine(a, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (!a.fused_combine && launch_combine(a, s) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }
 

@@ -45,6 +45,9 @@ struct FwdArgs {
   int max_splits;
   int *err;         // device error word (two ints: code, detail)
   int forced_timeout;  // test hook: load warps idle, the K wait gives up after 1 ms
+  int fused_combine;   // the split kernel combines split sequences after a grid barrier
+  uint32_t token;      // this call's tag for the barrier counters (never 0)
+  unsigned long long *grid_bar;  // workspace: {arrivals, departures}, tag in the high half
 };
 
 int max_splits_for(int b, int num_parts);

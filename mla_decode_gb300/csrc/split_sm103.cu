@@ -55,6 +55,7 @@
 
 #include <cuda_fp8.h>
 
+#include "combine.cuh"
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -1219,6 +1220,87 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
   }
 }
 
+// ------------------------------------------------------------------------------ fused combine
+
+// The grid barrier's counters: the high half of each word is the call's tag, the
+// low half a count.  The first CTA retags both words at its start when they hold
+// another call's tag (a fresh workspace holds anything); every CTA waits for its
+// call's tag before it counts itself in with one atomic add (a compare-and-swap
+// loop here, with ~150 CTAs arriving together, took ~100 us).  The last CTA out
+// sets both counts back to zero, so a replay of the same launch (same tag) starts
+// from zero.
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void grid_bar_retag(unsigned long long *w, unsigned long long tag) {
+  const unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(w);
+  if ((old & 0xffffffff00000000ull) != tag) atomicCAS(w, old, tag);
+}
+
+// Waits (bounded) until pred(word) holds; false on timeout (reported).
+template <typename Pred>
+__device__ __forceinline__ bool grid_bar_wait(const FwdArgs &a, const unsigned long long *w, Pred pred) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!pred(ld_acquire_gpu(w))) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      report_error(a.err, MLA_ERR_DEVICE_TIMEOUT, MLA_WAIT_GRID);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
+// The persistent variant of the TileLang kernels synchronises its split and
+// combine phases grid-wide ("用 TileLang 编写高性能 DeepSeek MLA 内核…", section
+// 变体内核).  Here: every CTA arrives once its parts are done (its partial
+// outputs and LSEs fenced first), waits (bounded) for all CTAs of the grid, and
+// then the grid's warps share the combine of every split sequence, one 32-row x
+// 32-column block per warp at a time.  The whole grid is resident (one CTA per
+// SM, at most one part per cluster that fits), so the barrier does not wait on
+// CTAs that have not started.
+template <typename T>
+__device__ __noinline__ void combine_phase(const FwdArgs &a, uint8_t *smem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned long long ctas = (unsigned long long)gridDim.x * gridDim.y;
+  const unsigned long long tag = (unsigned long long)a.token << 32;
+  auto tagged = [tag](unsigned long long v) { return (v & 0xffffffff00000000ull) == tag; };
+  __shared__ int passed;
+  __threadfence();  // this thread's partial outputs and LSEs, before the arrival
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool ok = grid_bar_wait(a, a.grid_bar, tagged);
+    if (ok) {
+      atomicAdd(a.grid_bar, 1ull);
+      ok = grid_bar_wait(a, a.grid_bar, [tag, ctas](unsigned long long v) { return v == tag + ctas; });
+    }
+    passed = ok ? 1 : 0;
+  }
+  __syncthreads();
+  if (!passed) return;
+  __threadfence();
+  uint4 (*tile)[4] = reinterpret_cast<uint4 (*)[4]>(smem + warp * 2048);
+  const int per_seq = ((a.h + 31) / 32) * 16;  // 32-row groups x 32-column blocks
+  const int64_t blocks = (int64_t)a.b * per_seq;
+  const int64_t warps = (int64_t)ctas * (kThreads / 32);
+  const int64_t u0 = (int64_t)(blockIdx.y * gridDim.x + blockIdx.x) * (kThreads / 32) + warp;
+  for (int64_t u = u0; u < blocks; u += warps) {
+    const int seq = (int)(u / per_seq), rem = (int)(u % per_seq);
+    const int s0 = a.num_splits[seq], n = a.num_splits[seq + 1] - s0;
+    if (n <= 1) continue;
+    combine_block<OutT<T>>(a, seq, s0, n, 32 * (rem >> 4), kCombineChunks * (rem & 15), tile, lane);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && grid_bar_wait(a, a.grid_bar + 1, tagged) &&
+      atomicAdd(a.grid_bar + 1, 1ull) + 1 == tag + ctas) {
+    atomicExch(a.grid_bar, tag);
+    atomicExch(a.grid_bar + 1, tag);
+  }
+}
+
 // ------------------------------------------------------------------------------ kernel
 
 template <typename T>
@@ -1292,6 +1374,10 @@ split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant
   // read only after it has completed
   grid_dependency_wait();
   launch_dependents();
+  if (a.fused_combine && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    grid_bar_retag(a.grid_bar, (unsigned long long)a.token << 32);
+    grid_bar_retag(a.grid_bar + 1, (unsigned long long)a.token << 32);
+  }
   const uint32_t tmem = b->tmem_base;
   const Ctx c{b, a.err, kWaitLimitNs};
 
@@ -1340,6 +1426,9 @@ split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // several splits in some sequence: the grid combines them (shared memory is free:
+  // every load and copy into it has been consumed)
+  if (a.fused_combine && a.num_splits[a.b] > a.b) combine_phase<T>(a, smem);
 }
 
 // ------------------------------------------------------------------------------ host

@@ -63,14 +63,15 @@ def scales(inputs):
     return dict(q_scale=inputs.get("q_scale", 1.0), kv_scale=inputs.get("kv_scale", 1.0))
 
 
-def run_gpu(inputs, heads, scale, num_sm=None, is_causal=False):
+def run_gpu(inputs, heads, scale, num_sm=None, is_causal=False, fused_combine=False):
     import mla_decode_gb300 as mla
     s_q = inputs["q"].shape[1]
     meta, num_splits = mla.mla_get_metadata(inputs["cache_seqlens"], heads, num_sm,
                                             seqlen_q=s_q)
     out, lse = mla.mla_decode_fwd(inputs["q"], inputs["kv_cache"], inputs["block_table"],
                                   inputs["cache_seqlens"], scale, meta, num_splits,
-                                  is_causal=is_causal, **scales(inputs))
+                                  is_causal=is_causal, fused_combine=fused_combine,
+                                  **scales(inputs))
     code, detail = mla.mla_get_device_error()
     assert code == 0, f"device error {code} ({mla.mla_status_string(code)}), detail {detail}"
     return out, lse, meta, num_splits
@@ -243,10 +244,11 @@ def _log(w, name, stats, num_sm=None):
                                 "num_sm": num_sm, **stats}) + "\n")
 
 
-def check_workload(w, seqs=None, num_sm=None, poison_tail=False, inputs=None):
+def check_workload(w, seqs=None, num_sm=None, poison_tail=False, inputs=None, fused_combine=False):
     if inputs is None:
         inputs = workloads.make_inputs(w, device="cuda", poison_tail=poison_tail)
-    out, lse, meta, ns = run_gpu(inputs, w.heads, w.softmax_scale, num_sm, is_causal=w.causal)
+    out, lse, meta, ns = run_gpu(inputs, w.heads, w.softmax_scale, num_sm, is_causal=w.causal,
+                                 fused_combine=fused_combine)
     stats = compare_chunked(w, inputs, [("out", out, lse)], seqs)["out"]
     return stats, out, lse, meta, ns, inputs
 

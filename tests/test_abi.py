@@ -45,7 +45,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_params_struct_matches(lib):
     import mla_decode_gb300 as m
     assert lib.mla_fwd_params_size() == ctypes.sizeof(m.FwdParams)
-    assert lib.mla_abi_version() == m.ABI_VERSION == 4
+    assert lib.mla_abi_version() == m.ABI_VERSION == 5
 
 
 def test_status_strings(lib):
@@ -76,8 +76,10 @@ def test_workspace_size(lib):
     import mla_decode_gb300 as m
     n = m.mla_workspace_size(64, 128, 76)
     splits = 64 + 76
-    assert n >= splits * 128 * 512 * 4 + splits * 128 * 4
-    assert n < splits * 128 * 512 * 4 + splits * 128 * 4 + 512
+    # partials, LSEs (padded to 256 bytes), then the fused combine's two 8-byte
+    # barrier counters in a 256-byte tail
+    assert n >= splits * 128 * 512 * 4 + splits * 128 * 4 + 16
+    assert n < splits * 128 * 512 * 4 + splits * 128 * 4 + 768
 
 
 def good_params():

@@ -1,0 +1,84 @@
+"""GPU: the split kernel's own combine phase (fused_combine, a grid-wide barrier
+between the split and combine phases, as in the persistent variant of the TileLang
+kernels) against the separate combine kernel and the oracle: the same bits, on
+batches whose sequences the scheduler splits, in every dtype; and its barrier
+counters, which carry no initial value, under workspace garbage and CUDA graph
+replays of one captured call."""
+import pytest
+import torch
+
+import workloads
+from tests import _parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from mla_decode_gb300 import _build
+    _build.build()
+    import mla_decode_gb300 as mla
+    mla._load()
+
+
+def _uneven(dtype, seed):
+    # lengths the scheduler splits unevenly (several sequences over several parts),
+    # plus an empty sequence and a one-token one
+    return workloads.custom(6, 128, (9000, 0, 3000, 1, 12000, 700), dtype, seed=seed,
+                            name=f"fused_{dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "e4m3"])
+@pytest.mark.parametrize("num_sm", [8, 20, 64, None])
+def test_fused_combine_matches_combine_kernel_bitwise(dtype, num_sm):
+    w = _uneven(dtype, 500 + num_sm if num_sm else 499)
+    inputs = workloads.make_inputs(w, "cuda")
+    out_f, lse_f, meta, ns = P.run_gpu(inputs, w.heads, w.softmax_scale, num_sm=num_sm,
+                                       fused_combine=True)
+    out_k, lse_k, *_ = P.run_gpu(inputs, w.heads, w.softmax_scale, num_sm=num_sm,
+                                 fused_combine=False)
+    assert int(ns[-1]) > w.batch, "the case must split some sequence"
+    assert torch.equal(out_f.view(torch.int16), out_k.view(torch.int16))
+    assert torch.equal(lse_f.view(torch.int32), lse_k.view(torch.int32))
+
+
+def test_fused_combine_against_oracle_many_splits():
+    # one long sequence over every part of the grid: the widest combine
+    w = workloads.custom(1, 128, (40000,), "bf16", seed=77, name="fused_wide")
+    stats, out, lse, meta, ns, _ = P.check_workload(w, fused_combine=True)
+    assert int(ns[-1]) > 8
+
+
+def test_fused_combine_garbage_workspace_and_graph_replays():
+    import mla_decode_gb300 as mla
+    w = _uneven("bf16", 321)
+    x = workloads.make_inputs(w, "cuda")
+    meta, ns = mla.mla_get_metadata(x["cache_seqlens"], w.heads, 20)
+    assert int(ns[-1]) > w.batch
+    need = mla.mla_workspace_size(w.batch, w.rows, meta.shape[0])
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")  # counters hold garbage
+    call = mla.prepare_decode(x["q"], x["kv_cache"], x["block_table"], x["cache_seqlens"],
+                              w.softmax_scale, meta, ns, workspace=ws, fused_combine=True)
+    ref_o, ref_l, *_ = P.run_gpu(x, w.heads, w.softmax_scale, num_sm=20, fused_combine=False)
+    call()
+    torch.cuda.synchronize()
+    assert torch.equal(call.out, ref_o) and torch.equal(call.lse, ref_l)
+    # one captured call, replayed: the same tag each time, so the counters must come
+    # back to zero after every run
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()  # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        call()
+    for _ in range(4):
+        call.out.zero_()
+        call.lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(call.out, ref_o) and torch.equal(call.lse, ref_l)
+    code, detail = mla.mla_get_device_error()
+    assert code == 0, f"device error {code} detail {detail}"
