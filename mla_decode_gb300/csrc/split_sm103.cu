@@ -285,15 +285,15 @@ __device__ __forceinline__ void finish_sb_pages(const FwdArgs &a, int seq, int n
 }
 
 template <typename T> struct Pack;
-// two(lo, hi): a packed pair of 16-bit values; sum(u): the sum of a packed pair,
-// as floats (the values the MMA reads).
+// two(lo, hi): a packed pair of 16-bit values; unpack(u): the pair as floats (the
+// values the MMA reads).
 template <> struct Pack<__nv_bfloat16> {
   static __device__ __forceinline__ uint32_t two(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
   }
-  static __device__ __forceinline__ float sum(uint32_t u) {
-    return __uint_as_float(u << 16) + __uint_as_float(u & 0xffff0000u);
+  static __device__ __forceinline__ float2 unpack(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
   }
   static constexpr bool kBf16 = true;
 };
@@ -302,9 +302,8 @@ template <> struct Pack<__half> {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
   }
-  static __device__ __forceinline__ float sum(uint32_t u) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u));
-    return f.x + f.y;
+  static __device__ __forceinline__ float2 unpack(uint32_t u) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(&u));
   }
   static constexpr bool kBf16 = false;
 };
@@ -787,22 +786,10 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       }
       // eight independent partial maxima (and sums below): 64-long dependent
       // chains would leave the warp waiting on instruction latency
-      float mloc;
-      if constexpr (kIsF8<T>) {
-        // the extreme of the raw scores, scaled once (the scale may be negative):
-        // three-input max / min, two new scores per instruction
-        mloc = sc >= 0.f ? sc * extreme3<true>(v) : sc * extreme3<false>(v);
-      } else {
-        float mp[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(v[i][e]) * sc);
-        mloc = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                     fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-      }
+      // the extreme of the raw scores, scaled once (the scale may be negative; a
+      // product rounds monotonically, so this is the largest scaled score):
+      // three-input max / min, two new scores per instruction
+      const float mloc = sc >= 0.f ? sc * extreme3<true>(v) : sc * extreme3<false>(v);
       float *rmax = red_max + (sb & 1) * 256;
       rmax[half * 128 + r] = mloc;
       if (bar_red_or(1, 256, !ok || c.aborted())) return;  // all softmax threads leave together
@@ -815,11 +802,9 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
       // the staging slot's previous superblock must have left for the value CTA
       if (ok && sb >= G::kNStage)
         ok = wait_bar<false>(c, &b->stage_free[buf], (sb / G::kNStage - 1) & 1, W_STAGE_FREE);
-      float ps[8], pr[4];
+      float ps[8], pr[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) ps[e] = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) pr[e] = 0.f;
+      for (int e = 0; e < 8; ++e) ps[e] = pr[e] = 0.f;
       const bool write = ok && half < np;
       // a row that has seen no token yet (causal rows only) has m_ref = -inf: its
       // weights are exp2(-inf) = 0, not exp2(-inf + inf)
@@ -857,27 +842,38 @@ __device__ void score_softmax(const FwdArgs &a, uint8_t *smem, const Ctx &c, int
           ps[2 * e + 1] = s2[e].y;
         }
       } else {
+        // pairs of scores through the packed fp32x2 FMA / add; the rounded weights'
+        // sums (what the MMA multiplies) likewise, eight running sums each
         const uint32_t row = smem_u32(stage + half * G::kPTile) + r * 128;
+        const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(nm, nm);
+        float2 s2[4], r2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s2[e] = r2[e] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
-          float p[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            p[e] = fast_exp2(fmaf(__uint_as_float(v[ch >> 2][(ch & 3) * 8 + e]), sc, nm));
-            ps[e] += p[e];
-          }
           uint32_t u[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            u[e] = Pack<T>::two(p[2 * e], p[2 * e + 1]);
-            pr[e] += Pack<T>::sum(u[e]);
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t *x = &v[ch >> 2][(ch & 3) * 8 + 2 * q];
+            float2 p = __ffma2_rn(make_float2(__uint_as_float(x[0]), __uint_as_float(x[1])), sc2, nm2);
+            p = make_float2(fast_exp2(p.x), fast_exp2(p.y));
+            s2[q] = __fadd2_rn(s2[q], p);
+            u[q] = Pack<T>::two(p.x, p.y);
+            r2[q] = __fadd2_rn(r2[q], Pack<T>::unpack(u[q]));
           }
           if (write) st_shared_v4(row + ((ch ^ (r & 7)) << 4), u[0], u[1], u[2], u[3]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          ps[2 * e] = s2[e].x;
+          ps[2 * e + 1] = s2[e].y;
+          pr[2 * e] = r2[e].x;
+          pr[2 * e + 1] = r2[e].y;
         }
       }
       l = l * alpha + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
       if constexpr (kIsF8<T>) lr = l;
-      else lr = lr * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+      else lr = lr * alpha + (((pr[0] + pr[1]) + (pr[2] + pr[3])) + ((pr[4] + pr[5]) + (pr[6] + pr[7])));
       Header *hdr = reinterpret_cast<Header *>(stage + 2 * G::kPTile);
       if (last) {  // the row's totals: both halves' sums
         red_sum[half * 128 + r] = l;
