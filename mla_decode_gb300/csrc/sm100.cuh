@@ -195,6 +195,18 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_
       : "memory");
 }
 
+// Shared -> global TMA store of one box (bulk-group completion): the caller
+// commits the group and waits for it before the source is reused.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tmap),
+               "r"(c0), "r"(c1), "r"(c2), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed bulk group of this thread has completed (its
+// global writes done, its shared-memory sources read).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // One lane of the (fully active) warp; the rest get false.
 __device__ __forceinline__ bool elect_one() {
   uint32_t p;

@@ -149,8 +149,10 @@ struct Geo {
   static constexpr int kScoreEnd = kOffRed + 8 * 128 * 4;
   static constexpr int kOffV = 0;                                      // value: V ring
   static constexpr int kOffPRing = kOffV + kNV * kVSlot;               // value: superblock slots
-  static constexpr int kOffEpi = kOffPRing + kNPSB * kSBSlot;          // value: 8 x 2 KB
-  static constexpr int kValueEnd = kOffEpi + 8 * 2048;                 // epilogue staging, one per warp
+  static constexpr int kValueEnd = kOffPRing + kNPSB * kSBSlot;
+  // the epilogue of a part's last segment stages `out` in the (then idle) V ring:
+  // 16 KB per correction warp
+  static_assert(kNV * kVSlot >= 8 * 16384, "epilogue staging in the V ring");
   static constexpr int kOffBars = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 127) & ~127;
   static constexpr int kSmemBytes = kOffBars + (int)sizeof(Bars) + 1024;  // + alignment slack
   static_assert(kNK <= kNKMax && kNV <= kNVMax && kNPSB <= kNPSBMax && kNStage <= kNStageMax,
@@ -247,6 +249,8 @@ struct SegWalk {
     ++split;
     return true;
   }
+  // no segment follows the one next() returned last
+  __device__ bool done() const { return !(seq < end_seq || (seq == end_seq && blk < end_blk)); }
 };
 
 
@@ -1060,7 +1064,8 @@ __device__ void value_receiver(const FwdArgs &a, const Ctx &c, int part) {
 // epilogue of one segment took ~10 us at ~26 GB/s.)
 template <typename T>
 __device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int nsplit, int head,
-                                       bool head_ok, int g, uint32_t tO, float lrow, uint32_t epi) {
+                                       bool head_ok, int g, uint32_t tO, float lrow, uint32_t stage,
+                                       const CUtensorMap *omap) {
   using O = OutT<T>;
   // o_scale: the value dequantisation scale (e4m3 caches), 1 otherwise
   const float inv = lrow > 0.f ? a.o_scale / lrow : 0.f;
@@ -1086,6 +1091,39 @@ __device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int
       }
       if (q < 7) tmem_wait_ld_regs(x[(q + 1) & 1]);
     }
+    return;
+  }
+  if (stage) {
+    // the part's last segment (the V ring is free): the warp's 32 rows x 256 columns
+    // go to its 16 KB of the ring as four [32 rows x 64 columns] boxes with the
+    // 128-byte swizzle (16-byte piece j of row r at j ^ (r & 7): no bank
+    // conflicts) and leave as four TMA stores; rows past h are clipped by the map
+    uint32_t w[2][32];
+    tmem_ld32(tO, w[0]);
+    tmem_wait_ld_regs(w[0]);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (q < 7) tmem_ld32(tO + 32 * (q + 1), w[(q + 1) & 1]);
+      uint32_t hv[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        hv[e] = Pack<O>::two(__uint_as_float(w[q & 1][2 * e]) * inv, __uint_as_float(w[q & 1][2 * e + 1]) * inv);
+      const uint32_t row = stage + (q >> 1) * 4096 + lane * 128;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        st_shared_v4(row + ((((q & 1) * 4 + k) ^ (lane & 7)) << 4), hv[4 * k], hv[4 * k + 1], hv[4 * k + 2],
+                     hv[4 * k + 3]);
+      if (q < 7) tmem_wait_ld_regs(w[(q + 1) & 1]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) tma_store_3d(omap, stage + k * 4096, 256 * g + 64 * k, row0, seq);
+      bulk_commit_group();
+      bulk_wait_all();
+    }
+    __syncwarp();
     return;
   }
   // one split: each thread writes its own row's 16-bit values, 32 columns (64 B) at a
@@ -1118,8 +1156,6 @@ __device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int
     }
     if (q < 7) tmem_wait_ld_regs(w[(q + 1) & 1]);
   }
-  (void)epi;
-  (void)lane;
 }
 
 // The zero output row half of an empty sequence (its lse is -inf).
@@ -1137,7 +1173,7 @@ __device__ __noinline__ void zero_out(const FwdArgs &a, int seq, int split, int 
 
 template <typename T>
 __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, int part,
-                                 uint32_t tmem, int head0) {
+                                 uint32_t tmem, int head0, const CUtensorMap *omap) {
   using G = GeoOf<T>;
   Bars *b = c.bars;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1205,10 +1241,14 @@ __device__ void value_correction(const FwdArgs &a, uint8_t *smem, const Ctx &c, 
       mbar_arrive(&b->o_ready[g][sb & 1]);
       if (flags & 2u) {  // epilogue
         if (ok) ok = wait_done((int)sb);
+        // one split and nothing after this segment: `out` leaves by TMA stores from
+        // the V ring, once both halves' MMAs are done with it
+        const bool staged = s.nsplit == 1 && walk.done();
+        if (ok && staged) ok = wait_bar<false>(c, &b->o_done[1 - g][sb & 1], (sb >> 1) & 1, W_O_DONE);
         if (bar_red_or(bar_id, 128, !ok || c.aborted())) return;
         tc_fence_after();
         write_out<T>(a, s.seq, s.split, s.nsplit, head, head_ok, g, tO, lrow,
-                     smem_u32(smem + G::kOffEpi + (warp - 2) * 2048));
+                     staged ? smem_u32(smem + G::kOffV + (warp - 2) * 16384) : 0u, omap);
         tc_fence_before();
         mbar_arrive(&b->o_free);
       }
@@ -1304,7 +1344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap q_map,
                 const __grid_constant__ CUtensorMap kpe_map,
                 const __grid_constant__ CUtensorMap qpe_map,
-                const __grid_constant__ CUtensorMap kv4_map, const FwdArgs a) {
+                const __grid_constant__ CUtensorMap kv4_map, const __grid_constant__ CUtensorMap o_map,
+                const FwdArgs a) {
   using G = GeoOf<T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1356,6 +1397,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant
     tma_prefetch_desc(&kpe_map);
     tma_prefetch_desc(&qpe_map);
     tma_prefetch_desc(&kv4_map);
+    tma_prefetch_desc(&o_map);
   }
   if (warp == 1) {
     tmem_alloc(&b->tmem_base, 512);
@@ -1402,7 +1444,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant
     } else if (warp == 1 || warp == 11) {
       value_mma<T>(a, smem, c, part, tmem, warp == 1 ? 0 : 1);
     } else if (warp < 10) {
-      value_correction<T>(a, smem, c, part, tmem, head0);
+      value_correction<T>(a, smem, c, part, tmem, head0, &o_map);
     } else {
       value_receiver<T>(a, c, part);
     }
@@ -1511,7 +1553,7 @@ cudaError_t make_block_map(CUtensorMap *m, const void *base, uint32_t block_cols
 template <typename T>
 cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
   constexpr uint64_t kLatent = MLA_HEAD_DIM_V, kRope = MLA_HEAD_DIM - MLA_HEAD_DIM_V;
-  CUtensorMap kmap, qmap, pemap, qpemap, map4;
+  CUtensorMap kmap, qmap, pemap, qpemap, map4, omap;
   cudaError_t e;
   if constexpr (kIsF8<T>) {
     // e4m3, RoPE columns inside the rows (the host rejects separate tensors).
@@ -1545,6 +1587,10 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
       e = make_map<T>(&qpemap, a.q_pe, kRope, a.h, a.b, a.q_pe_head_stride, a.q_pe_batch_stride, 64,
                       128);
   }
+  // out as [b][rows][512] 16-bit, boxes of 32 rows x 64 columns (the epilogue's TMA
+  // stores; rows past h are not written)
+  if (e == cudaSuccess)
+    e = make_map<OutT<T>>(&omap, a.out, MLA_HEAD_DIM_V, a.h, a.b, a.o_head_stride, a.o_batch_stride, 64, 32);
   if (e != cudaSuccess) return e;
   if ((e = smem_attr<T>()) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1561,7 +1607,7 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, split_tc_kernel<T>, kmap, qmap, pemap, qpemap, map4, a);
+  return cudaLaunchKernelEx(&cfg, split_tc_kernel<T>, kmap, qmap, pemap, qpemap, map4, omap, a);
 }
 
 }  // namespace
