@@ -16,6 +16,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace mla {
 
@@ -31,11 +32,14 @@ __device__ __forceinline__ void combine_block(const FwdArgs &a, int seq, int s0,
   // loads are in flight while it runs
   const float4 *base = reinterpret_cast<const float4 *>(a.oaccum) + (int64_t)c0 * a.h + head;
   const int64_t split_stride = (int64_t)128 * a.h;  // float4s between splits
+  // each partial row is read once: its L2 lines go first (the split kernel wrote
+  // them with evict_last)
+  const uint64_t drop = sm100::l2_policy_evict_first();
   auto load = [&](int k, float4 (&v)[kCombineChunks]) {
     const float4 *src = base + (int64_t)(s0 + k) * split_stride;
 #pragma unroll
     for (int c = 0; c < kCombineChunks; ++c)
-      v[c] = hv ? src[(int64_t)c * a.h] : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[c] = hv ? sm100::ld_global_v4_hint(src + (int64_t)c * a.h, drop) : make_float4(0.f, 0.f, 0.f, 0.f);
   };
   // the LSEs of the first kCombineLse splits are loaded together with the first
   // two partial rows (one memory round trip for the common case)

@@ -1074,7 +1074,9 @@ __device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int
   if (nsplit != 1) {
     // partials: the next 32 columns' TMEM load is in flight while the current ones
     // are stored
+    // kept in L2 (evict_last) until the combine reads them, across the KV stream
     float4 *o = reinterpret_cast<float4 *>(a.oaccum) + ((int64_t)split * 128 + 64 * g) * a.h + head;
+    const uint64_t keep = l2_policy_evict_last();
     uint32_t x[2][32];
     tmem_ld32(tO, x[0]);
     tmem_wait_ld_regs(x[0]);
@@ -1085,8 +1087,10 @@ __device__ __noinline__ void write_out(const FwdArgs &a, int seq, int split, int
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t *v = &x[q & 1][4 * k];
-          o[(int64_t)(8 * q + k) * a.h] = make_float4(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv,
-                                                      __uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
+          st_global_v4_hint(o + (int64_t)(8 * q + k) * a.h,
+                            make_float4(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv,
+                                        __uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                            keep);
         }
       }
       if (q < 7) tmem_wait_ld_regs(x[(q + 1) & 1]);
