@@ -127,6 +127,10 @@ def configs():
                           softmax_scale=192 ** -0.5, seed=1),
         "split": Workload("split", 128, 128, (8192,) * 128, "fp16", page_size=64,
                           softmax_scale=576 ** -0.5, seed=2),
+        # the far corner of the paged bf16 target range (batch 64-128 x 4-8K cache):
+        # the paged shape at twice the batch and twice the cache
+        "paged_8k": Workload("paged_8k", 128, 128, (8192,) * 128, "bf16", page_size=64,
+                             softmax_scale=192 ** -0.5, seed=22),
         "varlen": Workload("varlen", 128, 128, _varlen_lengths(128, 1, 16384, 3), "bf16",
                            page_size=64, softmax_scale=192 ** -0.5, seed=3),
         "mqa": Workload("mqa", 256, 16, (32768,) * 256, "bf16", page_size=64,
