@@ -21,8 +21,9 @@
 // part is served by a cluster of two CTAs with different roles:
 //   * score CTA (cluster rank 0): all 576 Q columns live in TMEM as the A operand
 //     (packed 16-bit pairs, columns 0..287).  K streams through a ring of whole
-//     pages (one TMA request per page: 64 rows x 576 columns as nine swizzled
-//     64-column atoms), and per page S = Q K^T is 36 MMAs of M=128 x N=64 x K=16
+//     pages (64 rows x 576 columns as nine swizzled 64-column atoms, in two TMA
+//     requests, atoms 0..3 and 4..8, each part filled and released on its own),
+//     and per page S = Q K^T is 36 MMAs of M=128 x N=64 x K=16
 //     into one of three page accumulators in TMEM (so the MMAs run a superblock
 //     ahead of the softmax).  A superblock is two pages.  Eight softmax warps (one
 //     64-token page each per head row) keep a lazy running max (the reference max
@@ -35,14 +36,15 @@
 //     of the value rows with exactly the weights the MMAs applied.
 //   * value CTA (rank 1): O lives in TMEM as two 256-column halves.  Its own TMA
 //     stream brings each page's value columns (one 4-D box of four atoms per
-//     256 columns); for each superblock it issues all
-//     M=128 x N=256 x K=16 MMAs of half 0 (P from shared memory, K-major, as A;
-//     V from shared memory, N-major, as B), then those of half 1.  Two groups of
+//     256 columns); per superblock one MMA warp per O half issues that half's
+//     M=128 x N=256 x K=16 MMAs (P from shared memory, K-major, as A; V from
+//     shared memory, N-major, as B).  Two groups of
 //     four correction warps, one per half, rescale their half of O when the
 //     score CTA moved its reference max, so one half is rescaled while the
-//     other half's MMAs still run, and write the epilogue (O / l to out through
-//     a shared-memory staging tile, or to the split workspace, whose rows are
-//     interleaved per 4-column chunk so that a warp writes 512 contiguous bytes).
+//     other half's MMAs still run, and write the epilogue: O / l to out as
+//     32-byte row stores (at a part's last segment through the idle V ring and
+//     TMA stores), or to the split workspace, whose rows are interleaved per
+//     4-column chunk so that a warp writes 512 contiguous bytes.
 // Every wait is bounded; a wait that runs out records MLA_ERR_DEVICE_TIMEOUT
 // with the wait site as detail, and the CTA unwinds.
 #include <cuda.h>
@@ -114,7 +116,7 @@ struct Bars {
 //    16-bit with the 128-byte swizzle; a V tile is one O half of one page, four
 //    [64 x 64] atoms (32 KB).
 //  e4m3 (kind::f8f6f4): a K ring entry is nine [64 rows x 64 B] atoms with the
-//    64-byte swizzle (36 KB, one TMA request), so the ring holds five pages; Q
+//    64-byte swizzle (36 KB, one TMA request), and the ring holds four pages; Q
 //    takes TMEM columns 0..127 and 128..143; P tiles are [128 x 64] bytes with the
 //    64-byte swizzle (8 KB); a V tile is two [64 rows x 128 B] atoms (16 KB).
 template <bool kF8>
@@ -427,13 +429,14 @@ __device__ __forceinline__ void issue_job(const FwdArgs &a, SbWalk &w, SbJob &j)
 
 // ------------------------------------------------------------------------------ score CTA
 
-// K producer.  Each 64-token page of K arrives as ONE TMA request: a 4-D box of
-// the page's rows x all 576 columns, landing as nine swizzled [64 rows x 64
-// columns] atoms back to back (72 KB, one ring entry).  A TMA request carries a
-// fixed cost of a few hundred nanoseconds, so one SM streams whole pages at
-// 80-90 GB/s where [64 x 64] boxes (8 KB) reach about 24.  With Q_pe / K_pe as
-// separate tensors the entry is two requests: the 512 latent columns (eight
-// atoms) and the 64 RoPE columns.  At a segment start the ring first carries
+// K producer.  A 64-token page of K lands as nine swizzled [64 rows x 64 columns]
+// atoms back to back (72 KB, one ring entry), in large 4-D TMA requests: a
+// request carries a fixed cost of a few hundred nanoseconds, so one SM streams
+// whole pages at 80-90 GB/s where [64 x 64] boxes (8 KB) reach about 24.  e4m3:
+// one request per page (36 KB).  16-bit: two, atoms 0..3 and atoms 4..8 (with
+// Q_pe / K_pe separate, latent atoms 4..7 plus the K_pe box), each part with its
+// own barriers, so the next page's first part streams in while this page's
+// second part is still being multiplied.  At a segment start the ring first carries
 // that sequence's Q, which the MMA warp moves into TMEM: the 512 latent columns
 // as eight [128 heads x 64] boxes, four per entry, then the 64 RoPE columns.
 // Heads past h read as zeros.  The part's first segment starts from an empty
@@ -1055,10 +1058,9 @@ __device__ void value_receiver(const FwdArgs &a, const Ctx &c, int part) {
 
 // Epilogue of one thread's head row and O half: O / l from TMEM to `out` (one
 // split) or to the fp32 split workspace.  Once per segment, so out of line.
-// Rows of `out` are 1 KB apart, so the 16-bit results pass through the warp's
-// 2 KB staging tile (`epi`, [32 rows][64 B], 16-byte pieces at j ^ ((row >> 1) & 3):
-// no bank conflicts) and leave as 64-byte row pieces, eight rows per store.
-// The workspace holds the partial outputs as [split][128 column chunks][h rows]
+// `out` (16-bit): with `stage` (a part's last segment) through the warp's 16 KB
+// of the idle V ring and four TMA stores, else as the thread's own 32-byte row
+// stores.  The workspace holds the partial outputs as [split][128 column chunks][h rows]
 // [4 floats]: a warp's 32 consecutive rows write 512 contiguous bytes per chunk.
 // (Row-major partials made every warp store touch 32 rows 2 KB apart, and the
 // epilogue of one segment took ~10 us at ~26 GB/s.)
