@@ -49,6 +49,14 @@ def test_fused_combine_against_oracle_many_splits():
     assert int(ns[-1]) > 8
 
 
+def test_fused_combine_varlen_full_size():
+    # the serving-like batch (128 sequences of 1..16384 tokens, many split) with the
+    # grid-synchronised combine: every sequence and head against the oracle
+    w = workloads.get("varlen")
+    stats, out, lse, meta, ns, _ = P.check_workload(w, fused_combine=True)
+    assert int(ns[-1]) > w.batch
+
+
 def test_fused_combine_garbage_workspace_and_graph_replays():
     import mla_decode_gb300 as mla
     w = _uneven("bf16", 321)
