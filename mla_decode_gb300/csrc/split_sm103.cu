@@ -116,7 +116,7 @@ struct Bars {
 //    16-bit with the 128-byte swizzle; a V tile is one O half of one page, four
 //    [64 x 64] atoms (32 KB).
 //  e4m3 (kind::f8f6f4): a K ring entry is nine [64 rows x 64 B] atoms with the
-//    64-byte swizzle (36 KB, one TMA request), and the ring holds four pages; Q
+//    64-byte swizzle (36 KB, two TMA requests), and the ring holds four pages; Q
 //    takes TMEM columns 0..127 and 128..143; P tiles are [128 x 64] bytes with the
 //    64-byte swizzle (8 KB); a V tile is two [64 rows x 128 B] atoms (16 KB).
 template <bool kF8>
@@ -126,8 +126,9 @@ struct Geo {
   // 16-bit: an entry fills and drains as two parts with barriers of their own,
   // atoms 0..3 (A) and atoms 4..8 (B): the next page's A half loads while this
   // page's B half is still in use, and a page's MMAs start once A is in
-  static constexpr int kKParts = kF8 ? 1 : 2;
+  static constexpr int kKParts = 2;
   static constexpr int kKAtomsA = 4;
+  static constexpr int kKAtom = kF8 ? 4096 : kChunk;  // bytes of one [64 rows x 64 columns] atom
   static constexpr int kNStage = kF8 ? 4 : 2;         // superblock staging slots (score CTA)
   static constexpr int kPTile = kF8 ? 8192 : 16384;
   static constexpr int kVSlot = kF8 ? 2 * kChunk : 4 * kChunk;
@@ -513,10 +514,18 @@ __device__ void score_producer(const FwdArgs &a, const CUtensorMap *kmap, const 
       next_entry(slot);
       uint8_t *dst = smem + G::kOffK + slot * G::kKEntry;
       if constexpr (kIsF8<T>) {
+        // part A: atoms 0..3 (16 KB, the four-block map `kmap`), part B: atoms 4..8
+        // (20 KB, the five-block map `pemap`)
         if (!part_free(slot, 0)) return false;
         if (leader) {
-          mbar_arrive_expect_tx(&b->k_full[2 * slot], G::kKEntry);
+          mbar_arrive_expect_tx(&b->k_full[2 * slot], G::kKAtomsA * G::kKAtom);
           tma_load_4d(dst, kmap, &b->k_full[2 * slot], 0, j.pg.row0[p], 0, j.pg.page[p]);
+        }
+        if (!part_free(slot, 1)) return false;
+        if (leader) {
+          mbar_arrive_expect_tx(&b->k_full[2 * slot + 1], (9 - G::kKAtomsA) * G::kKAtom);
+          tma_load_4d(dst + G::kKAtomsA * G::kKAtom, pemap, &b->k_full[2 * slot + 1], 0, j.pg.row0[p],
+                      G::kKAtomsA, j.pg.page[p]);
         }
       } else {
         // part A: latent atoms 0..3 (the four-block map); part B: atoms 4..8, as
@@ -643,16 +652,27 @@ __device__ void score_mma(const FwdArgs &a, uint8_t *smem, const Ctx &c, int par
       tc_fence_after();
       const uint64_t bd = kdesc + (uint64_t)(slot * (G::kKEntry >> 4));
       if constexpr (kIsF8<T>) {
+        // nine [64 x 64 B] atoms, 4 KB apart, two K = 32 steps each (Q's TMEM
+        // columns run on through the RoPE part, 16 per atom): part A, its
+        // release, then part B
         if (leader) {
-          // nine [64 x 64 B] atoms, 4 KB apart, two K = 32 steps each; Q's TMEM
-          // columns run on through the RoPE part (16 per atom)
 #pragma unroll
-          for (int blk = 0; blk < 9; ++blk)
+          for (int blk = 0; blk < G::kKAtomsA; ++blk)
 #pragma unroll
             for (int k = 0; k < 2; ++k)
               mma_ts_t<T>(tS, tQ + 16 * blk + 8 * k, bd + (uint64_t)(blk * (4096 >> 4) + 2 * k), idesc,
                           (blk | k) != 0);
           mma_commit_addr(kempty + 16 * slot);
+        }
+        if (!wait_addr<false>(c, kfull + 16 * slot + 8, phase, W_K_FULL)) return;
+        tc_fence_after();
+        if (leader) {
+#pragma unroll
+          for (int blk = G::kKAtomsA; blk < 9; ++blk)
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+              mma_ts_t<T>(tS, tQ + 16 * blk + 8 * k, bd + (uint64_t)(blk * (4096 >> 4) + 2 * k), idesc, 1);
+          mma_commit_addr(kempty + 16 * slot + 8);
         }
       } else {
         // part A (atoms 0..3), its release, then part B (atoms 4..8; the ninth is
@@ -1563,16 +1583,18 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t s) {
   cudaError_t e;
   if constexpr (kIsF8<T>) {
     // e4m3, RoPE columns inside the rows (the host rejects separate tensors).
-    // K: one box per page of nine [64 rows x 64 B] blocks, 64-byte swizzle.  V: the
+    // K: a page of nine [64 rows x 64 B] blocks, 64-byte swizzle, in two boxes
+    // (blocks 0..3 and 4..8).  V: the
     // first four 128-byte blocks, two per box (one O half of one page).  Q as
     // [b][h][576 B], boxes of 128 heads x 128 B; the RoPE box starts at column 512
     // and reads zeros past column 575.
-    e = make_block_map<T>(&kmap, a.kv, 64, 9, 9, CU_TENSOR_MAP_SWIZZLE_64B, a);
+    e = make_block_map<T>(&kmap, a.kv, 64, 9, GeoOf<T>::kKAtomsA, CU_TENSOR_MAP_SWIZZLE_64B, a);
+    if (e == cudaSuccess)
+      e = make_block_map<T>(&pemap, a.kv, 64, 9, 9 - GeoOf<T>::kKAtomsA, CU_TENSOR_MAP_SWIZZLE_64B, a);
     if (e == cudaSuccess) e = make_block_map<T>(&map4, a.kv, 128, 4, 2, CU_TENSOR_MAP_SWIZZLE_128B, a);
     if (e == cudaSuccess)
       e = make_map<T>(&qmap, a.q, MLA_HEAD_DIM, a.h, a.b, a.q_head_stride, a.q_batch_stride, 128, 128);
     qpemap = qmap;
-    pemap = kmap;  // unused
   } else {
     // K: a page in two parts, latent blocks 0..3 (the V map's box) and blocks 4..8
     // of the 576-column rows (five blocks), or, with K_pe separate, latent blocks
