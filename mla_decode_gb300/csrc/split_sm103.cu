@@ -123,9 +123,9 @@ template <bool kF8>
 struct Geo {
   static constexpr int kKEntry = kF8 ? 9 * 4096 : 9 * kChunk;
   static constexpr int kNK = kF8 ? 4 : 2;             // K ring entries, one page each
-  // 16-bit: an entry fills and drains as two parts with barriers of their own,
-  // atoms 0..3 (A) and atoms 4..8 (B): the next page's A half loads while this
-  // page's B half is still in use, and a page's MMAs start once A is in
+  // an entry fills and drains as two parts with barriers of their own, atoms 0..3
+  // (A) and atoms 4..8 (B): the next page's A half loads while this page's B
+  // half is still in use, and a page's MMAs start once A is in
   static constexpr int kKParts = 2;
   static constexpr int kKAtomsA = 4;
   static constexpr int kKAtom = kF8 ? 4096 : kChunk;  // bytes of one [64 rows x 64 columns] atom
@@ -431,13 +431,13 @@ __device__ __forceinline__ void issue_job(const FwdArgs &a, SbWalk &w, SbJob &j)
 // ------------------------------------------------------------------------------ score CTA
 
 // K producer.  A 64-token page of K lands as nine swizzled [64 rows x 64 columns]
-// atoms back to back (72 KB, one ring entry), in large 4-D TMA requests: a
-// request carries a fixed cost of a few hundred nanoseconds, so one SM streams
-// whole pages at 80-90 GB/s where [64 x 64] boxes (8 KB) reach about 24.  e4m3:
-// one request per page (36 KB).  16-bit: two, atoms 0..3 and atoms 4..8 (with
-// Q_pe / K_pe separate, latent atoms 4..7 plus the K_pe box), each part with its
-// own barriers, so the next page's first part streams in while this page's
-// second part is still being multiplied.  At a segment start the ring first carries
+// atoms back to back (72 KB, or 36 KB in e4m3: one ring entry), in large 4-D TMA
+// requests: a request carries a fixed cost of a few hundred nanoseconds, so one
+// SM streams whole pages at 80-90 GB/s where [64 x 64] boxes (8 KB) reach about
+// 24.  Two requests per page, atoms 0..3 and atoms 4..8 (with Q_pe / K_pe
+// separate, latent atoms 4..7 plus the K_pe box), each part with its own
+// barriers, so the next page's first part streams in while this page's second
+// part is still being multiplied.  At a segment start the ring first carries
 // that sequence's Q, which the MMA warp moves into TMEM: the 512 latent columns
 // as eight [128 heads x 64] boxes, four per entry, then the 64 RoPE columns.
 // Heads past h read as zeros.  The part's first segment starts from an empty
