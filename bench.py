@@ -2,7 +2,8 @@
 """MLA decode benchmark on GB300: one JSON line on rank 0.
 
 A step is one pass of the whole decode hot path (scheduler metadata, split
-kernel, combine kernel) over one batch of the chosen synthetic workload
+kernel, combine: its own kernel, or the split kernel's fused phase when the
+schedule splits no sequence) over one batch of the chosen synthetic workload
 (default: paged bf16, b=64, h=128, cache 4096, 64-token pages, shuffled block
 table).  Inputs are resident in HBM; the step rotates over several input sets
 whose KV caches are each larger than the 129 MB L2.  `value` is TFLOP/s with
@@ -54,9 +55,12 @@ def parse_args():
     ap.add_argument("--layout", choices=["fused", "split"], default="fused",
                     help="fused: 576-column q / kv_cache rows; split: Q / Q_pe and KV / K_pe "
                          "as separate tensors")
-    ap.add_argument("--combine", choices=["fused", "kernel"], default="kernel",
+    ap.add_argument("--combine", choices=["auto", "fused", "kernel"], default="auto",
                     help="fused: the split kernel combines the sequences it split (grid "
-                         "barrier); kernel: a separate combine kernel after it")
+                         "barrier); kernel: a separate combine kernel after it; auto: "
+                         "fused when the schedule splits no sequence (no combine then "
+                         "runs at all), else the combine kernel, decided once from the "
+                         "batch's metadata before anything is timed")
     return ap.parse_args()
 
 
@@ -367,6 +371,12 @@ def run_ours(args):
     parts, stride = mla.mla_metadata_shape(w.batch, w.rows, num_sm)
     meta = torch.empty((parts, stride), dtype=torch.int32, device=dev)
     nsplit = torch.empty((w.batch + 1,), dtype=torch.int32, device=dev)
+    combine = args.combine
+    if combine == "auto":
+        # every input set shares the batch's lengths, so one schedule decides for all
+        mla.prepare_metadata(base["cache_seqlens"], w.heads, num_sm, meta, nsplit,
+                             seqlen_q=w.seqlen_q)()
+        combine = "fused" if int(nsplit[-1]) == w.batch else "kernel"
     ws = torch.empty((mla.mla_workspace_size(w.batch, w.rows, parts),), dtype=torch.uint8,
                      device=dev)
     out = torch.empty((w.batch, w.seqlen_q, w.heads, 512), dtype=mla.out_dtype(w.torch_dtype),
@@ -376,7 +386,7 @@ def run_ours(args):
     calls = [mla.prepare_decode(s["q"], s["kv_cache"], s["block_table"], s["cache_seqlens"],
                                 w.softmax_scale, meta, nsplit, out, lse, ws, q_pe=s["q_pe"],
                                 k_pe=s["k_pe"], is_causal=w.causal, **input_scales(s),
-                                fused_combine=args.combine == "fused")
+                                fused_combine=combine == "fused")
              for s in sets]
     metas = [mla.prepare_metadata(s["cache_seqlens"], w.heads, num_sm, meta, nsplit,
                                   seqlen_q=w.seqlen_q) for s in sets]
@@ -437,7 +447,7 @@ def run_ours(args):
                                   dbuf["cache_seqlens"], w.softmax_scale, meta, nsplit, out, lse,
                                   ws, q_pe=dbuf.get("q_pe"), k_pe=dbuf.get("k_pe"),
                                   is_causal=w.causal, **input_scales(base),
-                                  fused_combine=args.combine == "fused")
+                                  fused_combine=combine == "fused")
     e2e_meta = mla.prepare_metadata(dbuf["cache_seqlens"], w.heads, num_sm, meta, nsplit,
                                     seqlen_q=w.seqlen_q)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
@@ -505,14 +515,15 @@ def run_ours(args):
                    "l2": f"{len(sets)} rotating input sets, KV "
                          f"{w.total_tokens * 576 * w.elem_bytes / 1e6:.0f} MB each (> 129 MB L2)",
                    "parallelism": f"replicas x{world}", "num_sm_parts": parts,
-                   "layout": args.layout, "combine": args.combine},
+                   "layout": args.layout, "combine": combine,
+                   "combine_choice": args.combine},
         "effective_hbm_gbs": world * nbytes / (ms * 1e-3) / 1e9,
         "roofline": roofline,
         "e2e": {"value": job_tflops(world, flops, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
                 "ms_per_step": e2e_ms},
         # metadata, split and (unless fused) combine kernels per step
-        "gpu_launches": (2 if args.combine == "fused" else 3) * K,
+        "gpu_launches": (2 if combine == "fused" else 3) * K,
         "clocks": clk,
         "kernel_source_hash": kernel_source_hash(),
     }

@@ -57,6 +57,18 @@ def test_fused_combine_varlen_full_size():
     assert int(ns[-1]) > w.batch
 
 
+def test_fused_combine_paged_full_size():
+    # the paged batch (64 x 4096 tokens, 76 SM pairs) in the mode the benchmark picks
+    # for it: the schedule splits no sequence, so no combine runs; every sequence and
+    # head against the oracle, and bit-identical to the combine-kernel mode
+    w = workloads.get("paged")
+    stats, out, lse, meta, ns, inputs = P.check_workload(w, fused_combine=True)
+    assert int(ns[-1]) == w.batch
+    out_k, lse_k, *_ = P.run_gpu(inputs, w.heads, w.softmax_scale, fused_combine=False)
+    assert torch.equal(out.view(torch.int16), out_k.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse_k.view(torch.int32))
+
+
 def test_fused_combine_garbage_workspace_and_graph_replays():
     import mla_decode_gb300 as mla
     w = _uneven("bf16", 321)
