@@ -53,6 +53,9 @@ extern "C" {
 /* Cost of one segment (a part's share of one sequence), in 64-token blocks, by
  * which the scheduler chooses how many parts to use. */
 #define MLA_SCHED_SEGMENT_COST 16
+/* Cost, in 64-token blocks, that the scheduler adds to a part count whose
+ * partition splits some sequence: the combine pass that such a schedule needs. */
+#define MLA_SCHED_SPLIT_COST 10
 /* Largest num_sm the scheduler accepts. */
 #define MLA_MAX_NUM_SM 2046
 
@@ -275,8 +278,10 @@ int mla_metadata_shape(int b, int h, int num_sm, int *num_sm_parts, int *meta_st
  * MLA_SCHED_FIXED_COST + ceil(L_i/64) blocks; with P parts, part k starts at
  * cost position floor(k*TOTAL/P).  P is chosen from ceil(num_sm_parts / 2) to
  * num_sm_parts: part k of P costs MLA_SCHED_SEGMENT_COST per segment it holds
- * (a sequence it touches) plus one per block, and the P whose most expensive
- * part is cheapest is used (the larger on a tie).  Parts P..num_sm_parts-1 are
+ * (a sequence it touches) plus one per block; P scores its most expensive part,
+ * plus MLA_SCHED_SPLIT_COST when some cut falls inside a sequence (the schedule
+ * then splits that sequence), and the lowest score is used (the larger P on a
+ * tie).  Parts P..num_sm_parts-1 are
  * empty: {b, 0, b, 0, num_splits[b], 0, 0, 0}.  Deterministic; the decode
  * result does not depend on it beyond rounding.  num_sm <= MLA_MAX_NUM_SM.
  */

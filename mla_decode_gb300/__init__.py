@@ -20,7 +20,7 @@ __all__ = [
     "mla_metadata_shape", "mla_get_metadata", "mla_workspace_size", "mla_decode_fwd",
     "mla_decode_fwd_timed", "prepare_decode", "DecodeCall", "prepare_metadata", "MetadataCall",
     "mla_get_device_error", "mla_test_forced_timeout", "library_path", "HEAD_DIM", "HEAD_DIM_V", "ROPE_DIM", "BLOCK_N",
-    "META_STRIDE", "SCHED_FIXED_COST", "SCHED_SEGMENT_COST", "MAX_NUM_SM", "out_dtype",
+    "META_STRIDE", "SCHED_FIXED_COST", "SCHED_SEGMENT_COST", "SCHED_SPLIT_COST", "MAX_NUM_SM", "out_dtype",
 ]
 
 HEAD_DIM = 576
@@ -31,6 +31,7 @@ BLOCK_N = 64
 META_STRIDE = 8
 SCHED_FIXED_COST = 5
 SCHED_SEGMENT_COST = 16
+SCHED_SPLIT_COST = 10
 MAX_NUM_SM = 2046
 STATIC_WORKSPACE_BYTES = 64 << 20
 _DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1, torch.float8_e4m3fn: 2}

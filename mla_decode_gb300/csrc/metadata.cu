@@ -17,10 +17,12 @@
 // ceil(P_max / 2), the first seven that divide b or are a multiple of b (on a
 // batch of equal sequences, the counts whose cuts fall on sequence boundaries or
 // split every sequence alike).  Part k of P costs G per segment it holds plus one
-// per block, and the P whose most expensive part is cheapest wins (the larger P
-// on a tie).  A segment costs more to run than F suggests (query load, pipeline
-// fill and drain, output), so on a batch of equal sequences one part per
-// sequence can beat more, split, parts.  Parts P..P_max-1 are left empty.
+// per block; P scores its most expensive part, plus S when it splits some
+// sequence (a partition with an interior cut needs the combine pass), and the
+// lowest score wins (the larger P on a tie).  A segment costs more to run than F
+// suggests (query load, pipeline fill and drain, output), so on a batch of equal
+// sequences one part per sequence can beat more, split, parts.  Parts
+// P..P_max-1 are left empty.
 //
 // One CTA; block scans in shared memory, no serial pass over the batch.
 #include <stdint.h>
@@ -111,7 +113,7 @@ __device__ void cut_of(int64_t x, const int64_t *chunk_start, int nchunks, int p
 
 __global__ void __launch_bounds__(kMetaThreads)
 metadata_kernel(const int32_t *__restrict__ seqlens, int b, int max_parts, int fixed, int seg_cost,
-                int32_t *__restrict__ meta, int32_t *__restrict__ num_splits) {
+                int split_cost, int32_t *__restrict__ meta, int32_t *__restrict__ num_splits) {
   extern __shared__ int32_t sh[];
   int32_t *cut_seq = sh;                        // [max_parts + 1]
   int32_t *cut_blk = cut_seq + max_parts + 1;   // [max_parts + 1]
@@ -120,6 +122,7 @@ metadata_kernel(const int32_t *__restrict__ seqlens, int b, int max_parts, int f
   __shared__ int64_t chunk_start[kMetaThreads];
   __shared__ int64_t warp_sums[kMetaWarps];
   __shared__ unsigned int worst[kMaxCand];  // per candidate part count (saturated at 2^31 - 1)
+  __shared__ unsigned int splits[kMaxCand];  // per candidate: some cut falls inside a sequence
   __shared__ int cand[kMaxCand], ncand_sh, chosen;
   const int tid = threadIdx.x;
   // launched with programmatic stream serialisation: cache_seqlens may have been
@@ -158,7 +161,10 @@ metadata_kernel(const int32_t *__restrict__ seqlens, int b, int max_parts, int f
     }
     if (tid == 0) ncand_sh = min(n, kMaxCand);
   }
-  if (tid < kMaxCand) worst[tid] = 0u;
+  if (tid < kMaxCand) {
+    worst[tid] = 0u;
+    splits[tid] = 0u;
+  }
   __syncthreads();
   const int ncand = ncand_sh;
   {
@@ -182,13 +188,15 @@ metadata_kernel(const int32_t *__restrict__ seqlens, int b, int max_parts, int f
       const int64_t segs = i0 < i1 ? (int64_t)(i1 - i0) + (b1 > 0 ? 1 : 0) : (b1 > b0 ? 1 : 0);
       const int64_t cst = segs * seg_cost + blocks;
       atomicMax(&worst[c], (unsigned int)(cst < 0x7fffffff ? cst : 0x7fffffff));
+      if (b0 > 0) atomicOr(&splits[c], 1u);  // cut k lies inside sequence i0's blocks
     }
   }
   __syncthreads();
   if (tid == 0) {
+    auto score = [&](int c) { return (int64_t)worst[c] + (splits[c] ? split_cost : 0); };
     int best = 0;  // candidates are in descending order: ties keep the larger count
     for (int c = 1; c < ncand; ++c)
-      if (worst[c] < worst[best]) best = c;
+      if (score(c) < score(best)) best = c;
     chosen = cand[best];
   }
   __syncthreads();
@@ -270,8 +278,8 @@ cudaError_t launch_metadata(const int32_t *seqlens, int b, int parts, int fixed,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, metadata_kernel, seqlens, b, parts, fixed, seg_cost, meta,
-                            num_splits);
+  return cudaLaunchKernelEx(&cfg, metadata_kernel, seqlens, b, parts, fixed, seg_cost,
+                            (int)MLA_SCHED_SPLIT_COST, meta, num_splits);
 }
 
 }  // namespace mla

@@ -36,8 +36,10 @@ A segment costs far more than the F of the cost axis suggests once it is run
 (loading the query, filling and draining the pipeline, writing its output), so
 cutting a sequence into more segments can lose more than the extra parts gain.
 `schedule_auto` therefore tries a few part counts, charges each part G per
-segment plus one per block, and keeps the count whose most expensive part is
-cheapest (the larger count on a tie).  The counts tried are P_max and, from
+segment plus one per block, scores a count by its most expensive part plus S
+when its partition splits some sequence (a split sequence needs the combine
+pass, a cost outside every part), and keeps the count with the lowest score
+(the larger count on a tie).  The counts tried are P_max and, from
 P_max - 1 down to ceil(P_max / 2), the first seven that divide b or are a
 multiple of it: on a batch of equal sequences those are the counts whose cuts
 fall on sequence boundaries or split every sequence alike.  Parts P..P_max-1
@@ -115,24 +117,28 @@ def candidate_parts(b, max_parts):
     return out
 
 
-def choose_parts(seqlens, max_parts, fixed_cost, segment_cost):
-    """Among candidate_parts(), the count whose partition has the cheapest most
-    expensive part; ties go to the larger count."""
+def choose_parts(seqlens, max_parts, fixed_cost, segment_cost, split_cost):
+    """Among candidate_parts(), the count with the lowest score: its most
+    expensive part, plus split_cost when some sequence gets more than one
+    segment; ties go to the larger count."""
+    b = len(seqlens)
     best, best_p = None, max_parts
-    for p in candidate_parts(len(seqlens), max_parts):
-        meta, _ = schedule(seqlens, p, fixed_cost)
+    for p in candidate_parts(b, max_parts):
+        meta, num_splits = schedule(seqlens, p, fixed_cost)
         t = max(part_costs(meta, seqlens, segment_cost))
+        if num_splits[b] > b:
+            t += split_cost
         if best is None or t < best:
             best, best_p = t, p
     return best_p
 
 
-def schedule_auto(seqlens, max_parts, fixed_cost, segment_cost):
+def schedule_auto(seqlens, max_parts, fixed_cost, segment_cost, split_cost):
     """schedule() with the part count chosen by choose_parts(); the metadata has
     max_parts rows, the ones past the chosen count empty.  Returns (metadata rows,
     num_splits prefix list, parts used)."""
     b = len(seqlens)
-    p = choose_parts(seqlens, max_parts, fixed_cost, segment_cost)
+    p = choose_parts(seqlens, max_parts, fixed_cost, segment_cost, split_cost)
     meta, num_splits = schedule(seqlens, p, fixed_cost)
     meta = meta + [[b, 0, b, 0, num_splits[b], 0, 0, 0] for _ in range(max_parts - p)]
     return meta, num_splits, p

@@ -71,9 +71,29 @@ def test_metadata_bit_exact(seed):
     meta, ns = mla.mla_get_metadata(torch.from_numpy(lens).cuda(), h, num_sm)
     parts, _ = mla.mla_metadata_shape(b, h, num_sm)
     ref_meta, ref_ns, _ = sch.schedule_auto([int(x) for x in lens], parts, mla.SCHED_FIXED_COST,
-                                            mla.SCHED_SEGMENT_COST)
+                                            mla.SCHED_SEGMENT_COST, mla.SCHED_SPLIT_COST)
     assert meta.cpu().tolist() == ref_meta
     assert ns.cpu().tolist() == ref_ns
+
+
+@pytest.mark.parametrize("b,L,h,num_sm", [(128, 4096, 128, 152), (128, 8192, 128, 152),
+                                          (64, 4096, 128, 152), (132, 8192, 128, 152),
+                                          (128, 2048, 128, 152), (64, 4096, 256, 152),
+                                          (96, 6000, 128, 152), (120, 4096, 16, 100)])
+def test_metadata_bit_exact_equal_batches(b, L, h, num_sm):
+    # batches of equal sequences, where the split cost decides between part counts
+    # whose most expensive parts are close
+    import mla_decode_gb300 as mla
+    lens = np.full(b, L, dtype=np.int32)
+    meta, ns = mla.mla_get_metadata(torch.from_numpy(lens).cuda(), h, num_sm)
+    parts, _ = mla.mla_metadata_shape(b, h, num_sm)
+    ref_meta, ref_ns, p = sch.schedule_auto([L] * b, parts, mla.SCHED_FIXED_COST,
+                                            mla.SCHED_SEGMENT_COST, mla.SCHED_SPLIT_COST)
+    assert meta.cpu().tolist() == ref_meta
+    assert ns.cpu().tolist() == ref_ns
+    if (b, L, h) == (128, 4096, 128):  # the case the split cost moves to whole sequences
+        assert p == 64 and ref_ns[-1] == b
+        assert sch.choose_parts([L] * b, parts, mla.SCHED_FIXED_COST, mla.SCHED_SEGMENT_COST, 0) == 76
 
 
 def test_out_of_range_page_is_reported_and_gpu_stays_usable():

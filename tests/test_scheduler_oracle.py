@@ -111,10 +111,20 @@ def test_candidate_parts():
     assert sch.candidate_parts(5, 10) == [10, 5]
 
 
+def splits_any_sequence(lens, parts):
+    """Brute force: some sequence is touched by more than one part."""
+    touched = [0] * len(lens)
+    for row in sch.schedule(lens, parts, FIXED)[0]:
+        for (i, _, _, _) in sch.segments_of_part(row, lens):
+            touched[i] += 1
+    return any(t > 1 for t in touched)
+
+
 @pytest.mark.parametrize("seed", range(25))
-def test_choose_parts_is_the_cheapest_worst_part(seed):
-    """Brute force over the candidate counts: the chosen one has the smallest most
-    expensive part, and no larger candidate ties with it."""
+def test_choose_parts_is_the_cheapest_score(seed):
+    """Brute force over the candidate counts: the chosen one has the lowest score
+    (most expensive part, plus S if some sequence is split, counted by walking
+    the parts), and no larger candidate ties with it."""
     rng = np.random.default_rng(1000 + seed)
     b = int(rng.integers(1, 120))
     lens = [int(x) for x in rng.integers(0, 9000, size=b)]
@@ -122,21 +132,38 @@ def test_choose_parts_is_the_cheapest_worst_part(seed):
         lens = [int(rng.integers(1, 9000))] * b       # equal sequences
     max_parts = int(rng.integers(1, 90))
     G = int(rng.choice([0, 4, 16, 40]))
-    p = sch.choose_parts(lens, max_parts, FIXED, G)
+    S = int(rng.choice([0, 10, 100]))
+    p = sch.choose_parts(lens, max_parts, FIXED, G, S)
     cands = sch.candidate_parts(b, max_parts)
     assert p in cands and (max_parts + 1) // 2 <= p <= max_parts
-    worst = {q: max(sch.part_costs(sch.schedule(lens, q, FIXED)[0], lens, G)) for q in cands}
-    assert worst[p] == min(worst.values())
-    assert all(worst[q] > worst[p] for q in cands if q > p)
+    score = {q: max(sch.part_costs(sch.schedule(lens, q, FIXED)[0], lens, G))
+             + (S if splits_any_sequence(lens, q) else 0) for q in cands}
+    assert score[p] == min(score.values())
+    assert all(score[q] > score[p] for q in cands if q > p)
+
+
+def test_split_cost_decides_only_close_calls():
+    # 128 sequences of 64 blocks on up to 76 parts: 76 parts (most expensive part
+    # 155, 68 sequences split) against 64 parts of two whole sequences (160): the
+    # combine pass of the split schedule tips it to 64
+    lens = [4096] * 128
+    assert sch.choose_parts(lens, 76, FIXED, 16, 0) == 76
+    assert sch.choose_parts(lens, 76, FIXED, 16, 10) == 64
+    # 8192-token sequences: 262 against 288, far apart: still 76 parts
+    assert sch.choose_parts([8192] * 128, 76, FIXED, 16, 10) == 76
+    # a schedule that splits nothing pays no split cost: 64 equal sequences
+    assert sch.choose_parts([4096] * 64, 76, FIXED, 16, 10 ** 6) == 64
+    # every candidate splits (one sequence): the cost shifts all scores alike
+    assert sch.choose_parts([100000], 76, FIXED, 16, 10) == sch.choose_parts([100000], 76, FIXED, 16, 0)
 
 
 def test_equal_sequences_get_one_part_each_when_segments_are_dear():
     # 64 sequences of 64 blocks on up to 76 parts: 76 parts cut most sequences in
     # two (two segments in most parts); 64 parts give each part one whole sequence
     lens = [4096] * 64
-    assert sch.choose_parts(lens, 76, FIXED, 16) == 64
+    assert sch.choose_parts(lens, 76, FIXED, 16, 0) == 64
     # with free segments the largest count wins
-    assert sch.choose_parts(lens, 76, FIXED, 0) == 76
+    assert sch.choose_parts(lens, 76, FIXED, 0, 0) == 76
 
 
 @pytest.mark.parametrize("seed", range(10))
@@ -145,10 +172,22 @@ def test_schedule_auto_pads_with_empty_parts(seed):
     b = int(rng.integers(1, 100))
     lens = [int(x) for x in rng.integers(0, 20000, size=b)]
     max_parts = int(rng.integers(2, 80))
-    meta, ns, p = sch.schedule_auto(lens, max_parts, FIXED, 16)
+    meta, ns, p = sch.schedule_auto(lens, max_parts, FIXED, 16, 10)
     assert len(meta) == max_parts
     ref_meta, ref_ns = check_partition(lens, p, FIXED)
     assert meta[:p] == ref_meta and ns == ref_ns
     for row in meta[p:]:
         assert row == [b, 0, b, 0, ns[b], 0, 0, 0]
         assert sch.segments_of_part(row, lens) == []
+
+
+def test_binding_constants_match_the_header():
+    import os
+    import re
+    import mla_decode_gb300 as mla
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "include", "mla_decode.h")).read()
+    for name in ("SCHED_FIXED_COST", "SCHED_SEGMENT_COST", "SCHED_SPLIT_COST", "BLOCK_N",
+                 "META_STRIDE", "MAX_NUM_SM"):
+        m = re.search(r"#define MLA_%s (\d+)" % name, hdr)
+        assert m and int(m.group(1)) == getattr(mla, name), name
