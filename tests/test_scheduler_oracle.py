@@ -191,3 +191,26 @@ def test_binding_constants_match_the_header():
                  "META_STRIDE", "MAX_NUM_SM"):
         m = re.search(r"#define MLA_%s (\d+)" % name, hdr)
         assert m and int(m.group(1)) == getattr(mla, name), name
+
+
+# (part count, split sequences) the scheduler gives each named workload on one GB300
+# (152 SMs: 76 SM pairs, halved per extra 128-row tile); the measured tables and the
+# benchmark's combine choice (fused exactly when nothing is split) rest on these
+WORKLOAD_SCHEDULES = {
+    "tiny": (76, 6), "paged": (64, 0), "split": (76, 72), "paged_8k": (76, 72),
+    "varlen": (76, 75), "mqa": (76, 72), "mtp": (32, 0), "paged_fp8": (64, 0),
+    "tl_example": (76, 72), "tl_bench_1024": (64, 0), "tl_bench_2048": (64, 0),
+    "tl_bench_4096": (64, 0), "tl_bench_8192": (76, 72), "tl_bench_16384": (76, 72),
+    "tl_bench_32768": (76, 72),
+}
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOAD_SCHEDULES))
+def test_workload_schedules(name):
+    import mla_decode_gb300 as mla
+    import workloads
+    w = workloads.get(name)
+    max_parts = 76 // ((w.rows + 127) // 128)
+    meta, ns, p = sch.schedule_auto([int(x) for x in w.seqlens], max_parts, mla.SCHED_FIXED_COST,
+                                    mla.SCHED_SEGMENT_COST, mla.SCHED_SPLIT_COST)
+    assert (p, ns[-1] - w.batch) == WORKLOAD_SCHEDULES[name]
