@@ -123,3 +123,23 @@ def test_static_largest_batch_that_fits(mla):
     lens = tuple(int(x) for x in torch.randint(0, 700, (b,), generator=gen))
     w = workloads.custom(batch=b, heads=h, seqlens=lens, seed=3)
     assert _compare_two_calls(mla, w) == parts
+
+
+@pytest.mark.gpu
+def test_static_fused_combine(mla):
+    # the grid-synchronised combine in the static scratch: its barrier words sit in
+    # the scratch's tail and keep the previous call's tag, which every call retags;
+    # three calls in a row, each the same bits as the workspace entry's combine kernel
+    w = workloads.custom(batch=5, heads=128, seqlens=(4097, 1, 0, 2000, 640), seed=8)
+    inp = workloads.make_inputs(w, device="cuda")
+    meta, num_splits = mla.mla_get_metadata(inp["cache_seqlens"], w.heads, 20)
+    assert int(num_splits[-1]) > w.batch, "the case must split some sequence"
+    args = (inp["q"], inp["kv_cache"], inp["block_table"], inp["cache_seqlens"],
+            w.softmax_scale, meta, num_splits)
+    ref_out, ref_lse = mla.mla_decode_fwd(*args)
+    for call in range(3):
+        out, lse = mla.mla_decode_fwd_static(*args, fused_combine=True)
+        code, detail = mla.mla_get_device_error()
+        assert code == 0, f"call {call}: device error {code}, detail {detail}"
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16)), f"call {call}: out bits"
+        assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32)), f"call {call}: lse bits"
