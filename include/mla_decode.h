@@ -237,7 +237,12 @@ typedef struct mla_fwd_params {
    * workspace (mla_workspace_size) and need no initial value: each call tags
    * them with its own number, and the last CTA to leave the barrier resets
    * them for a replay of the same call (a captured CUDA graph).  After a call
-   * that reported MLA_ERR_DEVICE_TIMEOUT, re-capture such a graph. */
+   * that reported MLA_ERR_DEVICE_TIMEOUT, re-capture such a graph.  The barrier
+   * needs the whole grid resident at once: num_sm_parts * ceil(seqlen_q * h /
+   * 128) must not exceed half of mla_device_num_sm (the co-resident clusters),
+   * which metadata shaped for at most that num_sm satisfies; otherwise the call
+   * returns MLA_ERR_SHAPE before launching anything.  With other kernels on the
+   * device the barrier waits until the grid's last CTA has started. */
   int32_t fused_combine;
 } mla_fwd_params;
 

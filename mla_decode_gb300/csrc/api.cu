@@ -269,6 +269,14 @@ int resolve_args(const mla_fwd_params *p, FwdArgs &a) {
   a.err = err;
   a.forced_timeout = 0;
   a.fused_combine = p->fused_combine != 0;
+  if (a.fused_combine) {
+    // the grid barrier waits for every CTA: the grid must fit on the device at once
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+    const int r = mla_device_num_sm(dev, &n);
+    if (r != MLA_OK) return r;
+    if ((int64_t)p->num_sm_parts * head_tiles(rows) > n / 2) return MLA_ERR_SHAPE;
+  }
   a.token = next_token();
   {
     const size_t o = (size_t)a.max_splits * rows * MLA_HEAD_DIM_V * sizeof(float);

@@ -69,6 +69,49 @@ def test_fused_combine_paged_full_size():
     assert torch.equal(lse.view(torch.int32), lse_k.view(torch.int32))
 
 
+@pytest.mark.parametrize("num_sm", [8, 20, 152])
+def test_fused_combine_query_tokens_bitwise(num_sm):
+    # three causal query tokens: the grid combines s * h rows per sequence (token-major,
+    # two 128-row tiles), and rows that see none of a split's tokens drop that split
+    w = workloads.custom(3, 64, (129, 2000, 3), "bf16", seed=411, name="fused_qtok", seqlen_q=3,
+                         causal=True)
+    x = workloads.make_inputs(w, "cuda")
+    out_f, lse_f, meta, ns = P.run_gpu(x, w.heads, w.softmax_scale, num_sm=num_sm, is_causal=True,
+                                       fused_combine=True)
+    out_k, lse_k, *_ = P.run_gpu(x, w.heads, w.softmax_scale, num_sm=num_sm, is_causal=True)
+    assert int(ns[-1]) > w.batch, "the case must split some sequence"
+    assert torch.equal(out_f.view(torch.int16), out_k.view(torch.int16))
+    assert torch.equal(lse_f.view(torch.int32), lse_k.view(torch.int32))
+
+
+def test_fused_combine_rejects_a_grid_larger_than_the_device():
+    # metadata shaped for 1024 SMs asks for 256 parts x 2 row tiles: more clusters than
+    # the device holds at once, so the grid barrier could not pass; the call is refused
+    # on the host before any launch, and the same call without fusing runs
+    import mla_decode_gb300 as mla
+    w = workloads.custom(3, 64, (129, 2000, 3), "bf16", seed=412, name="fused_big", seqlen_q=3,
+                         causal=True)
+    x = workloads.make_inputs(w, "cuda")
+    meta, ns = mla.mla_get_metadata(x["cache_seqlens"], w.heads, 1024, seqlen_q=3)
+    assert meta.shape[0] * 2 > mla.mla_device_num_sm() // 2
+    args = (x["q"], x["kv_cache"], x["block_table"], x["cache_seqlens"], w.softmax_scale, meta, ns)
+    with pytest.raises(mla.MlaError):
+        mla.mla_decode_fwd(*args, is_causal=True, fused_combine=True)
+    mla.mla_decode_fwd(*args, is_causal=True)
+    torch.cuda.synchronize()
+    code, detail = mla.mla_get_device_error()
+    assert code == 0, f"device error {code} detail {detail}"
+
+
+def test_fused_combine_mtp_full_size():
+    # the two-token batch (64 x 4096 tokens, 256 rows) in the mode the benchmark picks
+    # for it: 32 parts of whole sequences, nothing to combine; every sequence and row
+    # against the oracle
+    w = workloads.get("mtp")
+    stats, out, lse, meta, ns, inputs = P.check_workload(w, fused_combine=True)
+    assert int(ns[-1]) == w.batch
+
+
 def test_fused_combine_garbage_workspace_and_graph_replays():
     import mla_decode_gb300 as mla
     w = _uneven("bf16", 321)
