@@ -34,7 +34,7 @@ METRIC = ("MLA decode TFLOPS and effective HBM GB/s on 1 GB300 (paged bf16), "
           "% of roofline")
 UNIT = "TFLOP/s"
 FALLBACK_HBM_GBS = 6800.0
-EVENT_EVERY = 5  # timed steps between two event-instrumented split launches
+EVENT_EVERY = 10  # timed steps between two event-instrumented split launches
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -284,6 +284,20 @@ def oracle_sample_time(w, target_seconds, seqs_max=64):
 
 # ------------------------------------------------------------------------------- arms
 
+def workload_config(w, args, world):
+    """The `config` object of both arms' lines: the workload and how it is fed, not how
+    this library launches it (that goes under `launch`)."""
+    kv_mb = w.total_tokens * 576 * w.elem_bytes / 1e6
+    copies = max(1, args.copies)
+    return {"workload": w.name, "batch": w.batch, "heads": w.heads, "seqlen_q": w.seqlen_q,
+            "causal": w.causal, "seqlen": int(w.seqlens[0]), "page_block_size": w.page_size,
+            "block_table": "seeded random permutation" if w.shuffle else "identity (pages in order)",
+            "softmax_scale": w.softmax_scale, "input_dtype": w.dtype, "layout": args.layout,
+            "l2": f"{copies} rotating input sets, KV {kv_mb:.0f} MB each "
+                  + ("(> 129 MB L2)" if kv_mb > 129 else "(within the 129 MB L2)"),
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -330,10 +344,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "heads": w.heads,
-                   "seqlen_q": w.seqlen_q, "causal": w.causal,
-                   "seqlen": int(w.seqlens[0]), "page_block_size": w.page_size,
-                   "input_dtype": w.dtype},
+        "config": workload_config(w, args, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -404,10 +415,11 @@ def run_ours(args):
 
     K = args.steps
     # the split kernel's duration: CUDA events recorded around it on a sample of the
-    # timed steps (every EVENT_EVERY-th).  An event between two kernels ends the
-    # programmatic overlap of the second one's launch with the first one's tail, so
-    # events on every step would add their cost to every step
-    timed = [i for i in range(K) if i % EVENT_EVERY == 0]
+    # timed steps, one in the middle of every EVENT_EVERY (steps 5, 15, ...; step 0 when
+    # K <= 5).  An event between two kernels ends the programmatic overlap of the second
+    # one's launch with the first one's tail, so events on every step would add their
+    # cost to every step
+    timed = [i for i in range(K) if i % EVENT_EVERY == EVENT_EVERY // 2] or [0]
     ev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for i in timed}
     for a, b in ev.values():  # materialise the raw events
@@ -508,15 +520,8 @@ def run_ours(args):
         "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "heads": w.heads,
-                   "seqlen_q": w.seqlen_q, "causal": w.causal,
-                   "seqlen": int(w.seqlens[0]), "page_block_size": w.page_size,
-                   "block_table": "seeded random permutation", "softmax_scale": w.softmax_scale,
-                   "l2": f"{len(sets)} rotating input sets, KV "
-                         f"{w.total_tokens * 576 * w.elem_bytes / 1e6:.0f} MB each (> 129 MB L2)",
-                   "parallelism": f"replicas x{world}", "num_sm_parts": parts,
-                   "layout": args.layout, "combine": combine,
-                   "combine_choice": args.combine},
+        "config": workload_config(w, args, world),
+        "launch": {"num_sm_parts": parts, "combine": combine, "combine_choice": args.combine},
         "effective_hbm_gbs": world * nbytes / (ms * 1e-3) / 1e9,
         "roofline": roofline,
         "e2e": {"value": job_tflops(world, flops, e2e_ms), "unit": UNIT,
